@@ -1,0 +1,202 @@
+"""CPU oracle for the FP8 block-scaled GEMM and the MXFP8 GEMM.
+
+TEST INFRASTRUCTURE ONLY: the tests, ``__graft_entry__.smoke()`` and the
+benchmark's CPU-baseline leg use it; the product path never does. It shares no
+code with the CUDA library.
+
+``fp8bs_oracle.c`` holds the fp64 definition (dequantise -> naive triple loop ->
+one bf16 rounding; skill card "FlyDSL fp8 blockscale GEMM", section
+"Procedure" step 1, and PR "1x32 ue8m0 (MXFP8) 8-wave FlyDSL GEMM for gfx950",
+section "Correctness"). This module loads it with ctypes and adds a
+pure-Python exact evaluation with ``fractions.Fraction`` for tiny inputs,
+which the tests use as brute force.
+
+Every function here is pinned by tests/test_oracle_pins.py; nothing is
+"parity unpinned".
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+from fractions import Fraction
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "fp8bs_oracle.c")
+_LIB = os.path.join(_HERE, "liboracle.so")
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle with gcc (-O2, no fast-math, OpenMP)."""
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + f".tmp{os.getpid()}"
+        subprocess.check_call(["gcc", "-O2", "-std=c11", "-fopenmp", "-fPIC", "-shared",
+                               "-o", tmp, _SRC, "-lm"])
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        build()
+        lib = ctypes.CDLL(_LIB)
+        lib.oracle_e4m3_decode.restype = ctypes.c_double
+        lib.oracle_e4m3_decode.argtypes = [ctypes.c_uint8]
+        lib.oracle_ue8m0_decode.restype = ctypes.c_double
+        lib.oracle_ue8m0_decode.argtypes = [ctypes.c_uint8]
+        lib.oracle_bf16_rne.restype = ctypes.c_uint16
+        lib.oracle_bf16_rne.argtypes = [ctypes.c_double]
+        lib.oracle_max_threads.restype = ctypes.c_int
+        p = ctypes.c_void_p
+        i = ctypes.c_int
+        for name in ("oracle_blockscale", "oracle_blockscale_blockpartial", "oracle_mxfp8"):
+            f = getattr(lib, name)
+            f.restype = ctypes.c_int
+            f.argtypes = [p, p, p, p, i, i, i, i, i, p, p]
+        _lib = lib
+    return _lib
+
+
+def _ptr(a):
+    return a.ctypes.data_as(ctypes.c_void_p) if a is not None else None
+
+
+def e4m3_decode(code: int) -> float:
+    return _load().oracle_e4m3_decode(int(code))
+
+
+def ue8m0_decode(code: int) -> float:
+    return _load().oracle_ue8m0_decode(int(code))
+
+
+def bf16_rne(x: float) -> int:
+    return int(_load().oracle_bf16_rne(float(x)))
+
+
+def max_threads() -> int:
+    return int(_load().oracle_max_threads())
+
+
+def _run(name, A, s_a, B, s_b, M, N, K, rows, want_exact):
+    lib = _load()
+    r0, r1 = (0, M) if rows is None else rows
+    A = np.ascontiguousarray(A, dtype=np.uint8)
+    B = np.ascontiguousarray(B, dtype=np.uint8)
+    C = np.empty((r1 - r0, N), dtype=np.uint16)
+    Ce = np.empty((r1 - r0, N), dtype=np.float64) if want_exact else None
+    rc = getattr(lib, name)(_ptr(A), _ptr(s_a), _ptr(B), _ptr(s_b), M, N, K, r0, r1, _ptr(C), _ptr(Ce))
+    if rc != 0:
+        raise RuntimeError(f"{name} failed ({rc})")
+    return (C, Ce) if want_exact else C
+
+
+def blockscale(A, a_scale, B, b_scale, rows=None, exact=False):
+    """bf16 bits (uint16 [rows, N]) of the blockscale GEMM; a_scale is logical [M, K/128]."""
+    M, K = A.shape
+    N = B.shape[0]
+    sa = np.ascontiguousarray(a_scale, dtype=np.float32)
+    sb = np.ascontiguousarray(b_scale, dtype=np.float32)
+    assert sa.shape == (M, K // 128) and sb.shape == ((N + 127) // 128, K // 128)
+    return _run("oracle_blockscale", A, sa, B, sb, M, N, K, rows, exact)
+
+
+def blockscale_blockpartial(A, a_scale, B, b_scale, rows=None, exact=False):
+    M, K = A.shape
+    N = B.shape[0]
+    sa = np.ascontiguousarray(a_scale, dtype=np.float32)
+    sb = np.ascontiguousarray(b_scale, dtype=np.float32)
+    return _run("oracle_blockscale_blockpartial", A, sa, B, sb, M, N, K, rows, exact)
+
+
+def mxfp8(A, a_e8m0, B, b_e8m0, rows=None, exact=False):
+    """bf16 bits (uint16 [rows, N]) of the MXFP8 GEMM; scales are ue8m0 bytes [rows, K/32]."""
+    M, K = A.shape
+    N = B.shape[0]
+    ea = np.ascontiguousarray(a_e8m0, dtype=np.uint8)
+    eb = np.ascontiguousarray(b_e8m0, dtype=np.uint8)
+    assert ea.shape == (M, K // 32) and eb.shape == (N, K // 32)
+    return _run("oracle_mxfp8", A, ea, B, eb, M, N, K, rows, exact)
+
+
+def bf16_bits_to_float(bits: np.ndarray) -> np.ndarray:
+    """uint16 bf16 bit patterns -> float32 values (exact widening)."""
+    return (np.asarray(bits, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32)
+
+
+# ---------------------------------------------------------------------------
+# Exact rational evaluation (brute force for tiny inputs).
+
+def e4m3_fraction(code: int) -> Fraction:
+    """E4M3FN code -> exact value as a Fraction (NaN code raises)."""
+    s, e, m = code >> 7, (code >> 3) & 0xF, code & 7
+    if e == 0xF and m == 7:
+        raise ValueError("NaN code")
+    v = Fraction(m, 512) if e == 0 else Fraction(8 + m, 8) * (Fraction(2) ** (e - 7))
+    return -v if s else v
+
+
+def fraction_to_bf16_bits(q: Fraction) -> int:
+    """Correctly rounded (nearest, ties to even) bf16 of an exact rational."""
+    if q == 0:
+        return 0
+    sign = 0x8000 if q < 0 else 0
+    a = abs(q)
+    e = a.numerator.bit_length() - a.denominator.bit_length()
+    while Fraction(2) ** e > a:
+        e -= 1
+    while Fraction(2) ** (e + 1) <= a:
+        e += 1
+    qexp = max(e, -126) - 7
+    scaled = a / (Fraction(2) ** qexp)
+    fl = scaled.numerator // scaled.denominator
+    rem = scaled - fl
+    if rem > Fraction(1, 2) or (rem == Fraction(1, 2) and fl % 2 == 1):
+        fl += 1
+    value = Fraction(fl) * (Fraction(2) ** qexp)
+    if value > Fraction(255) * Fraction(2) ** 120:
+        return sign | 0x7F80
+    bits = int(np.array([float(value)], dtype=np.float32).view(np.uint32)[0])
+    return sign | ((bits >> 16) & 0x7FFF)
+
+
+def exact_blockscale(A, a_scale, B, b_scale):
+    """Exact rational C (list of lists of Fraction) of the blockscale definition."""
+    M, K = A.shape
+    N = B.shape[0]
+    fa = [[e4m3_fraction(int(c)) for c in row] for row in A]
+    fb = [[e4m3_fraction(int(c)) for c in row] for row in B]
+    out = []
+    for m in range(M):
+        row = []
+        for n in range(N):
+            acc = Fraction(0)
+            for k in range(K):
+                sa = Fraction(float(a_scale[m, k // 128]))
+                sb = Fraction(float(b_scale[n // 128, k // 128]))
+                acc += (fa[m][k] * sa) * (fb[n][k] * sb)
+            row.append(acc)
+        out.append(row)
+    return out
+
+
+def exact_mxfp8(A, a_e8m0, B, b_e8m0):
+    M, K = A.shape
+    N = B.shape[0]
+    fa = [[e4m3_fraction(int(c)) for c in row] for row in A]
+    fb = [[e4m3_fraction(int(c)) for c in row] for row in B]
+    out = []
+    for m in range(M):
+        row = []
+        for n in range(N):
+            acc = Fraction(0)
+            for k in range(K):
+                sa = Fraction(2) ** (int(a_e8m0[m, k // 32]) - 127)
+                sb = Fraction(2) ** (int(b_e8m0[n, k // 32]) - 127)
+                acc += (fa[m][k] * sa) * (fb[n][k] * sb)
+            row.append(acc)
+        out.append(row)
+    return out
