@@ -1,0 +1,181 @@
+"""FP8 block-scaled GEMM and MXFP8 GEMM on GB300 (sm_103a).
+
+Thin ctypes binding over libfp8bs.so (include/fp8bs.h). Every step of the
+computation runs in the library's CUDA kernels; this module only checks
+tensors, marshals pointers and the current CUDA stream, and raises on a
+non-zero status. PyTorch provides device memory and streams.
+
+There is no CPU fallback: if the library is missing, importing the package
+raises ImportError with the build command.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIBRARY_PATH = os.path.join(_HERE, "libfp8bs.so")
+
+if not os.path.exists(LIBRARY_PATH):
+    raise ImportError(
+        f"{LIBRARY_PATH} is not built; run `python -c 'import __graft_entry__ as g; g.build()'` "
+        "or `python fp8_block_scaled_e4m3_gb300/_build.py` (needs nvcc for sm_103a)")
+
+_lib = ctypes.CDLL(LIBRARY_PATH)
+_p = ctypes.c_void_p
+_i = ctypes.c_int
+_i64 = ctypes.c_int64
+
+_SIGS = {
+    "fp8bs_gemm": (_i, [_p, _p, _p, _p, _p, _i, _i, _i, _p]),
+    "fp8mx_gemm": (_i, [_p, _p, _p, _p, _p, _i, _i, _i, _p]),
+    "fp8bs_a_scale_ld": (_i64, [_i]),
+    "fp8bs_a_scale_index": (_i64, [_i, _i, _i]),
+    "fp8bs_b_scale_index": (_i64, [_i, _i, _i]),
+    "fp8mx_scale_index": (_i64, [_i, _i, _i]),
+    "fp8mx_sf_atom_offset": (_i, [_i, _i]),
+    "fp8bs_pack_a_scale": (_i, [_p, _p, _i, _i, _p]),
+    "fp8bs_get_status": (_i, [_p]),
+    "fp8bs_status_string": (ctypes.c_char_p, [_i]),
+    "fp8bs_last_config_id": (_i, []),
+    "fp8bs_select_config": (_i, [_i, _i, _i, _i]),
+    "fp8mx_select_config": (_i, [_i, _i, _i, _i]),
+    "fp8bs_launches_per_call": (_i, []),
+    "fp8bs_set_wait_limit_ns": (None, [ctypes.c_uint64]),
+    "fp8bs_version": (ctypes.c_char_p, []),
+}
+for _name, (_res, _args) in _SIGS.items():
+    _f = getattr(_lib, _name)
+    _f.restype = _res
+    _f.argtypes = _args
+
+STATUS = {0: "FP8BS_OK", -1: "FP8BS_ERR_NULL", -2: "FP8BS_ERR_ALIGN", -3: "FP8BS_ERR_SHAPE",
+          -4: "FP8BS_ERR_UNSUPPORTED_DEVICE", -5: "FP8BS_ERR_LAUNCH", -6: "FP8BS_ERR_DEVICE_TIMEOUT",
+          -7: "FP8BS_ERR_CUDA"}
+
+
+class Fp8bsError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        msg = _lib.fp8bs_status_string(code).decode()
+        super().__init__(f"{where}: {STATUS.get(code, code)} ({msg})")
+
+
+def _check(rc: int, where: str) -> None:
+    if rc != 0:
+        raise Fp8bsError(rc, where)
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded libfp8bs.so (for the C-ABI tests and the benchmark)."""
+    return _lib
+
+
+def _torch():
+    import torch
+    return torch
+
+
+def _stream_ptr(stream):
+    torch = _torch()
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _fp8_ptr(t, name, shape):
+    torch = _torch()
+    if t.dtype not in (torch.float8_e4m3fn, torch.uint8):
+        raise TypeError(f"{name} must be float8_e4m3fn or uint8 E4M3 codes, got {t.dtype}")
+    return _dev_ptr(t, name, shape)
+
+
+def _dev_ptr(t, name, shape):
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def a_scale_ld(M: int) -> int:
+    return int(_lib.fp8bs_a_scale_ld(M))
+
+
+def gemm_blockscale(A, a_scale, B, b_scale, C=None, stream=None):
+    """C[M,N] bf16 = sum_kb (A.B^T)_kb * a_scale[m,kb] * b_scale[n//128,kb].
+
+    A: [M,K] E4M3; a_scale: fp32 [K/128, a_scale_ld(M)] K-block-major;
+    B: [N,K] E4M3; b_scale: fp32 [ceil(N/128), K/128]; C: optional bf16 [M,N] output.
+    """
+    torch = _torch()
+    M, K = A.shape
+    N = B.shape[0]
+    if C is None:
+        C = torch.empty((M, N), dtype=torch.bfloat16, device=A.device)
+    if a_scale.dtype != torch.float32 or b_scale.dtype != torch.float32 or C.dtype != torch.bfloat16:
+        raise TypeError("scales must be float32 and C bfloat16")
+    rc = _lib.fp8bs_gemm(_fp8_ptr(A, "A", (M, K)), _dev_ptr(a_scale, "a_scale", (K // 128, a_scale_ld(M))),
+                         _fp8_ptr(B, "B", (N, K)), _dev_ptr(b_scale, "b_scale", ((N + 127) // 128, K // 128)),
+                         _dev_ptr(C, "C", (M, N)), M, N, K, _stream_ptr(stream))
+    _check(rc, "fp8bs_gemm")
+    return C
+
+
+def gemm_mxfp8(A, a_e8m0, B, b_e8m0, C=None, stream=None):
+    """C[M,N] bf16 = sum_k A[m,k] 2^(a_e8m0[m,k/32]-127) B[n,k] 2^(b_e8m0[n,k/32]-127).
+
+    A: [M,K] E4M3; a_e8m0: uint8 [M, K/32]; B: [N,K] E4M3; b_e8m0: uint8 [N, K/32].
+    """
+    torch = _torch()
+    M, K = A.shape
+    N = B.shape[0]
+    if C is None:
+        C = torch.empty((M, N), dtype=torch.bfloat16, device=A.device)
+    if a_e8m0.dtype != torch.uint8 or b_e8m0.dtype != torch.uint8 or C.dtype != torch.bfloat16:
+        raise TypeError("ue8m0 scales must be uint8 and C bfloat16")
+    rc = _lib.fp8mx_gemm(_fp8_ptr(A, "A", (M, K)), _dev_ptr(a_e8m0, "a_e8m0", (M, K // 32)),
+                         _fp8_ptr(B, "B", (N, K)), _dev_ptr(b_e8m0, "b_e8m0", (N, K // 32)),
+                         _dev_ptr(C, "C", (M, N)), M, N, K, _stream_ptr(stream))
+    _check(rc, "fp8mx_gemm")
+    return C
+
+
+def pack_a_scale(a_scale_rowmajor, K: int, out=None, stream=None):
+    """Row-major logical a_scale [M, K/128] -> the K-block-major layout gemm_blockscale takes."""
+    torch = _torch()
+    M = a_scale_rowmajor.shape[0]
+    if out is None:
+        out = torch.empty((K // 128, a_scale_ld(M)), dtype=torch.float32, device=a_scale_rowmajor.device)
+    rc = _lib.fp8bs_pack_a_scale(_dev_ptr(a_scale_rowmajor, "a_scale", (M, K // 128)),
+                                 _dev_ptr(out, "out", (K // 128, a_scale_ld(M))), M, K, _stream_ptr(stream))
+    _check(rc, "fp8bs_pack_a_scale")
+    return out
+
+
+def get_status(stream=None) -> int:
+    """Synchronise the stream and return (and clear) the device status word."""
+    return int(_lib.fp8bs_get_status(_stream_ptr(stream)))
+
+
+def last_config_id() -> int:
+    return int(_lib.fp8bs_last_config_id())
+
+
+def select_config(kind: str, M: int, N: int, K: int, num_sms: int) -> int:
+    f = _lib.fp8bs_select_config if kind == "bs" else _lib.fp8mx_select_config
+    return int(f(M, N, K, num_sms))
+
+
+def decode_config(cid: int) -> dict:
+    return {"kind": {1: "blockscale", 2: "mxfp8"}.get(cid // 1000000, "?"), "block_n": (cid // 1000) % 1000,
+            "stages": (cid // 100) % 10, "raster": (cid // 10) % 10, "group": cid % 10}
+
+
+def set_wait_limit_ns(ns: int) -> None:
+    _lib.fp8bs_set_wait_limit_ns(int(ns))
+
+
+def version() -> str:
+    return _lib.fp8bs_version().decode()

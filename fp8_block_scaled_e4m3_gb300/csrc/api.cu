@@ -1,0 +1,354 @@
+// Host side of libfp8bs: argument checks, shape-class -> kernel configuration,
+// tensor-map encoding, launches, the per-device status word and the layout
+// helpers declared in include/fp8bs.h.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <mutex>
+#include <stdint.h>
+#include <string.h>
+
+#include "../../include/fp8bs.h"
+#include "common.cuh"
+
+namespace fp8bs {
+
+template <int BN, int STAGES>
+cudaError_t launch_blockscale(const CUtensorMap &, const CUtensorMap &, const CUtensorMap &, const CUtensorMap &,
+                              const GemmArgs &, int, cudaStream_t);
+template <int BN, int STAGES>
+cudaError_t launch_mxfp8(const CUtensorMap &, const CUtensorMap &, const CUtensorMap &, const GemmArgs &, int,
+                         cudaStream_t);
+
+namespace host {
+
+__device__ int g_status_word;   // per-device status written by the kernels
+
+constexpr int kMaxDevices = 64;
+constexpr unsigned long long kDefaultWaitLimitNs = 2000000000ull;
+
+struct DeviceState {
+    bool ready = false;
+    int status = FP8BS_OK;       // result of the set-up
+    int num_sms = 0;
+    int *status_ptr = nullptr;   // device address of g_status_word
+};
+
+std::mutex g_mutex;
+DeviceState g_dev[kMaxDevices];
+std::atomic<unsigned long long> g_wait_limit_ns{kDefaultWaitLimitNs};
+thread_local int t_last_config = 0;
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn g_encode = nullptr;
+
+int ensure_device(int &dev, DeviceState *&st)
+{
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
+        return FP8BS_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_mutex);
+    st = &g_dev[dev];
+    if (st->ready)
+        return st->status;
+    st->ready = true;
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&st->num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return st->status = FP8BS_ERR_CUDA;
+    if (major != 10 || minor != 3)
+        return st->status = FP8BS_ERR_UNSUPPORTED_DEVICE;
+    if (cudaGetSymbolAddress(reinterpret_cast<void **>(&st->status_ptr), g_status_word) != cudaSuccess)
+        return st->status = FP8BS_ERR_CUDA;
+    if (!g_encode) {
+        cudaDriverEntryPointQueryResult q;
+        void *fn = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess || !fn)
+            return st->status = FP8BS_ERR_CUDA;
+        g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+    }
+    return st->status = FP8BS_OK;
+}
+
+// 2-D row-major tensor [rows][cols] of `esize`-byte elements, box [box_rows][box_cols].
+bool encode_2d(CUtensorMap *tm, CUtensorMapDataType dt, int esize, const void *base, uint64_t cols, uint64_t rows,
+               uint64_t row_stride_bytes, uint32_t box_cols, uint32_t box_rows, CUtensorMapSwizzle swz)
+{
+    cuuint64_t dims[2] = {cols, rows};
+    cuuint64_t strides[1] = {row_stride_bytes};
+    cuuint32_t box[2] = {box_cols, box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    (void)esize;
+    return g_encode(tm, dt, 2, const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+int check_shape(int M, int N, int K)
+{
+    if (M < 0 || N < 8 || (N % 8) != 0 || K < 128 || (K % 128) != 0 || K > (1 << 20))
+        return FP8BS_ERR_SHAPE;
+    return FP8BS_OK;
+}
+
+// Shape class -> configuration. Returns the config id (see fp8bs.h) and fills
+// tile width, stages and raster.
+struct Config {
+    int block_n, stages, raster, group;
+};
+
+int config_id(int kind, const Config &c)
+{
+    const int gcode = c.group >= 9 ? 9 : c.group;
+    return kind * 1000000 + c.block_n * 1000 + c.stages * 100 + c.raster * 10 + gcode;
+}
+
+Config choose_config(int kind, int M, int N, int K, int num_sms)
+{
+    (void)kind;
+    (void)K;
+    Config c;
+    // Wide tiles (128 x 256) keep shared-memory operand traffic at 96 B/clk per
+    // SM; the narrow tile only when the wide one leaves most SMs idle.
+    const long tiles256 = (long)((M + 127) / 128) * ((N + 255) / 256);
+    if (tiles256 * 2 <= num_sms) {
+        c.block_n = 128;
+        c.stages = 6;
+    } else {
+        c.block_n = 256;
+        c.stages = 4;
+    }
+    // Stream the larger operand once past a resident set of panels of the smaller one.
+    c.raster = ((long)M >= (long)N) ? 1 : 0;
+    c.group = 1;
+    return c;
+}
+
+} // namespace host
+} // namespace fp8bs
+
+using namespace fp8bs;
+using namespace fp8bs::host;
+
+extern "C" {
+
+int fp8bs_gemm(const void *A, const float *a_scale, const void *B, const float *b_scale, void *C, int M, int N,
+               int K, void *stream)
+{
+    int rc = check_shape(M, N, K);
+    if (rc)
+        return rc;
+    if (M == 0)
+        return FP8BS_OK;
+    if (!A || !a_scale || !B || !b_scale || !C)
+        return FP8BS_ERR_NULL;
+    if (!aligned(A, 16) || !aligned(a_scale, 16) || !aligned(B, 16) || !aligned(b_scale, 4) || !aligned(C, 16))
+        return FP8BS_ERR_ALIGN;
+    int dev;
+    DeviceState *st;
+    if ((rc = ensure_device(dev, st)))
+        return rc;
+    const Config cfg = choose_config(1, M, N, K, st->num_sms);
+    const int KB = K / 128;
+    const uint64_t ld_sa = static_cast<uint64_t>(fp8bs_a_scale_ld(M));
+    CUtensorMap tmA, tmB, tmSA, tmC;
+    if (!encode_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, A, K, M, K, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, B, K, N, K, 128, cfg.block_n,
+                   CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_2d(&tmSA, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, a_scale, ld_sa, KB, ld_sa * 4, 128, 1,
+                   CU_TENSOR_MAP_SWIZZLE_NONE) ||
+        !encode_2d(&tmC, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, C, N, M, static_cast<uint64_t>(N) * 2, 32, 32,
+                   CU_TENSOR_MAP_SWIZZLE_64B))
+        return FP8BS_ERR_LAUNCH;
+    GemmArgs args = {};
+    args.M = M;
+    args.N = N;
+    args.K = K;
+    args.raster.m_tiles = (M + kBlockM - 1) / kBlockM;
+    args.raster.n_tiles = (N + cfg.block_n - 1) / cfg.block_n;
+    args.raster.raster = cfg.raster;
+    args.raster.group = cfg.group;
+    args.b_scale = b_scale;
+    args.status = st->status_ptr;
+    args.wait_limit_ns = g_wait_limit_ns.load();
+    const int tiles = args.raster.num_tiles();
+    const int grid = tiles < st->num_sms ? tiles : st->num_sms;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = cfg.block_n == 256 ? launch_blockscale<256, 4>(tmA, tmB, tmSA, tmC, args, grid, s)
+                                       : launch_blockscale<128, 6>(tmA, tmB, tmSA, tmC, args, grid, s);
+    if (e != cudaSuccess)
+        return FP8BS_ERR_LAUNCH;
+    t_last_config = config_id(1, cfg);
+    return FP8BS_OK;
+}
+
+int fp8mx_gemm(const void *A, const uint8_t *a_e8m0, const void *B, const uint8_t *b_e8m0, void *C, int M, int N,
+               int K, void *stream)
+{
+    int rc = check_shape(M, N, K);
+    if (rc)
+        return rc;
+    if (M == 0)
+        return FP8BS_OK;
+    if (!A || !a_e8m0 || !B || !b_e8m0 || !C)
+        return FP8BS_ERR_NULL;
+    if (!aligned(A, 16) || !aligned(a_e8m0, 4) || !aligned(B, 16) || !aligned(b_e8m0, 4) || !aligned(C, 16))
+        return FP8BS_ERR_ALIGN;
+    int dev;
+    DeviceState *st;
+    if ((rc = ensure_device(dev, st)))
+        return rc;
+    const Config cfg = choose_config(2, M, N, K, st->num_sms);
+    CUtensorMap tmA, tmB, tmC;
+    if (!encode_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, A, K, M, K, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, B, K, N, K, 128, cfg.block_n,
+                   CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_2d(&tmC, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, C, N, M, static_cast<uint64_t>(N) * 2, 32, 32,
+                   CU_TENSOR_MAP_SWIZZLE_64B))
+        return FP8BS_ERR_LAUNCH;
+    GemmArgs args = {};
+    args.M = M;
+    args.N = N;
+    args.K = K;
+    args.raster.m_tiles = (M + kBlockM - 1) / kBlockM;
+    args.raster.n_tiles = (N + cfg.block_n - 1) / cfg.block_n;
+    args.raster.raster = cfg.raster;
+    args.raster.group = cfg.group;
+    args.a_e8m0 = a_e8m0;
+    args.b_e8m0 = b_e8m0;
+    args.status = st->status_ptr;
+    args.wait_limit_ns = g_wait_limit_ns.load();
+    const int tiles = args.raster.num_tiles();
+    const int grid = tiles < st->num_sms ? tiles : st->num_sms;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = cfg.block_n == 256 ? launch_mxfp8<256, 4>(tmA, tmB, tmC, args, grid, s)
+                                       : launch_mxfp8<128, 6>(tmA, tmB, tmC, args, grid, s);
+    if (e != cudaSuccess)
+        return FP8BS_ERR_LAUNCH;
+    t_last_config = config_id(2, cfg);
+    return FP8BS_OK;
+}
+
+int64_t fp8bs_a_scale_ld(int M) { return (static_cast<int64_t>(M) + 3) / 4 * 4; }
+
+int64_t fp8bs_a_scale_index(int m, int kb, int M) { return static_cast<int64_t>(kb) * fp8bs_a_scale_ld(M) + m; }
+
+int64_t fp8bs_b_scale_index(int n, int kb, int K) { return static_cast<int64_t>(n / 128) * (K / 128) + kb; }
+
+int64_t fp8mx_scale_index(int r, int g, int K) { return static_cast<int64_t>(r) * (K / 32) + g; }
+
+int fp8mx_sf_atom_offset(int r, int j) { return sf_atom_offset(r, j); }
+
+} // extern "C"
+
+namespace fp8bs {
+namespace host {
+__global__ void pack_a_scale_kernel(const float *__restrict__ src, float *__restrict__ dst, int M, int KB,
+                                    int64_t ld)
+{
+    const int64_t total = ld * KB;
+    for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int kb = static_cast<int>(i / ld);
+        const int m = static_cast<int>(i - static_cast<int64_t>(kb) * ld);
+        dst[i] = m < M ? src[static_cast<int64_t>(m) * KB + kb] : 0.f;
+    }
+}
+} // namespace host
+} // namespace fp8bs
+
+extern "C" {
+
+int fp8bs_pack_a_scale(const float *a_scale_rowmajor, float *a_scale_kmajor, int M, int K, void *stream)
+{
+    if (M < 0 || K < 128 || (K % 128) != 0 || K > (1 << 20))
+        return FP8BS_ERR_SHAPE;
+    if (M == 0)
+        return FP8BS_OK;
+    if (!a_scale_rowmajor || !a_scale_kmajor)
+        return FP8BS_ERR_NULL;
+    if (!aligned(a_scale_rowmajor, 4) || !aligned(a_scale_kmajor, 16))
+        return FP8BS_ERR_ALIGN;
+    int dev;
+    DeviceState *st;
+    int rc = ensure_device(dev, st);
+    if (rc)
+        return rc;
+    const int KB = K / 128;
+    const int64_t ld = fp8bs_a_scale_ld(M);
+    const int64_t total = ld * KB;
+    int blocks = static_cast<int>((total + 255) / 256);
+    if (blocks > st->num_sms * 8)
+        blocks = st->num_sms * 8;
+    pack_a_scale_kernel<<<blocks, 256, 0, static_cast<cudaStream_t>(stream)>>>(a_scale_rowmajor, a_scale_kmajor,
+                                                                              M, KB, ld);
+    return cudaGetLastError() == cudaSuccess ? FP8BS_OK : FP8BS_ERR_LAUNCH;
+}
+
+int fp8bs_get_status(void *stream)
+{
+    int dev;
+    DeviceState *st;
+    int rc = ensure_device(dev, st);
+    if (rc)
+        return rc;
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return FP8BS_ERR_CUDA;
+    int v = 0;
+    if (cudaMemcpy(&v, st->status_ptr, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+        return FP8BS_ERR_CUDA;
+    if (v != 0) {
+        const int zero = 0;
+        if (cudaMemcpy(st->status_ptr, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess)
+            return FP8BS_ERR_CUDA;
+    }
+    return v == kStatusTimeout ? FP8BS_ERR_DEVICE_TIMEOUT : (v == 0 ? FP8BS_OK : FP8BS_ERR_CUDA);
+}
+
+const char *fp8bs_status_string(int status)
+{
+    switch (status) {
+    case FP8BS_OK: return "ok";
+    case FP8BS_ERR_NULL: return "null pointer argument";
+    case FP8BS_ERR_ALIGN: return "pointer not aligned as required";
+    case FP8BS_ERR_SHAPE: return "shape outside the supported rules";
+    case FP8BS_ERR_UNSUPPORTED_DEVICE: return "device is not compute capability 10.3 (sm_103a)";
+    case FP8BS_ERR_LAUNCH: return "tensor-map encoding or kernel launch failed";
+    case FP8BS_ERR_DEVICE_TIMEOUT: return "a device-side wait exceeded its time limit";
+    case FP8BS_ERR_CUDA: return "CUDA runtime error";
+    default: return "unknown status";
+    }
+}
+
+int fp8bs_last_config_id(void) { return t_last_config; }
+
+int fp8bs_select_config(int M, int N, int K, int num_sms)
+{
+    if (check_shape(M, N, K) || num_sms <= 0)
+        return FP8BS_ERR_SHAPE;
+    return config_id(1, choose_config(1, M, N, K, num_sms));
+}
+
+int fp8mx_select_config(int M, int N, int K, int num_sms)
+{
+    if (check_shape(M, N, K) || num_sms <= 0)
+        return FP8BS_ERR_SHAPE;
+    return config_id(2, choose_config(2, M, N, K, num_sms));
+}
+
+int fp8bs_launches_per_call(void) { return 1; }
+
+void fp8bs_set_wait_limit_ns(uint64_t ns)
+{
+    g_wait_limit_ns.store(ns ? ns : kDefaultWaitLimitNs);
+}
+
+const char *fp8bs_version(void) { return "fp8bs 0.1.0 (sm_103a)"; }
+
+} // extern "C"

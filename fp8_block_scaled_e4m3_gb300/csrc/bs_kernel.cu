@@ -1,0 +1,291 @@
+// FP8 block-scaled GEMM kernel for sm_103a.
+//
+// Computes C[m,n] = bf16( sum_kb P_kb[m,n] * a_scale[m,kb] * b_scale[n/128,kb] ),
+// P_kb = the unscaled fp8 product over the 128-wide K block kb (skill card
+// "FlyDSL fp8 blockscale GEMM", section "Mechanism A": keep the matrix unit
+// unscaled and apply the arbitrary fp32 block scales in software after it, one
+// promote per K block, because those scales are not powers of two).
+//
+// Persistent, warp-specialised, one CTA per SM, 12 warps (3 warpgroups):
+//   warp 0      TMA producer: A tile [128 x 128] e4m3, B tile [BN x 128] e4m3 and
+//               the a_scale slice [128] fp32 of one K block into stage s of a
+//               STAGES-deep shared-memory ring (full/empty mbarriers).
+//   warp 1      TMEM allocator + single-thread MMA issuer: four
+//               tcgen05.mma.kind::f8f6f4 (M128 x BN x K32) overwrite TMEM partial
+//               buffer (kb & 1) with P_kb; tcgen05.commit releases the stage and
+//               signals the buffer.
+//   warps 2,3   idle (they complete warpgroup 0, which gives its registers away)
+//   warps 4..11 promote + epilogue: warp w reads TMEM lanes 32*(w%4).., column half
+//               (w-4)/4, so each thread owns one row of C and BN/2 columns, all
+//               in one 128-column N block (one b_scale). Per K block:
+//               acc += P_kb * (sa * sb) in fp32 registers; the TMEM buffer is
+//               released right after the loads, so MMA(kb+1) overlaps promote(kb).
+//               After the last K block: bf16 convert, 64-byte-swizzled staging,
+//               TMA store (tails clipped by the tensor map).
+// Registers: the launch gives 168 per thread (3 warps per SM sub-partition);
+// warpgroup 0 drops to 40 and the two promote warpgroups rise to 232, so one
+// sub-partition holds 40 + 232 + 232 = 504 <= 512 registers per lane and the
+// 128 fp32 accumulators plus 64 in-flight partials per thread fit without spills.
+#include "common.cuh"
+
+namespace fp8bs {
+
+constexpr int kBsThreads = (4 + kEpiWarps) * 32;
+constexpr int kBsRegsLow = 40;
+constexpr int kBsRegsHigh = 232;
+
+template <int BN, int STAGES>
+struct BsLayout {
+    static constexpr int A_BYTES = kBlockM * kBlockK;
+    static constexpr int B_BYTES = BN * kBlockK;
+    static constexpr int SA_BYTES = kBlockM * 4;
+    static constexpr int OFF_A = 0;
+    static constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
+    static constexpr int OFF_SA = OFF_B + STAGES * B_BYTES;
+    static constexpr int OFF_C = (OFF_SA + STAGES * SA_BYTES + 1023) / 1024 * 1024;
+    static constexpr int OFF_BAR = OFF_C + kEpiWarps * kCStageBytes;
+    static constexpr int NBAR = 2 * STAGES + 5;  // full[S], empty[S], tfull[2], tempty[2], mma_done
+    static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
+    static constexpr int BYTES = OFF_MISC + 16;
+    static constexpr int DYN_SMEM = BYTES + 1024;   // slack to align the base to 1024
+    static constexpr int TMEM_COLS = 2 * BN <= 32 ? 32 : (2 * BN <= 64 ? 64 : (2 * BN <= 128 ? 128 : (2 * BN <= 256 ? 256 : 512)));
+    static_assert(DYN_SMEM <= 232448, "shared memory budget");
+    static_assert(BN == 128 || BN == 256, "tile width");
+};
+
+template <int BN, int STAGES>
+__global__ void __launch_bounds__(kBsThreads, 1)
+    fp8bs_blockscale_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                            const __grid_constant__ CUtensorMap tmSA, const __grid_constant__ CUtensorMap tmC,
+                            const GemmArgs args)
+{
+    using L = BsLayout<BN, STAGES>;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_s = ptx::smem_u32(smem_raw);
+    const uint32_t sbase = (raw_s + 1023u) & ~1023u;
+    uint8_t *smem = smem_raw + (sbase - raw_s);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int KB = args.K / kBlockK;
+    const int num_tiles = args.raster.num_tiles();
+
+    auto full_bar = [&](int s) { return sbase + L::OFF_BAR + 8u * s; };
+    auto empty_bar = [&](int s) { return sbase + L::OFF_BAR + 8u * (STAGES + s); };
+    auto tfull_bar = [&](int b) { return sbase + L::OFF_BAR + 8u * (2 * STAGES + b); };
+    auto tempty_bar = [&](int b) { return sbase + L::OFF_BAR + 8u * (2 * STAGES + 2 + b); };
+    const uint32_t mma_done_bar = sbase + L::OFF_BAR + 8u * (2 * STAGES + 4);
+    uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + L::OFF_MISC);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::OFF_MISC + 4);
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            ptx::mbar_init(full_bar(s), 1);
+            ptx::mbar_init(empty_bar(s), 1 + kEpiWarps);   // MMA commit + every promote warp (a_scale slice)
+        }
+        for (int b = 0; b < 2; ++b) {
+            ptx::mbar_init(tfull_bar(b), 1);
+            ptx::mbar_init(tempty_bar(b), kEpiWarps);
+        }
+        ptx::mbar_init(mma_done_bar, 1);
+        *abort_flag = 0;
+        ptx::fence_mbar_init();
+    }
+    if (warp == 1) {
+        ptx::tmem_alloc(ptx::smem_u32(tmem_holder), L::TMEM_COLS);
+        ptx::tmem_relinquish();
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem_base = *tmem_holder;
+
+    if (warp < 4) {
+    ptx::setmaxnreg_dec<kBsRegsLow>();
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            ptx::prefetch_tmap(&tmA);
+            ptx::prefetch_tmap(&tmB);
+            ptx::prefetch_tmap(&tmSA);
+            int it = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+                int mb, nb;
+                args.raster.coords(t, mb, nb);
+                for (int kb = 0; kb < KB; ++kb, ++it) {
+                    const int s = it % STAGES;
+                    const uint32_t ph = (it / STAGES) & 1;
+                    if (!wait_bounded(empty_bar(s), ph ^ 1, abort_flag, args)) {
+                        ok = false;
+                        break;
+                    }
+                    ptx::mbar_arrive_expect_tx(full_bar(s), L::A_BYTES + L::B_BYTES + L::SA_BYTES);
+                    ptx::tma_load_2d(sbase + L::OFF_A + s * L::A_BYTES, &tmA, full_bar(s), kb * kBlockK, mb * kBlockM);
+                    ptx::tma_load_2d(sbase + L::OFF_B + s * L::B_BYTES, &tmB, full_bar(s), kb * kBlockK, nb * BN);
+                    ptx::tma_load_2d(sbase + L::OFF_SA + s * L::SA_BYTES, &tmSA, full_bar(s), mb * kBlockM, kb);
+                }
+            }
+            // Every load issued must have landed before the CTA exits.
+            for (int s = 0; s < STAGES; ++s) {
+                const int uses = it > s ? (it - s + STAGES - 1) / STAGES : 0;
+                if (uses > 0)
+                    wait_teardown(full_bar(s), (uses - 1) & 1, args);
+            }
+        }
+    } else if (warp == 1) {
+        // --------------------------------------------------------- MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t idesc = ptx::idesc_f8f6f4_e4m3(kBlockM, BN);
+            int it = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+                for (int kb = 0; kb < KB; ++kb, ++it) {
+                    const int s = it % STAGES;
+                    const uint32_t ph = (it / STAGES) & 1;
+                    const int buf = it & 1;
+                    const uint32_t tph = (it >> 1) & 1;
+                    if (!wait_bounded(tempty_bar(buf), tph ^ 1, abort_flag, args) ||
+                        !wait_bounded(full_bar(s), ph, abort_flag, args)) {
+                        ok = false;
+                        break;
+                    }
+                    ptx::tc_fence_after();
+                    const uint64_t adesc = ptx::desc_kmajor_sw128(sbase + L::OFF_A + s * L::A_BYTES);
+                    const uint64_t bdesc = ptx::desc_kmajor_sw128(sbase + L::OFF_B + s * L::B_BYTES);
+                    const uint32_t d = tmem_base + static_cast<uint32_t>(buf * BN);
+#pragma unroll
+                    for (int kk = 0; kk < kBlockK / kMmaK; ++kk)
+                        ptx::mma_f8f6f4(d, adesc + 2 * kk, bdesc + 2 * kk, idesc, kk > 0 ? 1u : 0u);
+                    ptx::tc_commit(empty_bar(s));
+                    ptx::tc_commit(tfull_bar(buf));
+                }
+            }
+            // No MMA may still be running when the tensor memory is freed.
+            ptx::tc_commit(mma_done_bar);
+            wait_teardown(mma_done_bar, 0, args);
+        }
+    }
+    } else {
+        ptx::setmaxnreg_inc<kBsRegsHigh>();
+        // ------------------------------------------------- promote + epilogue
+        constexpr int HALF = BN / 2;                 // columns per thread
+        const int ew = warp - 4;                     // 0..7
+        const int wg = ew >> 2;                      // column half
+        const int q = warp & 3;                      // TMEM lane quadrant this warp may access
+        const int row = q * 32 + lane;               // row of the tile
+        const int NB = (args.N + 127) / 128;
+        const uint32_t cstage = sbase + L::OFF_C + ew * kCStageBytes;
+        const int my_tiles = static_cast<int>(blockIdx.x) < num_tiles
+                                 ? (num_tiles - static_cast<int>(blockIdx.x) + static_cast<int>(gridDim.x) - 1) /
+                                       static_cast<int>(gridDim.x)
+                                 : 0;
+        const int total = my_tiles * KB;
+
+        // b_scale for flattened step g (tile g/KB of this CTA, K block g%KB).
+        auto sb_load = [&](int g) -> float {
+            if (g >= total)
+                return 0.f;
+            const int ti = g / KB;
+            const int kb = g - ti * KB;
+            int mb, nb;
+            args.raster.coords(static_cast<int>(blockIdx.x) + ti * static_cast<int>(gridDim.x), mb, nb);
+            const int nblk = (nb * BN + wg * HALF) >> 7;
+            if (nblk >= NB)
+                return 0.f;
+            return ptx::ldg_nc_f32(args.b_scale + static_cast<size_t>(nblk) * KB + kb);
+        };
+        float sbq0 = sb_load(0), sbq1 = sb_load(1), sbq2 = sb_load(2);
+
+        float acc[HALF];
+        int it = 0;
+        bool ok = true;
+        for (int t = blockIdx.x; t < num_tiles; t += gridDim.x) {
+            int mb, nb;
+            args.raster.coords(t, mb, nb);
+#pragma unroll
+            for (int j = 0; j < HALF; ++j)
+                acc[j] = 0.f;
+            for (int kb = 0; kb < KB; ++kb, ++it) {
+                const float sb = sbq0;
+                sbq0 = sbq1;
+                sbq1 = sbq2;
+                sbq2 = sb_load(it + 3);
+                const int s = it % STAGES;
+                const uint32_t ph = (it / STAGES) & 1;
+                const int buf = it & 1;
+                const uint32_t tph = (it >> 1) & 1;
+                if (!wait_bounded_warp(tfull_bar(buf), tph, abort_flag, args) ||
+                    !wait_bounded_warp(full_bar(s), ph, abort_flag, args)) {
+                    ok = false;
+                    break;
+                }
+                ptx::tc_fence_after();
+                const float sa = reinterpret_cast<const float *>(smem + L::OFF_SA + s * L::SA_BYTES)[row];
+                const float scale = sa * sb;
+                const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
+                                       static_cast<uint32_t>(buf * BN + wg * HALF);
+#pragma unroll
+                for (int h = 0; h < HALF / 64; ++h) {
+                    uint32_t r0[32], r1[32];
+                    ptx::tmem_ld_32x32b_x32(taddr + h * 64, r0);
+                    ptx::tmem_ld_32x32b_x32(taddr + h * 64 + 32, r1);
+                    ptx::tmem_wait_ld();
+#pragma unroll
+                    for (int j = 0; j < 32; ++j)
+                        acc[h * 64 + j] = fmaf(__uint_as_float(r0[j]), scale, acc[h * 64 + j]);
+#pragma unroll
+                    for (int j = 0; j < 32; ++j)
+                        acc[h * 64 + 32 + j] = fmaf(__uint_as_float(r1[j]), scale, acc[h * 64 + 32 + j]);
+                }
+                ptx::tc_fence_before();
+                __syncwarp();
+                if (lane == 0) {
+                    ptx::mbar_arrive(tempty_bar(buf));
+                    ptx::mbar_arrive(empty_bar(s));
+                }
+            }
+            if (!ok)
+                break;
+            const int x0 = nb * BN + wg * HALF;
+            const int y0 = mb * kBlockM + q * 32;
+#pragma unroll
+            for (int c = 0; c < HALF / 32; ++c)
+                store_c_chunk(&tmC, cstage, lane, acc + c * 32, x0 + c * 32, y0, args.M, args.N);
+        }
+        if (lane == 0)
+            ptx::bulk_wait_all();
+    }
+
+    ptx::tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc(tmem_base, L::TMEM_COLS);
+    }
+}
+
+// Launch helpers called by the host API (api.cu).
+template <int BN, int STAGES>
+cudaError_t launch_blockscale(const CUtensorMap &tmA, const CUtensorMap &tmB, const CUtensorMap &tmSA,
+                              const CUtensorMap &tmC, const GemmArgs &args, int grid, cudaStream_t stream)
+{
+    using L = BsLayout<BN, STAGES>;
+    auto kern = fp8bs_blockscale_kernel<BN, STAGES>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::DYN_SMEM);
+    if (e != cudaSuccess)
+        return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kBsThreads);
+    cfg.dynamicSmemBytes = L::DYN_SMEM;
+    cfg.stream = stream;
+    return cudaLaunchKernelEx(&cfg, kern, tmA, tmB, tmSA, tmC, args);
+}
+
+template cudaError_t launch_blockscale<256, 4>(const CUtensorMap &, const CUtensorMap &, const CUtensorMap &,
+                                               const CUtensorMap &, const GemmArgs &, int, cudaStream_t);
+template cudaError_t launch_blockscale<128, 6>(const CUtensorMap &, const CUtensorMap &, const CUtensorMap &,
+                                               const CUtensorMap &, const GemmArgs &, int, cudaStream_t);
+
+} // namespace fp8bs

@@ -1,0 +1,141 @@
+// Pieces shared by the blockscale and MXFP8 kernels and the host launcher.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "ptx.cuh"
+
+namespace fp8bs {
+
+constexpr int kBlockM = 128;   // rows of C per tile = TMEM lanes used by one MMA
+constexpr int kBlockK = 128;   // K per pipeline stage (one fp32 scale block / four MX groups)
+constexpr int kMmaK = 32;      // K of one fp8 tcgen05.mma
+constexpr int kEpiWarps = 8;   // promote / epilogue warps (two column halves x four lane quadrants)
+constexpr int kCStageBytes = 32 * 32 * 2;  // per epilogue warp: 32 rows x 32 bf16, 64-byte swizzle
+
+constexpr int kStatusTimeout = 1;   // value the device writes into the status word
+
+// Tile order. Tiles are visited in groups of `group` panels of the "inner"
+// operand; raster 0 keeps a group of N panels and walks M inside it (A tiles
+// stream past a resident set of B panels), raster 1 the converse.
+struct TileRaster {
+    int m_tiles, n_tiles, raster, group;
+
+    __host__ __device__ __forceinline__ int num_tiles() const { return m_tiles * n_tiles; }
+
+    __host__ __device__ __forceinline__ void coords(int t, int &mb, int &nb) const
+    {
+        if (raster == 0) {
+            const int per = group * m_tiles;
+            const int g = t / per;
+            const int r = t - g * per;
+            const int n0 = g * group;
+            const int gw = (n_tiles - n0) < group ? (n_tiles - n0) : group;
+            mb = r / gw;
+            nb = n0 + (r - mb * gw);
+        } else {
+            const int per = group * n_tiles;
+            const int g = t / per;
+            const int r = t - g * per;
+            const int m0 = g * group;
+            const int gh = (m_tiles - m0) < group ? (m_tiles - m0) : group;
+            nb = r / gh;
+            mb = m0 + (r - nb * gh);
+        }
+    }
+};
+
+struct GemmArgs {
+    int M, N, K;
+    TileRaster raster;
+    const float *b_scale;      // blockscale: [ceil(N/128)][K/128]
+    const uint8_t *a_e8m0;     // mxfp8: [M][K/32]
+    const uint8_t *b_e8m0;     // mxfp8: [N][K/32]
+    int *status;               // per-device status word
+    unsigned long long wait_limit_ns;
+};
+
+// Byte offset of (row r in 0..127, group j in 0..3) in a 512-byte scale-factor
+// atom: 32 rows of 16 bytes, row (r % 32) holds rows r%32, r%32+32, r%32+64,
+// r%32+96 as four 32-bit words, byte j of each word being K group j. This is
+// the shared-memory image that one tcgen05.cp 32x128b.warpx4 moves into four
+// tensor-memory columns.
+__host__ __device__ __forceinline__ int sf_atom_offset(int r, int j)
+{
+    return (r & 31) * 16 + ((r >> 5) & 3) * 4 + (j & 3);
+}
+
+// Bounded wait on an mbarrier phase. Returns false (and raises the CTA abort
+// flag and the device status word) when the wait exceeds the time limit, or
+// when another role of the CTA has already aborted.
+__device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, volatile int *abort_flag,
+                                             const GemmArgs &a)
+{
+    if (ptx::mbar_try_wait(bar, parity))
+        return true;
+    const uint64_t t0 = ptx::globaltimer();
+    while (!ptx::mbar_try_wait(bar, parity)) {
+        if (*abort_flag)
+            return false;
+        if (ptx::globaltimer() - t0 > a.wait_limit_ns) {
+            *abort_flag = 1;
+            atomicExch(a.status, kStatusTimeout);
+            return false;
+        }
+    }
+    return true;
+}
+
+// Wait used only while tearing down: no abort check, same time limit.
+__device__ __forceinline__ void wait_teardown(uint32_t bar, uint32_t parity, const GemmArgs &a)
+{
+    if (ptx::mbar_try_wait(bar, parity))
+        return;
+    const uint64_t t0 = ptx::globaltimer();
+    while (!ptx::mbar_try_wait(bar, parity)) {
+        if (ptx::globaltimer() - t0 > a.wait_limit_ns) {
+            atomicExch(a.status, kStatusTimeout);
+            return;
+        }
+    }
+}
+
+// Warp-uniform bounded wait: every lane waits, the result is agreed by vote.
+__device__ __forceinline__ bool wait_bounded_warp(uint32_t bar, uint32_t parity, volatile int *abort_flag,
+                                                  const GemmArgs &a)
+{
+    const bool ok = wait_bounded(bar, parity, abort_flag, a);
+    return __all_sync(0xffffffffu, ok);
+}
+
+// Store one epilogue warp's 32 rows x 32 columns of C (row = lane) through its
+// 2 KiB staging buffer with one TMA store. `v` are the 32 fp32 values of this
+// lane's row. The staging buffer uses the 64-byte swizzle: 16-byte chunk j of
+// row r sits at chunk j ^ ((r >> 1) & 3).
+__device__ __forceinline__ void store_c_chunk(const CUtensorMap *tmC, uint32_t stage, int lane, const float *v,
+                                              int x, int y, int M, int N)
+{
+    if (lane == 0)
+        ptx::bulk_wait_read_all();   // the previous store from this buffer has read it
+    __syncwarp();
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const uint32_t w0 = ptx::pack_bf16x2(v[j * 8 + 0], v[j * 8 + 1]);
+        const uint32_t w1 = ptx::pack_bf16x2(v[j * 8 + 2], v[j * 8 + 3]);
+        const uint32_t w2 = ptx::pack_bf16x2(v[j * 8 + 4], v[j * 8 + 5]);
+        const uint32_t w3 = ptx::pack_bf16x2(v[j * 8 + 6], v[j * 8 + 7]);
+        const int phys = j ^ ((lane >> 1) & 3);
+        ptx::st_shared_v4(stage + lane * 64 + phys * 16, w0, w1, w2, w3);
+    }
+    ptx::fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+        if (x < N && y < M)
+            ptx::tma_store_2d(tmC, stage, x, y);
+        ptx::bulk_commit();
+    }
+}
+
+} // namespace fp8bs

@@ -1,0 +1,302 @@
+// MXFP8 GEMM kernel for sm_103a.
+//
+// Computes C[m,n] = bf16( sum_k A[m,k] 2^(ea[m,k/32]-127) * B[n,k] 2^(eb[n,k/32]-127) ).
+// The PR "1x32 ue8m0 (MXFP8) 8-wave FlyDSL GEMM for gfx950" (section "Why it is
+// faster") feeds the ue8m0 scales to the matrix instruction as operands, so
+// there is no software promote: here tcgen05.mma.kind::mxf8f6f4.block_scale
+// (scale_vec::1X: one scale byte per row per 32-wide K slice) accumulates over
+// the whole K extent in tensor memory.
+//
+// Persistent, warp-specialised, one CTA per SM, 11 warps:
+//   warp 0       TMA producer: A [128 x 128] and B [BN x 128] e4m3 per 128-wide K step.
+//   warp 1       TMEM allocator + single-thread issuer: tcgen05.cp of the step's
+//                scale-factor atoms into TMEM, then four block-scaled MMAs
+//                (scale byte id = the 32-wide slice inside the step).
+//   warp 2       scale-factor stager: reads the quantiser's row-major ue8m0 bytes
+//                ([rows][K/32], 4 bytes per row and step) with plain loads, a few
+//                steps ahead, and writes them into 512-byte atoms in the stage
+//                (32 rows x 16 bytes, the image tcgen05.cp 32x128b.warpx4 copies).
+//                Row strides of K/32 bytes are not 16-byte multiples in general
+//                (K = 1280 gives 40), so these rows cannot be TMA tensors.
+//   warps 3..10  epilogue: drain the fp32 accumulator (128 columns per thread),
+//                release it to the next tile's MMAs, bf16 convert, TMA store.
+#include "common.cuh"
+
+namespace fp8bs {
+
+constexpr int kMxThreads = (3 + kEpiWarps) * 32;
+constexpr int kSfDepth = 3;   // steps of scale bytes the stager keeps in flight
+
+template <int BN, int STAGES>
+struct MxLayout {
+    static constexpr int A_BYTES = kBlockM * kBlockK;
+    static constexpr int B_BYTES = BN * kBlockK;
+    static constexpr int SFA_BYTES = 512;            // one atom: 128 rows x 4 groups
+    static constexpr int SFB_BYTES = 512 * (BN / 128);
+    static constexpr int SF_BYTES = SFA_BYTES + SFB_BYTES;
+    static constexpr int OFF_A = 0;
+    static constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
+    static constexpr int OFF_SF = OFF_B + STAGES * B_BYTES;
+    static constexpr int OFF_C = (OFF_SF + STAGES * SF_BYTES + 1023) / 1024 * 1024;
+    static constexpr int OFF_BAR = OFF_C + kEpiWarps * kCStageBytes;
+    static constexpr int NBAR = 2 * STAGES + 3;     // full[S], empty[S], acc_full, acc_empty, mma_done
+    static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
+    static constexpr int BYTES = OFF_MISC + 16;
+    static constexpr int DYN_SMEM = BYTES + 1024;
+    // TMEM: accumulator columns [0, BN), then 16 scale-factor columns per stage
+    // (A atom: 4 columns, B atoms: 4 columns per 128 rows).
+    static constexpr int SF_COL0 = BN;
+    static constexpr int SF_COLS_PER_STAGE = 16;
+    static constexpr int TMEM_COLS = 512;
+    static_assert(SF_COL0 + STAGES * SF_COLS_PER_STAGE <= TMEM_COLS, "tensor memory budget");
+    static_assert(4 + 4 * (BN / 128) <= SF_COLS_PER_STAGE, "scale columns per stage");
+    static_assert(DYN_SMEM <= 232448, "shared memory budget");
+    static_assert(BN == 128 || BN == 256, "tile width");
+};
+
+template <int BN, int STAGES>
+__global__ void __launch_bounds__(kMxThreads, 1)
+    fp8bs_mxfp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                       const __grid_constant__ CUtensorMap tmC, const GemmArgs args)
+{
+    using L = MxLayout<BN, STAGES>;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_s = ptx::smem_u32(smem_raw);
+    const uint32_t sbase = (raw_s + 1023u) & ~1023u;
+    uint8_t *smem = smem_raw + (sbase - raw_s);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int KS = args.K / kBlockK;
+    const int num_tiles = args.raster.num_tiles();
+
+    auto full_bar = [&](int s) { return sbase + L::OFF_BAR + 8u * s; };
+    auto empty_bar = [&](int s) { return sbase + L::OFF_BAR + 8u * (STAGES + s); };
+    const uint32_t acc_full_bar = sbase + L::OFF_BAR + 8u * (2 * STAGES);
+    const uint32_t acc_empty_bar = sbase + L::OFF_BAR + 8u * (2 * STAGES + 1);
+    const uint32_t mma_done_bar = sbase + L::OFF_BAR + 8u * (2 * STAGES + 2);
+    uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + L::OFF_MISC);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::OFF_MISC + 4);
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            ptx::mbar_init(full_bar(s), 2);      // producer (with tx bytes) + scale stager
+            ptx::mbar_init(empty_bar(s), 1);     // MMA commit
+        }
+        ptx::mbar_init(acc_full_bar, 1);
+        ptx::mbar_init(acc_empty_bar, kEpiWarps);
+        ptx::mbar_init(mma_done_bar, 1);
+        *abort_flag = 0;
+        ptx::fence_mbar_init();
+    }
+    if (warp == 1) {
+        ptx::tmem_alloc(ptx::smem_u32(tmem_holder), L::TMEM_COLS);
+        ptx::tmem_relinquish();
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem_base = *tmem_holder;
+
+    const int my_tiles = static_cast<int>(blockIdx.x) < num_tiles
+                             ? (num_tiles - static_cast<int>(blockIdx.x) + static_cast<int>(gridDim.x) - 1) /
+                                   static_cast<int>(gridDim.x)
+                             : 0;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            ptx::prefetch_tmap(&tmA);
+            ptx::prefetch_tmap(&tmB);
+            int it = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+                int mb, nb;
+                args.raster.coords(t, mb, nb);
+                for (int ks = 0; ks < KS; ++ks, ++it) {
+                    const int s = it % STAGES;
+                    const uint32_t ph = (it / STAGES) & 1;
+                    if (!wait_bounded(empty_bar(s), ph ^ 1, abort_flag, args)) {
+                        ok = false;
+                        break;
+                    }
+                    ptx::mbar_arrive_expect_tx(full_bar(s), L::A_BYTES + L::B_BYTES);
+                    ptx::tma_load_2d(sbase + L::OFF_A + s * L::A_BYTES, &tmA, full_bar(s), ks * kBlockK, mb * kBlockM);
+                    ptx::tma_load_2d(sbase + L::OFF_B + s * L::B_BYTES, &tmB, full_bar(s), ks * kBlockK, nb * BN);
+                }
+            }
+            for (int s = 0; s < STAGES; ++s) {
+                const int uses = it > s ? (it - s + STAGES - 1) / STAGES : 0;
+                if (uses > 0)
+                    wait_teardown(full_bar(s), (uses - 1) & 1, args);
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            int it = 0;
+            bool ok = true;
+            int titer = 0;
+            for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x, ++titer) {
+                if (!wait_bounded(acc_empty_bar, (titer & 1) ^ 1, abort_flag, args))
+                    break;
+                ptx::tc_fence_after();
+                for (int ks = 0; ks < KS; ++ks, ++it) {
+                    const int s = it % STAGES;
+                    const uint32_t ph = (it / STAGES) & 1;
+                    if (!wait_bounded(full_bar(s), ph, abort_flag, args)) {
+                        ok = false;
+                        break;
+                    }
+                    ptx::tc_fence_after();
+                    const uint32_t sf_smem = sbase + L::OFF_SF + s * L::SF_BYTES;
+                    const uint32_t sfa_t = tmem_base + static_cast<uint32_t>(L::SF_COL0 + s * L::SF_COLS_PER_STAGE);
+                    const uint32_t sfb_t = sfa_t + 4;
+                    ptx::tc_cp_32x128b_warpx4(sfa_t, ptx::desc_noswizzle(sf_smem, 16, 128));
+#pragma unroll
+                    for (int h = 0; h < BN / 128; ++h)
+                        ptx::tc_cp_32x128b_warpx4(sfb_t + 4 * h,
+                                                  ptx::desc_noswizzle(sf_smem + L::SFA_BYTES + 512 * h, 16, 128));
+                    const uint64_t adesc = ptx::desc_kmajor_sw128(sbase + L::OFF_A + s * L::A_BYTES);
+                    const uint64_t bdesc = ptx::desc_kmajor_sw128(sbase + L::OFF_B + s * L::B_BYTES);
+#pragma unroll
+                    for (int kk = 0; kk < kBlockK / kMmaK; ++kk)
+                        ptx::mma_mxf8f6f4(tmem_base, adesc + 2 * kk, bdesc + 2 * kk,
+                                          ptx::idesc_mxf8f6f4_e4m3(kBlockM, BN, kk, kk), sfa_t, sfb_t,
+                                          (ks | kk) != 0 ? 1u : 0u);
+                    ptx::tc_commit(empty_bar(s));
+                }
+                if (!ok)
+                    break;
+                ptx::tc_commit(acc_full_bar);
+            }
+            ptx::tc_commit(mma_done_bar);
+            wait_teardown(mma_done_bar, 0, args);
+        }
+    } else if (warp == 2) {
+        // -------------------------------------------------- scale stager
+        const int G = args.K / 32;
+        const int total = my_tiles * KS;
+        struct Slot {
+            uint32_t a[4];
+            uint32_t b[4 * (BN / 128)];
+        };
+        auto load = [&](int g, Slot &sl) {
+            if (g >= total) {
+#pragma unroll
+                for (int i = 0; i < 4; ++i) sl.a[i] = 0;
+#pragma unroll
+                for (int i = 0; i < 4 * (BN / 128); ++i) sl.b[i] = 0;
+                return;
+            }
+            const int ti = g / KS;
+            const int ks = g - ti * KS;
+            int mb, nb;
+            args.raster.coords(static_cast<int>(blockIdx.x) + ti * static_cast<int>(gridDim.x), mb, nb);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int m = mb * kBlockM + lane + 32 * i;
+                sl.a[i] = m < args.M ? ptx::ldg_nc_u32(args.a_e8m0 + static_cast<size_t>(m) * G + 4 * ks) : 0u;
+            }
+#pragma unroll
+            for (int i = 0; i < 4 * (BN / 128); ++i) {
+                const int n = nb * BN + lane + 32 * i;
+                sl.b[i] = n < args.N ? ptx::ldg_nc_u32(args.b_e8m0 + static_cast<size_t>(n) * G + 4 * ks) : 0u;
+            }
+        };
+        Slot q0, q1, q2;
+        load(0, q0);
+        load(1, q1);
+        load(2, q2);
+        for (int g = 0; g < total; ++g) {
+            const Slot cur = q0;
+            q0 = q1;
+            q1 = q2;
+            load(g + kSfDepth, q2);
+            const int s = g % STAGES;
+            const uint32_t ph = (g / STAGES) & 1;
+            if (!wait_bounded_warp(empty_bar(s), ph ^ 1, abort_flag, args))
+                break;
+            const uint32_t sf_smem = sbase + L::OFF_SF + s * L::SF_BYTES;
+            // lane l writes the 16 bytes of atom row l: rows l, l+32, l+64, l+96.
+            ptx::st_shared_v4(sf_smem + lane * 16, cur.a[0], cur.a[1], cur.a[2], cur.a[3]);
+#pragma unroll
+            for (int h = 0; h < BN / 128; ++h)
+                ptx::st_shared_v4(sf_smem + L::SFA_BYTES + 512 * h + lane * 16, cur.b[4 * h + 0], cur.b[4 * h + 1],
+                                  cur.b[4 * h + 2], cur.b[4 * h + 3]);
+            ptx::fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0)
+                ptx::mbar_arrive(full_bar(s));
+        }
+    } else {
+        // ------------------------------------------------------ epilogue
+        constexpr int HALF = BN / 2;
+        const int ew = warp - 3;                // 0..7
+        const int wg = ew >> 2;
+        const int q = warp & 3;
+        const uint32_t cstage = sbase + L::OFF_C + ew * kCStageBytes;
+        int titer = 0;
+        for (int t = blockIdx.x; t < num_tiles; t += gridDim.x, ++titer) {
+            int mb, nb;
+            args.raster.coords(t, mb, nb);
+            if (!wait_bounded_warp(acc_full_bar, titer & 1, abort_flag, args))
+                break;
+            ptx::tc_fence_after();
+            float v[HALF];
+            const uint32_t taddr =
+                tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(wg * HALF);
+#pragma unroll
+            for (int c = 0; c < HALF / 32; ++c) {
+                uint32_t r[32];
+                ptx::tmem_ld_32x32b_x32(taddr + c * 32, r);
+#pragma unroll
+                for (int j = 0; j < 32; ++j)
+                    v[c * 32 + j] = __uint_as_float(r[j]);
+            }
+            ptx::tmem_wait_ld();
+            ptx::tc_fence_before();
+            __syncwarp();
+            if (lane == 0)
+                ptx::mbar_arrive(acc_empty_bar);
+            const int x0 = nb * BN + wg * HALF;
+            const int y0 = mb * kBlockM + q * 32;
+#pragma unroll
+            for (int c = 0; c < HALF / 32; ++c)
+                store_c_chunk(&tmC, cstage, lane, v + c * 32, x0 + c * 32, y0, args.M, args.N);
+        }
+        if (lane == 0)
+            ptx::bulk_wait_all();
+    }
+
+    ptx::tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc(tmem_base, L::TMEM_COLS);
+    }
+}
+
+template <int BN, int STAGES>
+cudaError_t launch_mxfp8(const CUtensorMap &tmA, const CUtensorMap &tmB, const CUtensorMap &tmC,
+                         const GemmArgs &args, int grid, cudaStream_t stream)
+{
+    using L = MxLayout<BN, STAGES>;
+    auto kern = fp8bs_mxfp8_kernel<BN, STAGES>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::DYN_SMEM);
+    if (e != cudaSuccess)
+        return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kMxThreads);
+    cfg.dynamicSmemBytes = L::DYN_SMEM;
+    cfg.stream = stream;
+    return cudaLaunchKernelEx(&cfg, kern, tmA, tmB, tmC, args);
+}
+
+template cudaError_t launch_mxfp8<256, 4>(const CUtensorMap &, const CUtensorMap &, const CUtensorMap &,
+                                          const GemmArgs &, int, cudaStream_t);
+template cudaError_t launch_mxfp8<128, 6>(const CUtensorMap &, const CUtensorMap &, const CUtensorMap &,
+                                          const GemmArgs &, int, cudaStream_t);
+
+} // namespace fp8bs

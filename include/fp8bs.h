@@ -1,0 +1,130 @@
+/*
+ * fp8bs — FP8 block-scaled GEMM and MXFP8 GEMM for NVIDIA GB300 (sm_103a).
+ *
+ * C ABI of libfp8bs.so. Plain pointers and sizes only. Device pointers are
+ * CUDA device addresses owned by the caller; `stream` is a cudaStream_t passed
+ * as void* (NULL = the legacy default stream). Every GEMM call is asynchronous
+ * on `stream`, performs no host synchronisation and no allocation after the
+ * first call on a device, and can be captured in a CUDA graph.
+ *
+ * Error behaviour: functions return FP8BS_OK (0) or a negative fp8bs_status.
+ * Argument errors are detected on the host before anything is launched.
+ * A device-side wait that exceeds its time limit does not trap: the kernel
+ * records FP8BS_ERR_DEVICE_TIMEOUT in a per-device status word, releases its
+ * resources and returns; fp8bs_get_status() reads and clears that word.
+ */
+#ifndef FP8BS_H
+#define FP8BS_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    FP8BS_OK = 0,
+    FP8BS_ERR_NULL = -1,               /* a required pointer is NULL                          */
+    FP8BS_ERR_ALIGN = -2,              /* a pointer is not 16-byte aligned                    */
+    FP8BS_ERR_SHAPE = -3,              /* M, N or K outside the documented shape rules        */
+    FP8BS_ERR_UNSUPPORTED_DEVICE = -4, /* current device is not compute capability 10.3       */
+    FP8BS_ERR_LAUNCH = -5,             /* the kernel launch or tensor-map encoding failed     */
+    FP8BS_ERR_DEVICE_TIMEOUT = -6,     /* a device wait ran out of time (status word)         */
+    FP8BS_ERR_CUDA = -7                /* another CUDA runtime error                          */
+} fp8bs_status;
+
+/*
+ * FP8 block-scaled GEMM (skill card "FlyDSL fp8 blockscale GEMM", sections
+ * "When to use" and "Mechanism A"):
+ *
+ *   C[m,n] = bf16( sum_kb (sum_{k in kb} A[m,k] * B[n,k]) * a_scale[m,kb] * b_scale[n/128,kb] )
+ *
+ * with 128-wide K blocks kb. The fp8 products are accumulated unscaled per K
+ * block and the arbitrary fp32 scales are applied afterwards in fp32 (they are
+ * never rounded to powers of two).
+ *
+ *   A        E4M3 (OCP E4M3FN) [M][K] row-major, 16-byte aligned.
+ *   a_scale  fp32 [K/128][fp8bs_a_scale_ld(M)], K-block-major ("transposed
+ *            contiguous [scale_k, M]", skill card section "Procedure" step 6):
+ *            a_scale[m,kb] is at kb*fp8bs_a_scale_ld(M) + m. 16-byte aligned.
+ *   B        E4M3 [N][K] row-major (the weight, K contiguous), 16-byte aligned.
+ *   b_scale  fp32 [ceil(N/128)][K/128] row-major ("[scale_n, scale_k]"), 4-byte aligned.
+ *   C        bf16 [M][N] row-major, written (never read), 16-byte aligned.
+ *
+ * Shape rules: M >= 1; N >= 8 and N % 8 == 0; K >= 128, K % 128 == 0 and
+ * K <= 65536. Otherwise FP8BS_ERR_SHAPE. M = 0 is a no-op returning FP8BS_OK.
+ * A partial last N block of 128 rows uses its own b_scale row.
+ */
+int fp8bs_gemm(const void *A, const float *a_scale, const void *B, const float *b_scale, void *C,
+               int M, int N, int K, void *stream);
+
+/*
+ * MXFP8 GEMM (PR "1x32 ue8m0 (MXFP8) 8-wave FlyDSL GEMM for gfx950", sections
+ * "Why it is faster" and "Correctness"): both operands E4M3 with one ue8m0
+ * scale 2^(e-127) per row and 32-wide K group g = k/32:
+ *
+ *   C[m,n] = bf16( sum_k A[m,k]*2^(a_e8m0[m,g]-127) * B[n,k]*2^(b_e8m0[n,g]-127) )
+ *
+ *   A       E4M3 [M][K] row-major, 16-byte aligned.
+ *   a_e8m0  uint8 [M][K/32] row-major (the quantiser's own layout), 4-byte aligned.
+ *   B       E4M3 [N][K] row-major, 16-byte aligned.
+ *   b_e8m0  uint8 [N][K/32] row-major, 4-byte aligned.
+ *   C       bf16 [M][N] row-major, written, 16-byte aligned.
+ *
+ * Shape rules as fp8bs_gemm. The scale bytes 0xFF (NaN) are outside the
+ * contract. This entry point and fp8bs_gemm are deliberately separate: the
+ * two scale formats cannot be told apart by shape or dtype.
+ */
+int fp8mx_gemm(const void *A, const uint8_t *a_e8m0, const void *B, const uint8_t *b_e8m0, void *C,
+               int M, int N, int K, void *stream);
+
+/* ---- layout helpers (bit-exact; host functions, no CUDA calls) ---------- */
+
+/* Leading dimension of the K-block-major a_scale: M rounded up to 4 (a
+ * multiple of 16 bytes, as the tensor-memory-access unit requires). */
+int64_t fp8bs_a_scale_ld(int M);
+/* Element offset of logical a_scale[m,kb] in the K-block-major buffer. */
+int64_t fp8bs_a_scale_index(int m, int kb, int M);
+/* Element offset of the scale that applies to B row n in K block kb. */
+int64_t fp8bs_b_scale_index(int n, int kb, int K);
+/* Element offset of the ue8m0 byte for row r and 32-wide K group g. */
+int64_t fp8mx_scale_index(int r, int g, int K);
+/* Byte offset, inside one 512-byte scale-factor atom (128 rows x 4 groups),
+ * at which the MXFP8 kernel stages the byte of row r (0..127) and group j
+ * (0..3) before copying the atom to tensor memory: (r%32)*16 + (r/32)*4 + j. */
+int fp8mx_sf_atom_offset(int r, int j);
+
+/* Repack a row-major logical a_scale [M][K/128] (device) into the
+ * K-block-major layout above (device, fp8bs_a_scale_ld(M)*(K/128) floats,
+ * padding rows zeroed). Asynchronous on `stream`. */
+int fp8bs_pack_a_scale(const float *a_scale_rowmajor, float *a_scale_kmajor, int M, int K, void *stream);
+
+/* ---- status and introspection ---------------------------------------------- */
+
+/* Synchronises `stream`, then returns and clears the current device's status
+ * word: FP8BS_OK, FP8BS_ERR_DEVICE_TIMEOUT, or FP8BS_ERR_CUDA if the
+ * synchronisation itself failed. */
+int fp8bs_get_status(void *stream);
+/* Static string for a status code. */
+const char *fp8bs_status_string(int status);
+/* Identifier of the kernel configuration the last successful GEMM call on this
+ * host thread launched (0 if none): kind*1000000 + block_n*1000 + stages*100 +
+ * raster*10 + group_code, kind 1 = blockscale, 2 = mxfp8. */
+int fp8bs_last_config_id(void);
+/* Configuration id fp8bs_gemm / fp8mx_gemm would choose for a shape on a
+ * device with `num_sms` SMs (host-only, no CUDA calls). */
+int fp8bs_select_config(int M, int N, int K, int num_sms);
+int fp8mx_select_config(int M, int N, int K, int num_sms);
+/* Number of kernels one fp8bs_gemm / fp8mx_gemm call launches (1). */
+int fp8bs_launches_per_call(void);
+/* Set the per-wait device time limit in nanoseconds (default 2e9) used by
+ * subsequent launches from this process; 0 restores the default. */
+void fp8bs_set_wait_limit_ns(uint64_t ns);
+/* Library version string. */
+const char *fp8bs_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FP8BS_H */

@@ -1,0 +1,62 @@
+"""Helpers for the GPU tests: run the library on numpy inputs, compare to the oracle."""
+import numpy as np
+
+import oracle
+import workloads
+
+# Tolerance of the comparison: elementwise |gpu - oracle| <= ATOL + RTOL*|oracle|
+# and ||gpu - oracle||_2 / ||oracle||_2 <= REL_L2 (the oracle's bf16 is the reference).
+ATOL = 1e-2
+RTOL = 1e-2
+REL_L2 = 2e-3
+
+
+def to_dev(a):
+    import torch
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+def run_blockscale(A, a_scale, B, b_scale, C=None):
+    """GPU blockscale GEMM on numpy inputs (a_scale logical [M, K/128]); returns bf16 bits (uint16 numpy)."""
+    import torch
+    import fp8_block_scaled_e4m3_gb300 as f
+    M, K = A.shape
+    N = B.shape[0]
+    dA = to_dev(A)
+    dB = to_dev(B)
+    dsa = to_dev(workloads.a_scale_to_kmajor(a_scale))
+    dsb = to_dev(np.ascontiguousarray(b_scale, dtype=np.float32))
+    out = f.gemm_blockscale(dA, dsa, dB, dsb, C=C)
+    assert f.get_status() == 0
+    return out.view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+def run_mxfp8(A, a_e8m0, B, b_e8m0, C=None):
+    import torch
+    import fp8_block_scaled_e4m3_gb300 as f
+    out = f.gemm_mxfp8(to_dev(A), to_dev(a_e8m0), to_dev(B), to_dev(b_e8m0), C=C)
+    assert f.get_status() == 0
+    return out.view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+def compare(gpu_bits, ref_bits, what=""):
+    """Apply the tolerance; return a dict of metrics (raises AssertionError on failure)."""
+    g = oracle.bf16_bits_to_float(gpu_bits).astype(np.float64)
+    o = oracle.bf16_bits_to_float(ref_bits).astype(np.float64)
+    assert g.shape == o.shape
+    assert np.all(np.isfinite(g)), f"{what}: non-finite GPU output"
+    err = np.abs(g - o)
+    bad = err > ATOL + RTOL * np.abs(o)
+    nrm = np.linalg.norm(o)
+    rel = float(np.linalg.norm(g - o) / nrm) if nrm > 0 else float(np.linalg.norm(g - o))
+    cos = float(np.dot(g.ravel(), o.ravel()) / (np.linalg.norm(g) * nrm)) if nrm > 0 else 1.0
+    m = {"maxabs": float(err.max()) if err.size else 0.0, "rel_l2": rel, "cos": cos,
+         "n_out_of_tol": int(bad.sum()), "n": int(g.size)}
+    if bad.any():
+        idx = np.argwhere(bad)
+        rows = np.unique(idx[:, 0] % 128)
+        cols = np.unique(idx[:, 1] % 256)
+        raise AssertionError(f"{what}: {m}; first bad {idx[:5].tolist()}, rows%128 {rows[:16].tolist()}, "
+                             f"cols%256 {cols[:16].tolist()}")
+    assert rel <= REL_L2, f"{what}: {m}"
+    return m

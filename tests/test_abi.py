@@ -1,0 +1,115 @@
+"""C-ABI library: loads, exports every declared symbol, host-side checks and
+layout helpers (CPU only; no call here reaches a CUDA launch)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "fp8bs.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from fp8_block_scaled_e4m3_gb300 import _build
+    _build.build()
+    import fp8_block_scaled_e4m3_gb300 as f
+    return f
+
+
+def declared_functions():
+    txt = open(HEADER).read()
+    txt = re.sub(r"/\*.*?\*/", "", txt, flags=re.S)
+    return sorted(set(re.findall(r"\b(fp8(?:bs|mx)_\w+)\s*\(", txt)))
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    assert "fp8bs_gemm" in names and "fp8mx_gemm" in names
+    assert len(names) >= 15
+
+
+def test_library_exports_every_declared_symbol(lib):
+    so = ctypes.CDLL(lib.LIBRARY_PATH)
+    missing = [n for n in declared_functions() if not hasattr(so, n)]
+    assert not missing, missing
+
+
+def test_shape_rules_rejected_before_launch(lib):
+    L = lib.lib()
+    P = ctypes.c_void_p(16)   # never dereferenced: shape checks come first
+    for f in (L.fp8bs_gemm, L.fp8mx_gemm):
+        assert f(P, P, P, P, P, 4, 8, 100, None) == -3        # K % 128
+        assert f(P, P, P, P, P, 4, 8, 0, None) == -3          # K < 128
+        assert f(P, P, P, P, P, 4, 12, 128, None) == -3       # N % 8
+        assert f(P, P, P, P, P, 4, 0, 128, None) == -3        # N < 8
+        assert f(P, P, P, P, P, -1, 8, 128, None) == -3       # M < 0
+        assert f(P, P, P, P, P, 4, 8, (1 << 20) + 128, None) == -3
+        assert f(None, None, None, None, None, 0, 8, 128, None) == 0   # M == 0 is a no-op
+        assert f(None, P, P, P, P, 4, 8, 128, None) == -1
+        assert f(P, P, P, P, None, 4, 8, 128, None) == -1
+
+
+def test_alignment_rejected_before_launch(lib):
+    L = lib.lib()
+    a16 = ctypes.c_void_p(1 << 20)
+    odd = ctypes.c_void_p((1 << 20) + 8)
+    odd4 = ctypes.c_void_p((1 << 20) + 2)
+    assert L.fp8bs_gemm(odd, a16, a16, a16, a16, 4, 8, 128, None) == -2
+    assert L.fp8bs_gemm(a16, odd, a16, a16, a16, 4, 8, 128, None) == -2
+    assert L.fp8bs_gemm(a16, a16, a16, odd4, a16, 4, 8, 128, None) == -2
+    assert L.fp8bs_gemm(a16, a16, a16, a16, odd, 4, 8, 128, None) == -2
+    assert L.fp8mx_gemm(a16, odd4, a16, a16, a16, 4, 8, 128, None) == -2
+    assert L.fp8mx_gemm(a16, a16, odd, a16, a16, 4, 8, 128, None) == -2
+
+
+def test_layout_helpers_bit_exact(lib):
+    L = lib.lib()
+    for M in list(range(1, 131)):
+        ld = (M + 3) // 4 * 4
+        assert L.fp8bs_a_scale_ld(M) == ld
+        for K in (128, 256, 768):
+            KB = K // 128
+            for kb in range(KB):
+                for m in (0, M // 2, M - 1):
+                    assert L.fp8bs_a_scale_index(m, kb, M) == kb * ld + m
+    for K in (128, 256, 768, 7168):
+        KB = K // 128
+        for n in range(0, 300, 7):
+            for kb in range(KB):
+                assert L.fp8bs_b_scale_index(n, kb, K) == (n // 128) * KB + kb
+                for g in range(4 * kb, 4 * kb + 4):
+                    assert L.fp8mx_scale_index(n, g, K) == n * (K // 32) + g
+
+
+def test_sf_atom_layout_is_a_bijection(lib):
+    L = lib.lib()
+    seen = set()
+    for r in range(128):
+        for j in range(4):
+            off = L.fp8mx_sf_atom_offset(r, j)
+            assert off == (r % 32) * 16 + (r // 32) * 4 + j
+            seen.add(off)
+    assert seen == set(range(512))
+
+
+def test_config_selection(lib):
+    # wide tiles for the large shapes, the narrow tile when a wide grid would starve the SMs
+    for M, N, K in [(4096, 2048, 7168), (16384, 1536, 7168), (16384, 7168, 768), (4096, 65536, 1536)]:
+        c = lib.decode_config(lib.select_config("bs", M, N, K, 152))
+        assert c["kind"] == "blockscale" and c["block_n"] == 256
+    c = lib.decode_config(lib.select_config("bs", 256, 512, 512, 152))
+    assert c["block_n"] == 128
+    assert lib.decode_config(lib.select_config("mx", 16384, 5120, 2048, 152))["kind"] == "mxfp8"
+    # raster streams the larger operand
+    assert lib.decode_config(lib.select_config("bs", 4096, 65536, 1536, 152))["raster"] == 0
+    assert lib.decode_config(lib.select_config("bs", 16384, 1536, 7168, 152))["raster"] == 1
+    assert lib.select_config("bs", 4, 12, 128, 152) == -3
+
+
+def test_status_strings(lib):
+    L = lib.lib()
+    for code in range(-7, 1):
+        assert L.fp8bs_status_string(code)
+    assert L.fp8bs_launches_per_call() == 1

@@ -1,0 +1,236 @@
+"""GPU path vs the CPU oracle (needs a GB300).
+
+Every case goes through the C ABI (via the ctypes binding) on seeded inputs and
+compares element by element with the oracle: bit-exact where the result is an
+exact integer, within the stated tolerance otherwise.
+"""
+import numpy as np
+import pytest
+
+import oracle
+import workloads
+from gpu_util import compare, run_blockscale, run_mxfp8, to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import fp8_block_scaled_e4m3_gb300  # noqa: F401  (fails loudly if the library is missing)
+
+
+def _int_codes(vals):
+    lut = {-2: 0xC0, -1: 0xB8, 0: 0x00, 1: 0x38, 2: 0x40}
+    return np.vectorize(lut.get)(vals).astype(np.uint8)
+
+
+# ---------------------------------------------------------------- exact cases
+
+@pytest.mark.parametrize("M,N,K", [(128, 256, 256), (256, 512, 512), (200, 136, 384)])
+def test_blockscale_integer_inputs_bit_exact(M, N, K):
+    rng = np.random.Generator(np.random.PCG64(M + N + K))
+    va = rng.integers(-1, 2, size=(M, K))
+    vb = rng.integers(-1, 2, size=(N, K))
+    A, B = _int_codes(va), _int_codes(vb)
+    sa = np.ones((M, K // 128), np.float32)
+    sb = np.ones(((N + 127) // 128, K // 128), np.float32)
+    got = run_blockscale(A, sa, B, sb)
+    ref = oracle.blockscale(A, sa, B, sb)
+    assert np.array_equal(got, ref)
+    exact = va @ vb.T
+    if np.abs(exact).max() <= 256:          # every such integer is a bf16 value
+        assert np.array_equal(oracle.bf16_bits_to_float(got), exact.astype(np.float32))
+
+
+@pytest.mark.parametrize("M,N,K", [(128, 256, 256), (200, 136, 384)])
+def test_mxfp8_integer_inputs_bit_exact(M, N, K):
+    rng = np.random.Generator(np.random.PCG64(7 + M))
+    va = rng.integers(-1, 2, size=(M, K))
+    vb = rng.integers(-1, 2, size=(N, K))
+    A, B = _int_codes(va), _int_codes(vb)
+    ea = np.full((M, K // 32), 127, np.uint8)
+    eb = np.full((N, K // 32), 127, np.uint8)
+    got = run_mxfp8(A, ea, B, eb)
+    assert np.array_equal(got, oracle.mxfp8(A, ea, B, eb))
+
+
+def test_blockscale_per_block_scales_bit_exact():
+    """Integer operands, power-of-two scales that differ per row, per K block and per N block."""
+    M, N, K = 256, 384, 512
+    rng = np.random.Generator(np.random.PCG64(21))
+    A = _int_codes(rng.integers(-2, 3, size=(M, K)))
+    B = _int_codes(rng.integers(-2, 3, size=(N, K)))
+    sa = np.ldexp(np.float32(1), rng.integers(-3, 4, size=(M, K // 128))).astype(np.float32)
+    sb = np.ldexp(np.float32(1), rng.integers(-3, 4, size=(N // 128, K // 128))).astype(np.float32)
+    assert np.array_equal(run_blockscale(A, sa, B, sb), oracle.blockscale(A, sa, B, sb))
+
+
+def test_mxfp8_per_group_scales_bit_exact():
+    """Integer operands with ue8m0 scales that differ per row and per 32-wide group:
+    pins which tensor-memory scale byte each row and K slice uses."""
+    M, N, K = 256, 512, 512
+    rng = np.random.Generator(np.random.PCG64(22))
+    A = _int_codes(rng.integers(-2, 3, size=(M, K)))
+    B = _int_codes(rng.integers(-2, 3, size=(N, K)))
+    ea = rng.integers(124, 131, size=(M, K // 32)).astype(np.uint8)
+    eb = rng.integers(124, 131, size=(N, K // 32)).astype(np.uint8)
+    got = run_mxfp8(A, ea, B, eb)
+    ref = oracle.mxfp8(A, ea, B, eb)
+    if not np.array_equal(got, ref):
+        bad = np.argwhere(got != ref)
+        raise AssertionError(f"{len(bad)} mismatches, rows%128 {np.unique(bad[:, 0] % 128)[:20]}, "
+                             f"cols%256 {np.unique(bad[:, 1] % 256)[:20]}")
+
+
+def test_zero_operand_gives_zero():
+    x = workloads.make_blockscale_inputs(256, 256, 256, seed=1)
+    got = run_blockscale(np.zeros_like(x.A), x.a_scale, x.B, x.b_scale)
+    assert np.all(got == 0)
+
+
+# -------------------------------------------------------- tolerance cases
+
+def test_blockscale_small_config_seed0():
+    """256 x 512 x 512, the smallest workload, full output."""
+    x = workloads.make_blockscale_inputs(256, 512, 512, seed=0)
+    compare(run_blockscale(x.A, x.a_scale, x.B, x.b_scale), oracle.blockscale(x.A, x.a_scale, x.B, x.b_scale),
+            "bs 256x512x512")
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 8, 128), (64, 128, 256), (127, 136, 128), (129, 264, 768),
+                                   (300, 520, 1280), (513, 1032, 384), (1000, 2056, 1024)])
+def test_blockscale_tails(M, N, K):
+    x = workloads.make_blockscale_inputs(M, N, K, seed=M)
+    compare(run_blockscale(x.A, x.a_scale, x.B, x.b_scale), oracle.blockscale(x.A, x.a_scale, x.B, x.b_scale),
+            f"bs {M}x{N}x{K}")
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 8, 128), (64, 256, 256), (127, 136, 1280), (300, 520, 2048),
+                                   (1024, 640, 1280)])
+def test_mxfp8_tails(M, N, K):
+    x = workloads.make_mxfp8_inputs(M, N, K, seed=M)
+    compare(run_mxfp8(x.A, x.a_e8m0, x.B, x.b_e8m0), oracle.mxfp8(x.A, x.a_e8m0, x.B, x.b_e8m0),
+            f"mx {M}x{N}x{K}")
+
+
+def test_scales_are_applied():
+    """A changed scale must change exactly the rows / blocks it governs."""
+    x = workloads.make_blockscale_inputs(256, 512, 512, seed=5)
+    base = run_blockscale(x.A, x.a_scale, x.B, x.b_scale)
+    sa = x.a_scale.copy()
+    sa[37, 2] *= np.float32(4.0)
+    changed = run_blockscale(x.A, sa, x.B, x.b_scale)
+    diff_rows = np.unique(np.argwhere(changed != base)[:, 0])
+    assert diff_rows.tolist() == [37]
+    sb = x.b_scale.copy()
+    sb[3, 1] *= np.float32(0.25)
+    changed = run_blockscale(x.A, x.a_scale, x.B, sb)
+    cols = np.unique(np.argwhere(changed != base)[:, 1])
+    assert cols.min() >= 384 and cols.max() < 512
+    y = workloads.make_mxfp8_inputs(256, 512, 512, seed=5)
+    mbase = run_mxfp8(y.A, y.a_e8m0, y.B, y.b_e8m0)
+    eb = y.b_e8m0.copy()
+    eb[300, :] += 1
+    ch = run_mxfp8(y.A, y.a_e8m0, y.B, eb)
+    assert np.unique(np.argwhere(ch != mbase)[:, 1]).tolist() == [300]
+    assert np.array_equal(oracle.bf16_bits_to_float(ch[:, 300]), 2 * oracle.bf16_bits_to_float(mbase[:, 300]))
+
+
+def test_blockscale_and_mxfp8_agree_on_power_of_two_scales():
+    rng = np.random.Generator(np.random.PCG64(9))
+    M, N, K = 256, 384, 768
+    x = workloads.make_blockscale_inputs(M, N, K, seed=9)
+    ja = rng.integers(-8, -2, size=(M, K // 128))
+    jb = rng.integers(-10, -4, size=((N + 127) // 128, K // 128))
+    sa = np.ldexp(np.float32(1), ja).astype(np.float32)
+    sb = np.ldexp(np.float32(1), jb).astype(np.float32)
+    ea = np.repeat(ja + 127, 4, axis=1).astype(np.uint8)
+    eb = np.repeat(np.repeat(jb + 127, 128, axis=0)[:N], 4, axis=1).astype(np.uint8)
+    g1 = run_blockscale(x.A, sa, x.B, sb)
+    g2 = run_mxfp8(x.A, ea, x.B, eb)
+    ref = oracle.blockscale(x.A, sa, x.B, sb)
+    compare(g1, ref, "bs pow2")
+    compare(g2, ref, "mx pow2")
+
+
+def test_repeat_calls_bitwise_identical_and_config_recorded():
+    import fp8_block_scaled_e4m3_gb300 as f
+    x = workloads.make_blockscale_inputs(512, 1024, 1024, seed=3)
+    a = run_blockscale(x.A, x.a_scale, x.B, x.b_scale)
+    cid = f.last_config_id()
+    b = run_blockscale(x.A, x.a_scale, x.B, x.b_scale)
+    assert np.array_equal(a, b)
+    assert f.decode_config(cid)["kind"] == "blockscale"
+
+
+def test_pack_a_scale_bit_exact():
+    import torch
+    import fp8_block_scaled_e4m3_gb300 as f
+    rng = np.random.Generator(np.random.PCG64(4))
+    for M, K in [(1, 128), (5, 256), (130, 768), (4097, 7168)]:
+        sa = rng.standard_normal((M, K // 128)).astype(np.float32)
+        out = f.pack_a_scale(to_dev(sa), K)
+        torch.cuda.synchronize()
+        assert np.array_equal(out.cpu().numpy(), workloads.a_scale_to_kmajor(sa))
+
+
+def test_m_zero_is_noop():
+    import torch
+    import fp8_block_scaled_e4m3_gb300 as f
+    A = torch.empty((0, 128), dtype=torch.uint8, device="cuda")
+    B = torch.zeros((8, 128), dtype=torch.uint8, device="cuda")
+    sa = torch.zeros((1, 0), dtype=torch.float32, device="cuda")
+    sb = torch.ones((1, 1), dtype=torch.float32, device="cuda")
+    C = f.gemm_blockscale(A, sa, B, sb)
+    assert C.shape == (0, 8)
+
+
+# ------------------------------------------------ full-size workloads (sampled rows)
+
+def _sample_rows(M, rng):
+    """Two rows from every 128-row tile (random offsets) plus the first and last row."""
+    rows = set([0, M - 1])
+    for t in range(0, M, 128):
+        hi = min(128, M - t)
+        rows.update((t + rng.integers(0, hi, size=2)).tolist())
+    return sorted(rows)
+
+
+def _check_full_size(kind, M, N, K, seed):
+    x = workloads.make_inputs(kind, M, N, K, seed)
+    if kind == "bs":
+        got = run_blockscale(x.A, x.a_scale, x.B, x.b_scale)
+    else:
+        got = run_mxfp8(x.A, x.a_e8m0, x.B, x.b_e8m0)
+    rng = np.random.Generator(np.random.PCG64(1000 + seed))
+    rows = _sample_rows(M, rng)
+    # the oracle on the sampled rows only: compute row blocks [r, r+1)
+    refs = []
+    for r in rows:
+        if kind == "bs":
+            refs.append(oracle.blockscale(x.A, x.a_scale, x.B, x.b_scale, rows=(r, r + 1)))
+        else:
+            refs.append(oracle.mxfp8(x.A, x.a_e8m0, x.B, x.b_e8m0, rows=(r, r + 1)))
+    ref = np.concatenate(refs, axis=0)
+    return compare(got[rows], ref, f"{kind} {M}x{N}x{K} seed {seed}")
+
+
+@pytest.mark.parametrize("seed", [0, 1, 2, 3])
+def test_full_blockscale_narrowN_4096x2048x7168(seed):
+    _check_full_size("bs", 4096, 2048, 7168, seed)
+
+
+@pytest.mark.parametrize("name", ["bs_narrowN_16384x1536x7168", "bs_Klight_16384x7168x768",
+                                  "bs_wideN_4096x65536x1536"])
+def test_full_blockscale_other_shapes(name):
+    w = workloads.WORKLOADS[name]
+    _check_full_size("bs", w["M"], w["N"], w["K"], 0)
+
+
+@pytest.mark.parametrize("M", [1024, 2048, 4096, 16384])
+@pytest.mark.parametrize("N,K", [(5120, 2048), (8192, 1280)])
+def test_full_mxfp8(M, N, K):
+    _check_full_size("mx", M, N, K, 0)
