@@ -12,8 +12,8 @@ HEADER = os.path.join(ROOT, "include", "fp8bs.h")
 
 @pytest.fixture(scope="module")
 def lib():
-    from fp8_block_scaled_e4m3_gb300 import _build
-    _build.build()
+    import __graft_entry__
+    __graft_entry__._build_module().build()
     import fp8_block_scaled_e4m3_gb300 as f
     return f
 
