@@ -29,6 +29,10 @@ _i64 = ctypes.c_int64
 _SIGS = {
     "fp8bs_gemm": (_i, [_p, _p, _p, _p, _p, _i, _i, _i, _p]),
     "fp8mx_gemm": (_i, [_p, _p, _p, _p, _p, _i, _i, _i, _p]),
+    "fp8mx_gemm_packed": (_i, [_p, _p, _p, _p, _p, _i, _i, _i, _p]),
+    "fp8mx_packed_scale_bytes": (_i64, [_i, _i]),
+    "fp8mx_pack_scales": (_i, [_p, _p, _i, _i, _p]),
+    "fp8mx_launches_per_call": (_i, []),
     "fp8bs_a_scale_ld": (_i64, [_i]),
     "fp8bs_a_scale_index": (_i64, [_i, _i, _i]),
     "fp8bs_b_scale_index": (_i64, [_i, _i, _i]),
@@ -139,6 +143,40 @@ def gemm_mxfp8(A, a_e8m0, B, b_e8m0, C=None, stream=None):
                          _fp8_ptr(B, "B", (N, K)), _dev_ptr(b_e8m0, "b_e8m0", (N, K // 32)),
                          _dev_ptr(C, "C", (M, N)), M, N, K, _stream_ptr(stream))
     _check(rc, "fp8mx_gemm")
+    return C
+
+
+def packed_scale_bytes(rows: int, K: int) -> int:
+    return int(_lib.fp8mx_packed_scale_bytes(rows, K))
+
+
+def pack_mx_scales(e8m0, K: int, out=None, stream=None):
+    """ue8m0 bytes [rows, K/32] -> the packed scale-factor layout gemm_mxfp8_packed takes."""
+    torch = _torch()
+    rows = e8m0.shape[0]
+    if out is None:
+        out = torch.empty((packed_scale_bytes(rows, K),), dtype=torch.uint8, device=e8m0.device)
+    if e8m0.dtype != torch.uint8:
+        raise TypeError("ue8m0 scales must be uint8")
+    rc = _lib.fp8mx_pack_scales(_dev_ptr(e8m0, "e8m0", (rows, K // 32)),
+                                _dev_ptr(out, "out", (packed_scale_bytes(rows, K),)), rows, K, _stream_ptr(stream))
+    _check(rc, "fp8mx_pack_scales")
+    return out
+
+
+def gemm_mxfp8_packed(A, a_sf, B, b_sf, C=None, stream=None):
+    """MXFP8 GEMM on packed scale factors (from pack_mx_scales); one kernel, no allocation."""
+    torch = _torch()
+    M, K = A.shape
+    N = B.shape[0]
+    if C is None:
+        C = torch.empty((M, N), dtype=torch.bfloat16, device=A.device)
+    if a_sf.dtype != torch.uint8 or b_sf.dtype != torch.uint8 or C.dtype != torch.bfloat16:
+        raise TypeError("packed scales must be uint8 and C bfloat16")
+    rc = _lib.fp8mx_gemm_packed(_fp8_ptr(A, "A", (M, K)), _dev_ptr(a_sf, "a_sf", (packed_scale_bytes(M, K),)),
+                                _fp8_ptr(B, "B", (N, K)), _dev_ptr(b_sf, "b_sf", (packed_scale_bytes(N, K),)),
+                                _dev_ptr(C, "C", (M, N)), M, N, K, _stream_ptr(stream))
+    _check(rc, "fp8mx_gemm_packed")
     return C
 
 

@@ -9,7 +9,7 @@
 #include <stdint.h>
 #include <string.h>
 
-#include "../../include/fp8bs.h"
+#include "fp8bs.h"
 #include "common.cuh"
 
 namespace fp8bs {
@@ -33,6 +33,7 @@ struct DeviceState {
     int status = FP8BS_OK;       // result of the set-up
     int num_sms = 0;
     int *status_ptr = nullptr;   // device address of g_status_word
+    cudaMemPool_t pool = nullptr; // stream-ordered pool for fp8mx_gemm's packed scales
 };
 
 std::mutex g_mutex;
@@ -62,6 +63,15 @@ int ensure_device(int &dev, DeviceState *&st)
     if (major != 10 || minor != 3)
         return st->status = FP8BS_ERR_UNSUPPORTED_DEVICE;
     if (cudaGetSymbolAddress(reinterpret_cast<void **>(&st->status_ptr), g_status_word) != cudaSuccess)
+        return st->status = FP8BS_ERR_CUDA;
+    cudaMemPoolProps props = {};
+    props.allocType = cudaMemAllocationTypePinned;
+    props.location.type = cudaMemLocationTypeDevice;
+    props.location.id = dev;
+    if (cudaMemPoolCreate(&st->pool, &props) != cudaSuccess)
+        return st->status = FP8BS_ERR_CUDA;
+    uint64_t keep = UINT64_MAX;   // keep freed workspace in the pool between calls
+    if (cudaMemPoolSetAttribute(st->pool, cudaMemPoolAttrReleaseThreshold, &keep) != cudaSuccess)
         return st->status = FP8BS_ERR_CUDA;
     if (!g_encode) {
         cudaDriverEntryPointQueryResult q;
@@ -130,6 +140,46 @@ Config choose_config(int kind, int M, int N, int K, int num_sms)
     return c;
 }
 
+// Repack ue8m0 bytes [rows][K/32] into 512-byte scale-factor atoms (see
+// mx_kernel.cu): one thread per (row, 128-wide K step), K steps fastest so the
+// 4-byte reads of a row are contiguous. Two tensors (A and B) in one launch.
+__global__ void pack_scales_kernel(const uint8_t *__restrict__ e0, uint8_t *__restrict__ p0, int rows0,
+                                   const uint8_t *__restrict__ e1, uint8_t *__restrict__ p1, int rows1, int KS)
+{
+    const int64_t n0 = static_cast<int64_t>((rows0 + 127) / 128) * 128 * KS;
+    const int64_t n1 = static_cast<int64_t>((rows1 + 127) / 128) * 128 * KS;
+    const int G = KS * 4;
+    for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n0 + n1;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const bool first = i < n0;
+        const int64_t idx = first ? i : i - n0;
+        const uint8_t *e = first ? e0 : e1;
+        uint8_t *p = first ? p0 : p1;
+        const int rows = first ? rows0 : rows1;
+        const int row = static_cast<int>(idx / KS);
+        const int ks = static_cast<int>(idx - static_cast<int64_t>(row) * KS);
+        uint32_t v = 0;
+        if (row < rows)
+            v = *reinterpret_cast<const uint32_t *>(e + static_cast<int64_t>(row) * G + 4 * ks);
+        const int64_t atom = static_cast<int64_t>(row / 128) * KS + ks;
+        *reinterpret_cast<uint32_t *>(p + atom * 512 + sf_atom_offset(row % 128, 0)) = v;
+    }
+}
+
+int launch_pack_scales(const uint8_t *e0, uint8_t *p0, int rows0, const uint8_t *e1, uint8_t *p1, int rows1, int K,
+                       int num_sms, cudaStream_t stream)
+{
+    const int KS = K / 128;
+    const int64_t total = (static_cast<int64_t>((rows0 + 127) / 128) + (rows1 + 127) / 128) * 128 * KS;
+    int64_t blocks = (total + 255) / 256;
+    if (blocks > static_cast<int64_t>(num_sms) * 16)
+        blocks = static_cast<int64_t>(num_sms) * 16;
+    if (blocks < 1)
+        blocks = 1;
+    pack_scales_kernel<<<static_cast<int>(blocks), 256, 0, stream>>>(e0, p0, rows0, e1, p1, rows1, KS);
+    return cudaGetLastError() == cudaSuccess ? FP8BS_OK : FP8BS_ERR_LAUNCH;
+}
+
 } // namespace host
 } // namespace fp8bs
 
@@ -163,8 +213,8 @@ int fp8bs_gemm(const void *A, const float *a_scale, const void *B, const float *
                    CU_TENSOR_MAP_SWIZZLE_128B) ||
         !encode_2d(&tmSA, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, a_scale, ld_sa, KB, ld_sa * 4, 128, 1,
                    CU_TENSOR_MAP_SWIZZLE_NONE) ||
-        !encode_2d(&tmC, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, C, N, M, static_cast<uint64_t>(N) * 2, 32, 32,
-                   CU_TENSOR_MAP_SWIZZLE_64B))
+        !encode_2d(&tmC, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, C, N, M, static_cast<uint64_t>(N) * 2, kCChunkCols, 32,
+                   CU_TENSOR_MAP_SWIZZLE_32B))
         return FP8BS_ERR_LAUNCH;
     GemmArgs args = {};
     args.M = M;
@@ -188,6 +238,78 @@ int fp8bs_gemm(const void *A, const float *a_scale, const void *B, const float *
     return FP8BS_OK;
 }
 
+int fp8mx_gemm_packed(const void *A, const uint8_t *a_sf, const void *B, const uint8_t *b_sf, void *C, int M,
+                      int N, int K, void *stream)
+{
+    int rc = check_shape(M, N, K);
+    if (rc)
+        return rc;
+    if (M == 0)
+        return FP8BS_OK;
+    if (!A || !a_sf || !B || !b_sf || !C)
+        return FP8BS_ERR_NULL;
+    if (!aligned(A, 16) || !aligned(a_sf, 16) || !aligned(B, 16) || !aligned(b_sf, 16) || !aligned(C, 16))
+        return FP8BS_ERR_ALIGN;
+    int dev;
+    DeviceState *st;
+    if ((rc = ensure_device(dev, st)))
+        return rc;
+    const Config cfg = choose_config(2, M, N, K, st->num_sms);
+    CUtensorMap tmA, tmB, tmC;
+    if (!encode_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, A, K, M, K, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, B, K, N, K, 128, cfg.block_n,
+                   CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_2d(&tmC, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, C, N, M, static_cast<uint64_t>(N) * 2, kCChunkCols, 32,
+                   CU_TENSOR_MAP_SWIZZLE_32B))
+        return FP8BS_ERR_LAUNCH;
+    GemmArgs args = {};
+    args.M = M;
+    args.N = N;
+    args.K = K;
+    args.raster.m_tiles = (M + kBlockM - 1) / kBlockM;
+    args.raster.n_tiles = (N + cfg.block_n - 1) / cfg.block_n;
+    args.raster.raster = cfg.raster;
+    args.raster.group = cfg.group;
+    args.a_sf = a_sf;
+    args.b_sf = b_sf;
+    args.status = st->status_ptr;
+    args.wait_limit_ns = g_wait_limit_ns.load();
+    const int tiles = args.raster.num_tiles();
+    const int grid = tiles < st->num_sms ? tiles : st->num_sms;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = cfg.block_n == 256 ? launch_mxfp8<256, 4>(tmA, tmB, tmC, args, grid, s)
+                                       : launch_mxfp8<128, 6>(tmA, tmB, tmC, args, grid, s);
+    if (e != cudaSuccess)
+        return FP8BS_ERR_LAUNCH;
+    t_last_config = config_id(2, cfg);
+    return FP8BS_OK;
+}
+
+int64_t fp8mx_packed_scale_bytes(int rows, int K)
+{
+    if (rows < 0 || K < 128 || (K % 128) != 0)
+        return FP8BS_ERR_SHAPE;
+    return static_cast<int64_t>((rows + 127) / 128) * (K / 128) * 512;
+}
+
+int fp8mx_pack_scales(const uint8_t *e8m0, uint8_t *packed, int rows, int K, void *stream)
+{
+    if (rows < 0 || K < 128 || (K % 128) != 0 || K > (1 << 20))
+        return FP8BS_ERR_SHAPE;
+    if (rows == 0)
+        return FP8BS_OK;
+    if (!e8m0 || !packed)
+        return FP8BS_ERR_NULL;
+    if (!aligned(e8m0, 4) || !aligned(packed, 16))
+        return FP8BS_ERR_ALIGN;
+    int dev;
+    DeviceState *st;
+    int rc = ensure_device(dev, st);
+    if (rc)
+        return rc;
+    return launch_pack_scales(e8m0, packed, rows, e8m0, packed, 0, K, st->num_sms, static_cast<cudaStream_t>(stream));
+}
+
 int fp8mx_gemm(const void *A, const uint8_t *a_e8m0, const void *B, const uint8_t *b_e8m0, void *C, int M, int N,
                int K, void *stream)
 {
@@ -204,35 +326,20 @@ int fp8mx_gemm(const void *A, const uint8_t *a_e8m0, const void *B, const uint8_
     DeviceState *st;
     if ((rc = ensure_device(dev, st)))
         return rc;
-    const Config cfg = choose_config(2, M, N, K, st->num_sms);
-    CUtensorMap tmA, tmB, tmC;
-    if (!encode_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, A, K, M, K, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !encode_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, B, K, N, K, 128, cfg.block_n,
-                   CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !encode_2d(&tmC, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, C, N, M, static_cast<uint64_t>(N) * 2, 32, 32,
-                   CU_TENSOR_MAP_SWIZZLE_64B))
-        return FP8BS_ERR_LAUNCH;
-    GemmArgs args = {};
-    args.M = M;
-    args.N = N;
-    args.K = K;
-    args.raster.m_tiles = (M + kBlockM - 1) / kBlockM;
-    args.raster.n_tiles = (N + cfg.block_n - 1) / cfg.block_n;
-    args.raster.raster = cfg.raster;
-    args.raster.group = cfg.group;
-    args.a_e8m0 = a_e8m0;
-    args.b_e8m0 = b_e8m0;
-    args.status = st->status_ptr;
-    args.wait_limit_ns = g_wait_limit_ns.load();
-    const int tiles = args.raster.num_tiles();
-    const int grid = tiles < st->num_sms ? tiles : st->num_sms;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    cudaError_t e = cfg.block_n == 256 ? launch_mxfp8<256, 4>(tmA, tmB, tmC, args, grid, s)
-                                       : launch_mxfp8<128, 6>(tmA, tmB, tmC, args, grid, s);
-    if (e != cudaSuccess)
-        return FP8BS_ERR_LAUNCH;
-    t_last_config = config_id(2, cfg);
-    return FP8BS_OK;
+    const size_t a_bytes = static_cast<size_t>(fp8mx_packed_scale_bytes(M, K));
+    const size_t b_bytes = static_cast<size_t>(fp8mx_packed_scale_bytes(N, K));
+    void *ws = nullptr;
+    if (cudaMallocFromPoolAsync(&ws, a_bytes + b_bytes, st->pool, s) != cudaSuccess)
+        return FP8BS_ERR_CUDA;
+    uint8_t *a_sf = static_cast<uint8_t *>(ws);
+    uint8_t *b_sf = a_sf + a_bytes;
+    rc = launch_pack_scales(a_e8m0, a_sf, M, b_e8m0, b_sf, N, K, st->num_sms, s);
+    if (rc == FP8BS_OK)
+        rc = fp8mx_gemm_packed(A, a_sf, B, b_sf, C, M, N, K, stream);
+    if (cudaFreeAsync(ws, s) != cudaSuccess && rc == FP8BS_OK)
+        rc = FP8BS_ERR_CUDA;
+    return rc;
 }
 
 int64_t fp8bs_a_scale_ld(int M) { return (static_cast<int64_t>(M) + 3) / 4 * 4; }
@@ -343,6 +450,8 @@ int fp8mx_select_config(int M, int N, int K, int num_sms)
 }
 
 int fp8bs_launches_per_call(void) { return 1; }
+
+int fp8mx_launches_per_call(void) { return 2; }
 
 void fp8bs_set_wait_limit_ns(uint64_t ns)
 {

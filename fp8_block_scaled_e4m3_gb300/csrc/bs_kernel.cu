@@ -7,19 +7,23 @@
 // promote per K block, because those scales are not powers of two).
 //
 // Persistent, warp-specialised, one CTA per SM, 12 warps (3 warpgroups):
-//   warp 0      TMA producer: A tile [128 x 128] e4m3, B tile [BN x 128] e4m3 and
-//               the a_scale slice [128] fp32 of one K block into stage s of a
-//               STAGES-deep shared-memory ring (full/empty mbarriers).
+//   warp 0      TMA producer: A tile [128 x 128] e4m3 and B tile [BN x 128] e4m3 of
+//               one K block into stage s of a STAGES-deep shared-memory ring
+//               (full/empty mbarriers, a stage is freed by the MMA commit), and
+//               the a_scale slice [128] fp32 of the K block into a separate
+//               kSaSlots-deep ring freed by the promote warps.
 //   warp 1      TMEM allocator + single-thread MMA issuer: four
 //               tcgen05.mma.kind::f8f6f4 (M128 x BN x K32) overwrite TMEM partial
-//               buffer (kb & 1) with P_kb; tcgen05.commit releases the stage and
+//               buffer (kb % NBUF) with P_kb, NBUF = 512 / BN buffers (2 for
+//               BN = 256, 4 for BN = 128, so the MMA can run NBUF-1 K blocks
+//               ahead of the promote); tcgen05.commit releases the stage and
 //               signals the buffer.
 //   warps 2,3   idle (they complete warpgroup 0, which gives its registers away)
 //   warps 4..11 promote + epilogue: warp w reads TMEM lanes 32*(w%4).., column half
 //               (w-4)/4, so each thread owns one row of C and BN/2 columns, all
 //               in one 128-column N block (one b_scale). Per K block:
 //               acc += P_kb * (sa * sb) in fp32 registers; the TMEM buffer is
-//               released right after the loads, so MMA(kb+1) overlaps promote(kb).
+//               released right after the loads, so MMA(kb+1..) overlaps promote(kb).
 //               After the last K block: bf16 convert, 64-byte-swizzled staging,
 //               TMA store (tails clipped by the tensor map).
 // Registers: the launch gives 168 per thread (3 warps per SM sub-partition);
@@ -33,6 +37,7 @@ namespace fp8bs {
 constexpr int kBsThreads = (4 + kEpiWarps) * 32;
 constexpr int kBsRegsLow = 40;
 constexpr int kBsRegsHigh = 232;
+constexpr int kSaSlots = 16;   // a_scale ring depth (>= STAGES + NBUF, so it never holds back A/B)
 
 template <int BN, int STAGES>
 struct BsLayout {
@@ -42,13 +47,15 @@ struct BsLayout {
     static constexpr int OFF_A = 0;
     static constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
     static constexpr int OFF_SA = OFF_B + STAGES * B_BYTES;
-    static constexpr int OFF_C = (OFF_SA + STAGES * SA_BYTES + 1023) / 1024 * 1024;
+    static constexpr int OFF_C = (OFF_SA + kSaSlots * SA_BYTES + 1023) / 1024 * 1024;
     static constexpr int OFF_BAR = OFF_C + kEpiWarps * kCStageBytes;
-    static constexpr int NBAR = 2 * STAGES + 5;  // full[S], empty[S], tfull[2], tempty[2], mma_done
+    static constexpr int NBUF = 512 / BN;        // TMEM partial buffers
+    // full[S], empty[S], tfull[NBUF], tempty[NBUF], mma_done, sa_full[kSaSlots], sa_empty[kSaSlots]
+    static constexpr int NBAR = 2 * STAGES + 2 * NBUF + 1 + 2 * kSaSlots;
     static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
     static constexpr int BYTES = OFF_MISC + 16;
     static constexpr int DYN_SMEM = BYTES + 1024;   // slack to align the base to 1024
-    static constexpr int TMEM_COLS = 2 * BN <= 32 ? 32 : (2 * BN <= 64 ? 64 : (2 * BN <= 128 ? 128 : (2 * BN <= 256 ? 256 : 512)));
+    static constexpr int TMEM_COLS = 512;
     static_assert(DYN_SMEM <= 232448, "shared memory budget");
     static_assert(BN == 128 || BN == 256, "tile width");
 };
@@ -73,17 +80,23 @@ __global__ void __launch_bounds__(kBsThreads, 1)
     auto full_bar = [&](int s) { return sbase + L::OFF_BAR + 8u * s; };
     auto empty_bar = [&](int s) { return sbase + L::OFF_BAR + 8u * (STAGES + s); };
     auto tfull_bar = [&](int b) { return sbase + L::OFF_BAR + 8u * (2 * STAGES + b); };
-    auto tempty_bar = [&](int b) { return sbase + L::OFF_BAR + 8u * (2 * STAGES + 2 + b); };
-    const uint32_t mma_done_bar = sbase + L::OFF_BAR + 8u * (2 * STAGES + 4);
+    auto tempty_bar = [&](int b) { return sbase + L::OFF_BAR + 8u * (2 * STAGES + L::NBUF + b); };
+    const uint32_t mma_done_bar = sbase + L::OFF_BAR + 8u * (2 * STAGES + 2 * L::NBUF);
+    auto sa_full_bar = [&](int a) { return sbase + L::OFF_BAR + 8u * (2 * STAGES + 2 * L::NBUF + 1 + a); };
+    auto sa_empty_bar = [&](int a) { return sbase + L::OFF_BAR + 8u * (2 * STAGES + 2 * L::NBUF + 1 + kSaSlots + a); };
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + L::OFF_MISC);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::OFF_MISC + 4);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
             ptx::mbar_init(full_bar(s), 1);
-            ptx::mbar_init(empty_bar(s), 1 + kEpiWarps);   // MMA commit + every promote warp (a_scale slice)
+            ptx::mbar_init(empty_bar(s), 1);              // MMA commit
         }
-        for (int b = 0; b < 2; ++b) {
+        for (int a = 0; a < kSaSlots; ++a) {
+            ptx::mbar_init(sa_full_bar(a), 1);
+            ptx::mbar_init(sa_empty_bar(a), kEpiWarps);   // every promote warp has read the slice
+        }
+        for (int b = 0; b < L::NBUF; ++b) {
             ptx::mbar_init(tfull_bar(b), 1);
             ptx::mbar_init(tempty_bar(b), kEpiWarps);
         }
@@ -116,14 +129,18 @@ __global__ void __launch_bounds__(kBsThreads, 1)
                 for (int kb = 0; kb < KB; ++kb, ++it) {
                     const int s = it % STAGES;
                     const uint32_t ph = (it / STAGES) & 1;
-                    if (!wait_bounded(empty_bar(s), ph ^ 1, abort_flag, args)) {
+                    const int a = it % kSaSlots;
+                    const uint32_t aph = (it / kSaSlots) & 1;
+                    if (!wait_bounded(empty_bar(s), ph ^ 1, abort_flag, args) ||
+                        !wait_bounded(sa_empty_bar(a), aph ^ 1, abort_flag, args)) {
                         ok = false;
                         break;
                     }
-                    ptx::mbar_arrive_expect_tx(full_bar(s), L::A_BYTES + L::B_BYTES + L::SA_BYTES);
+                    ptx::mbar_arrive_expect_tx(full_bar(s), L::A_BYTES + L::B_BYTES);
                     ptx::tma_load_2d(sbase + L::OFF_A + s * L::A_BYTES, &tmA, full_bar(s), kb * kBlockK, mb * kBlockM);
                     ptx::tma_load_2d(sbase + L::OFF_B + s * L::B_BYTES, &tmB, full_bar(s), kb * kBlockK, nb * BN);
-                    ptx::tma_load_2d(sbase + L::OFF_SA + s * L::SA_BYTES, &tmSA, full_bar(s), mb * kBlockM, kb);
+                    ptx::mbar_arrive_expect_tx(sa_full_bar(a), L::SA_BYTES);
+                    ptx::tma_load_2d(sbase + L::OFF_SA + a * L::SA_BYTES, &tmSA, sa_full_bar(a), mb * kBlockM, kb);
                 }
             }
             // Every load issued must have landed before the CTA exits.
@@ -131,6 +148,11 @@ __global__ void __launch_bounds__(kBsThreads, 1)
                 const int uses = it > s ? (it - s + STAGES - 1) / STAGES : 0;
                 if (uses > 0)
                     wait_teardown(full_bar(s), (uses - 1) & 1, args);
+            }
+            for (int a = 0; a < kSaSlots; ++a) {
+                const int uses = it > a ? (it - a + kSaSlots - 1) / kSaSlots : 0;
+                if (uses > 0)
+                    wait_teardown(sa_full_bar(a), (uses - 1) & 1, args);
             }
         }
     } else if (warp == 1) {
@@ -143,8 +165,8 @@ __global__ void __launch_bounds__(kBsThreads, 1)
                 for (int kb = 0; kb < KB; ++kb, ++it) {
                     const int s = it % STAGES;
                     const uint32_t ph = (it / STAGES) & 1;
-                    const int buf = it & 1;
-                    const uint32_t tph = (it >> 1) & 1;
+                    const int buf = it % L::NBUF;
+                    const uint32_t tph = (it / L::NBUF) & 1;
                     if (!wait_bounded(tempty_bar(buf), tph ^ 1, abort_flag, args) ||
                         !wait_bounded(full_bar(s), ph, abort_flag, args)) {
                         ok = false;
@@ -182,8 +204,11 @@ __global__ void __launch_bounds__(kBsThreads, 1)
                                  : 0;
         const int total = my_tiles * KB;
 
-        // b_scale for flattened step g (tile g/KB of this CTA, K block g%KB).
-        auto sb_load = [&](int g) -> float {
+        // b_scale of flattened step g (tile g/KB of this CTA, K block g%KB) for
+        // this warp's 128-column N block. Lane l of the warp loads step 32*b + l
+        // of batch b; the value for step g is taken with a shuffle. Batch b+1 is
+        // requested when batch b starts, so its loads have 32 K blocks to land.
+        auto sb_lane_load = [&](int g) -> float {
             if (g >= total)
                 return 0.f;
             const int ti = g / KB;
@@ -195,7 +220,8 @@ __global__ void __launch_bounds__(kBsThreads, 1)
                 return 0.f;
             return ptx::ldg_nc_f32(args.b_scale + static_cast<size_t>(nblk) * KB + kb);
         };
-        float sbq0 = sb_load(0), sbq1 = sb_load(1), sbq2 = sb_load(2);
+        float sb_cur = sb_lane_load(lane);
+        float sb_next = sb_lane_load(32 + lane);
 
         float acc[HALF];
         int it = 0;
@@ -207,21 +233,22 @@ __global__ void __launch_bounds__(kBsThreads, 1)
             for (int j = 0; j < HALF; ++j)
                 acc[j] = 0.f;
             for (int kb = 0; kb < KB; ++kb, ++it) {
-                const float sb = sbq0;
-                sbq0 = sbq1;
-                sbq1 = sbq2;
-                sbq2 = sb_load(it + 3);
-                const int s = it % STAGES;
-                const uint32_t ph = (it / STAGES) & 1;
-                const int buf = it & 1;
-                const uint32_t tph = (it >> 1) & 1;
+                const float sb = __shfl_sync(0xffffffffu, sb_cur, it & 31);
+                if ((it & 31) == 31) {
+                    sb_cur = sb_next;
+                    sb_next = sb_lane_load(it + 33 + lane);
+                }
+                const int a = it % kSaSlots;
+                const uint32_t aph = (it / kSaSlots) & 1;
+                const int buf = it % L::NBUF;
+                const uint32_t tph = (it / L::NBUF) & 1;
                 if (!wait_bounded_warp(tfull_bar(buf), tph, abort_flag, args) ||
-                    !wait_bounded_warp(full_bar(s), ph, abort_flag, args)) {
+                    !wait_bounded_warp(sa_full_bar(a), aph, abort_flag, args)) {
                     ok = false;
                     break;
                 }
                 ptx::tc_fence_after();
-                const float sa = reinterpret_cast<const float *>(smem + L::OFF_SA + s * L::SA_BYTES)[row];
+                const float sa = reinterpret_cast<const float *>(smem + L::OFF_SA + a * L::SA_BYTES)[row];
                 const float scale = sa * sb;
                 const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                                        static_cast<uint32_t>(buf * BN + wg * HALF);
@@ -242,7 +269,7 @@ __global__ void __launch_bounds__(kBsThreads, 1)
                 __syncwarp();
                 if (lane == 0) {
                     ptx::mbar_arrive(tempty_bar(buf));
-                    ptx::mbar_arrive(empty_bar(s));
+                    ptx::mbar_arrive(sa_empty_bar(a));
                 }
             }
             if (!ok)
@@ -250,8 +277,8 @@ __global__ void __launch_bounds__(kBsThreads, 1)
             const int x0 = nb * BN + wg * HALF;
             const int y0 = mb * kBlockM + q * 32;
 #pragma unroll
-            for (int c = 0; c < HALF / 32; ++c)
-                store_c_chunk(&tmC, cstage, lane, acc + c * 32, x0 + c * 32, y0, args.M, args.N);
+            for (int c = 0; c < HALF / kCChunkCols; ++c)
+                store_c_chunk(&tmC, cstage, lane, c, acc + c * kCChunkCols, x0 + c * kCChunkCols, y0, args.M, args.N);
         }
         if (lane == 0)
             ptx::bulk_wait_all();

@@ -7,25 +7,27 @@
 // (scale_vec::1X: one scale byte per row per 32-wide K slice) accumulates over
 // the whole K extent in tensor memory.
 //
-// Persistent, warp-specialised, one CTA per SM, 11 warps:
-//   warp 0       TMA producer: A [128 x 128] and B [BN x 128] e4m3 per 128-wide K step.
-//   warp 1       TMEM allocator + single-thread issuer: tcgen05.cp of the step's
-//                scale-factor atoms into TMEM, then four block-scaled MMAs
-//                (scale byte id = the 32-wide slice inside the step).
-//   warp 2       scale-factor stager: reads the quantiser's row-major ue8m0 bytes
-//                ([rows][K/32], 4 bytes per row and step) with plain loads, a few
-//                steps ahead, and writes them into 512-byte atoms in the stage
-//                (32 rows x 16 bytes, the image tcgen05.cp 32x128b.warpx4 copies).
-//                Row strides of K/32 bytes are not 16-byte multiples in general
-//                (K = 1280 gives 40), so these rows cannot be TMA tensors.
-//   warps 3..10  epilogue: drain the fp32 accumulator (128 columns per thread),
+// Persistent, warp-specialised, one CTA per SM, 10 warps:
+//   warp 0       TMA producer: A [128 x 128] and B [BN x 128] e4m3 per 128-wide K
+//                step, plus the step's scale-factor atoms (512 bytes per 128 rows)
+//                from the packed scale layout, all on one mbarrier.
+//   warp 1       TMEM allocator + single-thread issuer: tcgen05.cp of the atoms
+//                into TMEM (32x128b.warpx4), then four block-scaled MMAs (scale
+//                byte id = the 32-wide slice inside the step).
+//   warps 2..9   epilogue: drain the fp32 accumulator (128 columns per thread),
 //                release it to the next tile's MMAs, bf16 convert, TMA store.
+//
+// Packed scale layout (written by fp8mx_pack_scales from the quantiser's
+// row-major [rows][K/32] bytes, which are not TMA-addressable because a row of
+// K/32 bytes is not a 16-byte multiple in general): for 128-row block rb and
+// K step ks, a 512-byte atom at ((rb * K/128) + ks) * 512 holding byte j of row
+// r at sf_atom_offset(r, j), i.e. the shared-memory image one tcgen05.cp
+// 32x128b.warpx4 moves into four TMEM columns.
 #include "common.cuh"
 
 namespace fp8bs {
 
-constexpr int kMxThreads = (3 + kEpiWarps) * 32;
-constexpr int kSfDepth = 3;   // steps of scale bytes the stager keeps in flight
+constexpr int kMxThreads = (2 + kEpiWarps) * 32;
 
 template <int BN, int STAGES>
 struct MxLayout {
@@ -80,7 +82,7 @@ __global__ void __launch_bounds__(kMxThreads, 1)
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
-            ptx::mbar_init(full_bar(s), 2);      // producer (with tx bytes) + scale stager
+            ptx::mbar_init(full_bar(s), 1);      // producer (with tx bytes)
             ptx::mbar_init(empty_bar(s), 1);     // MMA commit
         }
         ptx::mbar_init(acc_full_bar, 1);
@@ -97,11 +99,6 @@ __global__ void __launch_bounds__(kMxThreads, 1)
     __syncthreads();
     ptx::tc_fence_after();
     const uint32_t tmem_base = *tmem_holder;
-
-    const int my_tiles = static_cast<int>(blockIdx.x) < num_tiles
-                             ? (num_tiles - static_cast<int>(blockIdx.x) + static_cast<int>(gridDim.x) - 1) /
-                                   static_cast<int>(gridDim.x)
-                             : 0;
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
@@ -120,9 +117,16 @@ __global__ void __launch_bounds__(kMxThreads, 1)
                         ok = false;
                         break;
                     }
-                    ptx::mbar_arrive_expect_tx(full_bar(s), L::A_BYTES + L::B_BYTES);
+                    ptx::mbar_arrive_expect_tx(full_bar(s), L::A_BYTES + L::B_BYTES + L::SF_BYTES);
                     ptx::tma_load_2d(sbase + L::OFF_A + s * L::A_BYTES, &tmA, full_bar(s), ks * kBlockK, mb * kBlockM);
                     ptx::tma_load_2d(sbase + L::OFF_B + s * L::B_BYTES, &tmB, full_bar(s), ks * kBlockK, nb * BN);
+                    const uint32_t sf_smem = sbase + L::OFF_SF + s * L::SF_BYTES;
+                    ptx::bulk_load(sf_smem, args.a_sf + (static_cast<size_t>(mb) * KS + ks) * 512, 512, full_bar(s));
+#pragma unroll
+                    for (int h = 0; h < BN / 128; ++h)
+                        ptx::bulk_load(sf_smem + L::SFA_BYTES + 512 * h,
+                                       args.b_sf + (static_cast<size_t>(nb * (BN / 128) + h) * KS + ks) * 512, 512,
+                                       full_bar(s));
                 }
             }
             for (int s = 0; s < STAGES; ++s) {
@@ -173,66 +177,10 @@ __global__ void __launch_bounds__(kMxThreads, 1)
             ptx::tc_commit(mma_done_bar);
             wait_teardown(mma_done_bar, 0, args);
         }
-    } else if (warp == 2) {
-        // -------------------------------------------------- scale stager
-        const int G = args.K / 32;
-        const int total = my_tiles * KS;
-        struct Slot {
-            uint32_t a[4];
-            uint32_t b[4 * (BN / 128)];
-        };
-        auto load = [&](int g, Slot &sl) {
-            if (g >= total) {
-#pragma unroll
-                for (int i = 0; i < 4; ++i) sl.a[i] = 0;
-#pragma unroll
-                for (int i = 0; i < 4 * (BN / 128); ++i) sl.b[i] = 0;
-                return;
-            }
-            const int ti = g / KS;
-            const int ks = g - ti * KS;
-            int mb, nb;
-            args.raster.coords(static_cast<int>(blockIdx.x) + ti * static_cast<int>(gridDim.x), mb, nb);
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const int m = mb * kBlockM + lane + 32 * i;
-                sl.a[i] = m < args.M ? ptx::ldg_nc_u32(args.a_e8m0 + static_cast<size_t>(m) * G + 4 * ks) : 0u;
-            }
-#pragma unroll
-            for (int i = 0; i < 4 * (BN / 128); ++i) {
-                const int n = nb * BN + lane + 32 * i;
-                sl.b[i] = n < args.N ? ptx::ldg_nc_u32(args.b_e8m0 + static_cast<size_t>(n) * G + 4 * ks) : 0u;
-            }
-        };
-        Slot q0, q1, q2;
-        load(0, q0);
-        load(1, q1);
-        load(2, q2);
-        for (int g = 0; g < total; ++g) {
-            const Slot cur = q0;
-            q0 = q1;
-            q1 = q2;
-            load(g + kSfDepth, q2);
-            const int s = g % STAGES;
-            const uint32_t ph = (g / STAGES) & 1;
-            if (!wait_bounded_warp(empty_bar(s), ph ^ 1, abort_flag, args))
-                break;
-            const uint32_t sf_smem = sbase + L::OFF_SF + s * L::SF_BYTES;
-            // lane l writes the 16 bytes of atom row l: rows l, l+32, l+64, l+96.
-            ptx::st_shared_v4(sf_smem + lane * 16, cur.a[0], cur.a[1], cur.a[2], cur.a[3]);
-#pragma unroll
-            for (int h = 0; h < BN / 128; ++h)
-                ptx::st_shared_v4(sf_smem + L::SFA_BYTES + 512 * h + lane * 16, cur.b[4 * h + 0], cur.b[4 * h + 1],
-                                  cur.b[4 * h + 2], cur.b[4 * h + 3]);
-            ptx::fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0)
-                ptx::mbar_arrive(full_bar(s));
-        }
     } else {
         // ------------------------------------------------------ epilogue
         constexpr int HALF = BN / 2;
-        const int ew = warp - 3;                // 0..7
+        const int ew = warp - 2;                // 0..7
         const int wg = ew >> 2;
         const int q = warp & 3;
         const uint32_t cstage = sbase + L::OFF_C + ew * kCStageBytes;
@@ -262,8 +210,8 @@ __global__ void __launch_bounds__(kMxThreads, 1)
             const int x0 = nb * BN + wg * HALF;
             const int y0 = mb * kBlockM + q * 32;
 #pragma unroll
-            for (int c = 0; c < HALF / 32; ++c)
-                store_c_chunk(&tmC, cstage, lane, v + c * 32, x0 + c * 32, y0, args.M, args.N);
+            for (int c = 0; c < HALF / kCChunkCols; ++c)
+                store_c_chunk(&tmC, cstage, lane, c, v + c * kCChunkCols, x0 + c * kCChunkCols, y0, args.M, args.N);
         }
         if (lane == 0)
             ptx::bulk_wait_all();

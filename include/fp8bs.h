@@ -5,7 +5,8 @@
  * CUDA device addresses owned by the caller; `stream` is a cudaStream_t passed
  * as void* (NULL = the legacy default stream). Every GEMM call is asynchronous
  * on `stream`, performs no host synchronisation and no allocation after the
- * first call on a device, and can be captured in a CUDA graph.
+ * first call on a device (except fp8mx_gemm's pooled workspace, see there),
+ * and can be captured in a CUDA graph.
  *
  * Error behaviour: functions return FP8BS_OK (0) or a negative fp8bs_status.
  * Argument errors are detected on the host before anything is launched.
@@ -52,7 +53,7 @@ typedef enum {
  *   C        bf16 [M][N] row-major, written (never read), 16-byte aligned.
  *
  * Shape rules: M >= 1; N >= 8 and N % 8 == 0; K >= 128, K % 128 == 0 and
- * K <= 65536. Otherwise FP8BS_ERR_SHAPE. M = 0 is a no-op returning FP8BS_OK.
+ * K <= 1048576. Otherwise FP8BS_ERR_SHAPE. M = 0 is a no-op returning FP8BS_OK.
  * A partial last N block of 128 rows uses its own b_scale row.
  */
 int fp8bs_gemm(const void *A, const float *a_scale, const void *B, const float *b_scale, void *C,
@@ -74,9 +75,39 @@ int fp8bs_gemm(const void *A, const float *a_scale, const void *B, const float *
  * Shape rules as fp8bs_gemm. The scale bytes 0xFF (NaN) are outside the
  * contract. This entry point and fp8bs_gemm are deliberately separate: the
  * two scale formats cannot be told apart by shape or dtype.
+ *
+ * Launches two kernels on `stream`: fp8mx_pack_scales for both scale tensors
+ * (into a workspace taken from a library-owned stream-ordered memory pool and
+ * returned to it on the same stream; the pool keeps the memory between calls),
+ * then the GEMM of fp8mx_gemm_packed.
  */
 int fp8mx_gemm(const void *A, const uint8_t *a_e8m0, const void *B, const uint8_t *b_e8m0, void *C,
                int M, int N, int K, void *stream);
+
+/*
+ * MXFP8 GEMM on scale factors already in the packed layout (no allocation,
+ * one kernel). The PR above keeps its scale shuffles as separate weight-prep
+ * helpers for the same reason: the kernel wants a layout the quantiser does
+ * not produce.
+ *   a_sf  fp8mx_packed_scale_bytes(M, K) bytes, 16-byte aligned, from fp8mx_pack_scales.
+ *   b_sf  fp8mx_packed_scale_bytes(N, K) bytes, 16-byte aligned.
+ * Other arguments as fp8mx_gemm.
+ */
+int fp8mx_gemm_packed(const void *A, const uint8_t *a_sf, const void *B, const uint8_t *b_sf, void *C,
+                      int M, int N, int K, void *stream);
+
+/* Size in bytes of the packed scale layout of a [rows][K/32] ue8m0 tensor:
+ * ceil(rows/128) * (K/128) * 512. Negative (FP8BS_ERR_SHAPE) for bad shapes. */
+int64_t fp8mx_packed_scale_bytes(int rows, int K);
+
+/*
+ * Repack ue8m0 bytes [rows][K/32] (row-major, 4-byte aligned, device) into the
+ * packed layout (device, 16-byte aligned): for 128-row block rb and 128-wide K
+ * step ks a 512-byte atom at byte ((rb * (K/128)) + ks) * 512, in which byte j
+ * (K group 4*ks + j) of row rb*128 + r sits at fp8mx_sf_atom_offset(r, j);
+ * rows past `rows` are zero. Asynchronous on `stream`, one kernel.
+ */
+int fp8mx_pack_scales(const uint8_t *e8m0, uint8_t *packed, int rows, int K, void *stream);
 
 /* ---- layout helpers (bit-exact; host functions, no CUDA calls) ---------- */
 
@@ -115,8 +146,10 @@ int fp8bs_last_config_id(void);
  * device with `num_sms` SMs (host-only, no CUDA calls). */
 int fp8bs_select_config(int M, int N, int K, int num_sms);
 int fp8mx_select_config(int M, int N, int K, int num_sms);
-/* Number of kernels one fp8bs_gemm / fp8mx_gemm call launches (1). */
+/* Number of kernels one fp8bs_gemm call launches (1). */
 int fp8bs_launches_per_call(void);
+/* Number of kernels one fp8mx_gemm call launches (2: scale pack + GEMM). */
+int fp8mx_launches_per_call(void);
 /* Set the per-wait device time limit in nanoseconds (default 2e9) used by
  * subsequent launches from this process; 0 restores the default. */
 void fp8bs_set_wait_limit_ns(uint64_t ns);

@@ -177,6 +177,45 @@ def test_pack_a_scale_bit_exact():
         assert np.array_equal(out.cpu().numpy(), workloads.a_scale_to_kmajor(sa))
 
 
+def _packed_reference(e8m0, K):
+    """The packed scale layout written out from its definition in include/fp8bs.h."""
+    rows = e8m0.shape[0]
+    RB, KS = (rows + 127) // 128, K // 128
+    out = np.zeros(RB * KS * 512, np.uint8)
+    for rb in range(RB):
+        for ks in range(KS):
+            base = (rb * KS + ks) * 512
+            for r in range(128):
+                if rb * 128 + r < rows:
+                    for j in range(4):
+                        out[base + (r % 32) * 16 + (r // 32) * 4 + j] = e8m0[rb * 128 + r, 4 * ks + j]
+    return out
+
+
+@pytest.mark.parametrize("rows,K", [(1, 128), (130, 256), (257, 1280)])
+def test_pack_mx_scales_bit_exact(rows, K):
+    import torch
+    import fp8_block_scaled_e4m3_gb300 as f
+    rng = np.random.Generator(np.random.PCG64(rows))
+    e = rng.integers(0, 255, size=(rows, K // 32), dtype=np.uint8)
+    out = torch.full((f.packed_scale_bytes(rows, K),), 0xAB, dtype=torch.uint8, device="cuda")
+    f.pack_mx_scales(to_dev(e), K, out=out)
+    assert np.array_equal(out.cpu().numpy(), _packed_reference(e, K))
+
+
+@pytest.mark.parametrize("M,N,K", [(200, 136, 384), (1024, 640, 1280)])
+def test_mxfp8_packed_entry_matches_oracle(M, N, K):
+    import torch
+    import fp8_block_scaled_e4m3_gb300 as f
+    x = workloads.make_mxfp8_inputs(M, N, K, seed=M + 1)
+    a_sf = f.pack_mx_scales(to_dev(x.a_e8m0), K)
+    b_sf = f.pack_mx_scales(to_dev(x.b_e8m0), K)
+    C = f.gemm_mxfp8_packed(to_dev(x.A), a_sf, to_dev(x.B), b_sf)
+    assert f.get_status() == 0
+    got = C.view(torch.int16).cpu().numpy().view(np.uint16)
+    compare(got, oracle.mxfp8(x.A, x.a_e8m0, x.B, x.b_e8m0), f"mx packed {M}x{N}x{K}")
+
+
 def test_m_zero_is_noop():
     import torch
     import fp8_block_scaled_e4m3_gb300 as f
