@@ -46,6 +46,7 @@ _SIGS = {
     "fp8mx_select_config": (_i, [_i, _i, _i, _i]),
     "fp8bs_launches_per_call": (_i, []),
     "fp8bs_set_wait_limit_ns": (None, [ctypes.c_uint64]),
+    "fp8bs_set_config_override": (_i, [_i]),
     "fp8bs_version": (ctypes.c_char_p, []),
 }
 for _name, (_res, _args) in _SIGS.items():
@@ -207,8 +208,14 @@ def select_config(kind: str, M: int, N: int, K: int, num_sms: int) -> int:
 
 
 def decode_config(cid: int) -> dict:
-    return {"kind": {1: "blockscale", 2: "mxfp8"}.get(cid // 1000000, "?"), "block_n": (cid // 1000) % 1000,
+    return {"kind": {1: "blockscale", 2: "mxfp8", 3: "blockscale_pair"}.get(cid // 1000000, "?"),
+            "block_n": (cid // 1000) % 1000,
             "stages": (cid // 100) % 10, "raster": (cid // 10) % 10, "group": cid % 10}
+
+
+def set_config_override(config_id: int) -> None:
+    """Force a kernel configuration (0 = choose by shape); see include/fp8bs.h."""
+    _check(_lib.fp8bs_set_config_override(int(config_id)), "fp8bs_set_config_override")
 
 
 def set_wait_limit_ns(ns: int) -> None:

@@ -11,7 +11,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libfp8bs.so")
-SOURCES = ["api.cu", "bs_kernel.cu", "mx_kernel.cu"]
+SOURCES = ["api.cu", "bs_kernel.cu", "bs2_kernel.cu", "mx_kernel.cu"]
 HEADERS = ["ptx.cuh", "common.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
@@ -60,7 +60,7 @@ def check_resources(log_path: str) -> None:
     valid when the kernel is compiled to exactly 168 registers. No kernel may spill."""
     info = parse_ptxas(log_path)
     for sym, r in info.items():
-        if "fp8bs_blockscale_kernel" in sym and r.get("registers") != 168:
+        if "fp8bs_blockscale_" in sym and r.get("registers") != 168:
             raise RuntimeError(f"{sym}: {r.get('registers')} registers, the setmaxnreg split needs 168")
         if r.get("spill_stores", 0) or r.get("spill_loads", 0):
             raise RuntimeError(f"{sym}: register spills {r}")

@@ -1,6 +1,6 @@
 // Host side of libfp8bs: argument checks, shape-class -> kernel configuration,
-// tensor-map encoding, launches, the per-device status word and the layout
-// helpers declared in include/fp8bs.h.
+// tensor-map encoding, launches, the per-device status word, the scale repack
+// kernels and the layout helpers declared in include/fp8bs.h.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -17,6 +17,11 @@ namespace fp8bs {
 template <int BN, int STAGES>
 cudaError_t launch_blockscale(const CUtensorMap &, const CUtensorMap &, const CUtensorMap &, const CUtensorMap &,
                               const GemmArgs &, int, cudaStream_t);
+template <int STAGES>
+cudaError_t launch_blockscale_pair(const CUtensorMap &, const CUtensorMap &, const CUtensorMap &, const CUtensorMap &,
+                                   const GemmArgs &, int, cudaStream_t);
+template <int STAGES>
+cudaError_t max_pair_clusters(int *);
 template <int BN, int STAGES>
 cudaError_t launch_mxfp8(const CUtensorMap &, const CUtensorMap &, const CUtensorMap &, const GemmArgs &, int,
                          cudaStream_t);
@@ -27,18 +32,21 @@ __device__ int g_status_word;   // per-device status written by the kernels
 
 constexpr int kMaxDevices = 64;
 constexpr unsigned long long kDefaultWaitLimitNs = 2000000000ull;
+constexpr int kPairStages = 8;
 
 struct DeviceState {
     bool ready = false;
-    int status = FP8BS_OK;       // result of the set-up
+    int status = FP8BS_OK;          // result of the set-up
     int num_sms = 0;
-    int *status_ptr = nullptr;   // device address of g_status_word
-    cudaMemPool_t pool = nullptr; // stream-ordered pool for fp8mx_gemm's packed scales
+    int *status_ptr = nullptr;      // device address of g_status_word
+    cudaMemPool_t pool = nullptr;   // stream-ordered pool for fp8mx_gemm's packed scales
+    int pair_clusters = 0;          // co-resident CTA pairs of the pair kernel
 };
 
 std::mutex g_mutex;
 DeviceState g_dev[kMaxDevices];
 std::atomic<unsigned long long> g_wait_limit_ns{kDefaultWaitLimitNs};
+std::atomic<int> g_config_override{0};
 thread_local int t_last_config = 0;
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
@@ -46,6 +54,9 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t
                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 EncodeTiledFn g_encode = nullptr;
 
+// One-time set-up per device, with that device current: capability check, SM
+// count, the device address of the status word, the workspace pool, and the
+// number of co-resident CTA pairs.
 int ensure_device(int &dev, DeviceState *&st)
 {
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
@@ -73,6 +84,8 @@ int ensure_device(int &dev, DeviceState *&st)
     uint64_t keep = UINT64_MAX;   // keep freed workspace in the pool between calls
     if (cudaMemPoolSetAttribute(st->pool, cudaMemPoolAttrReleaseThreshold, &keep) != cudaSuccess)
         return st->status = FP8BS_ERR_CUDA;
+    if (max_pair_clusters<kPairStages>(&st->pair_clusters) != cudaSuccess || st->pair_clusters < 1)
+        return st->status = FP8BS_ERR_CUDA;
     if (!g_encode) {
         cudaDriverEntryPointQueryResult q;
         void *fn = nullptr;
@@ -85,15 +98,14 @@ int ensure_device(int &dev, DeviceState *&st)
     return st->status = FP8BS_OK;
 }
 
-// 2-D row-major tensor [rows][cols] of `esize`-byte elements, box [box_rows][box_cols].
-bool encode_2d(CUtensorMap *tm, CUtensorMapDataType dt, int esize, const void *base, uint64_t cols, uint64_t rows,
+// 2-D row-major tensor [rows][cols], box [box_rows][box_cols].
+bool encode_2d(CUtensorMap *tm, CUtensorMapDataType dt, const void *base, uint64_t cols, uint64_t rows,
                uint64_t row_stride_bytes, uint32_t box_cols, uint32_t box_rows, CUtensorMapSwizzle swz)
 {
     cuuint64_t dims[2] = {cols, rows};
     cuuint64_t strides[1] = {row_stride_bytes};
     cuuint32_t box[2] = {box_cols, box_rows};
     cuuint32_t estr[2] = {1, 1};
-    (void)esize;
     return g_encode(tm, dt, 2, const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -107,23 +119,54 @@ int check_shape(int M, int N, int K)
     return FP8BS_OK;
 }
 
-// Shape class -> configuration. Returns the config id (see fp8bs.h) and fills
-// tile width, stages and raster.
+// Kernel configuration. kind 1: one-CTA blockscale kernel, 2: MXFP8 kernel,
+// 3: CTA-pair blockscale kernel (256 x 128 tiles over two SMs).
 struct Config {
-    int block_n, stages, raster, group;
+    int kind, block_n, stages, raster, group;
 };
 
-int config_id(int kind, const Config &c)
+int config_id(const Config &c)
 {
     const int gcode = c.group >= 9 ? 9 : c.group;
-    return kind * 1000000 + c.block_n * 1000 + c.stages * 100 + c.raster * 10 + gcode;
+    return c.kind * 1000000 + c.block_n * 1000 + c.stages * 100 + c.raster * 10 + gcode;
 }
 
+// Only the instantiated kernels are valid configurations.
+bool decode_config_id(int id, Config &c)
+{
+    c.kind = id / 1000000;
+    c.block_n = (id / 1000) % 1000;
+    c.stages = (id / 100) % 10;
+    c.raster = (id / 10) % 10;
+    c.group = id % 10;
+    if (c.group < 1 || c.raster > 1)
+        return false;
+    if (c.kind == 1 || c.kind == 2)
+        return (c.block_n == 256 && c.stages == 4) || (c.block_n == 128 && c.stages == 6);
+    if (c.kind == 3)
+        return c.block_n == 128 && c.stages == kPairStages;
+    return false;
+}
+
+// Shape class -> configuration, from (M, N, K) only.
 Config choose_config(int kind, int M, int N, int K, int num_sms)
 {
-    (void)kind;
     (void)K;
     Config c;
+    // Stream the larger operand once past a resident set of panels of the smaller one.
+    c.raster = ((long)M >= (long)N) ? 1 : 0;
+    c.group = 1;
+    if (kind == 1) {
+        // Blockscale: the CTA-pair kernel. Its four TMEM partial buffers per CTA
+        // let the MMA run ahead of the fp32 promote, which the two buffers of a
+        // one-CTA 128 x 256 tile cannot (the promote's FMAs cost about half the
+        // MMA time per SM).
+        c.kind = 3;
+        c.block_n = 128;
+        c.stages = kPairStages;
+        return c;
+    }
+    c.kind = 2;
     // Wide tiles (128 x 256) keep shared-memory operand traffic at 96 B/clk per
     // SM; the narrow tile only when the wide one leaves most SMs idle.
     const long tiles256 = (long)((M + 127) / 128) * ((N + 255) / 256);
@@ -134,10 +177,19 @@ Config choose_config(int kind, int M, int N, int K, int num_sms)
         c.block_n = 256;
         c.stages = 4;
     }
-    // Stream the larger operand once past a resident set of panels of the smaller one.
-    c.raster = ((long)M >= (long)N) ? 1 : 0;
-    c.group = 1;
     return c;
+}
+
+bool override_config(int kind_a, int kind_b, Config &cfg)
+{
+    const int ovr = g_config_override.load();
+    if (!ovr)
+        return true;
+    Config o;
+    if (!decode_config_id(ovr, o) || (o.kind != kind_a && o.kind != kind_b))
+        return false;
+    cfg = o;
+    return true;
 }
 
 // Repack ue8m0 bytes [rows][K/32] into 512-byte scale-factor atoms (see
@@ -180,6 +232,18 @@ int launch_pack_scales(const uint8_t *e0, uint8_t *p0, int rows0, const uint8_t 
     return cudaGetLastError() == cudaSuccess ? FP8BS_OK : FP8BS_ERR_LAUNCH;
 }
 
+__global__ void pack_a_scale_kernel(const float *__restrict__ src, float *__restrict__ dst, int M, int KB,
+                                    int64_t ld)
+{
+    const int64_t total = ld * KB;
+    for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int kb = static_cast<int>(i / ld);
+        const int m = static_cast<int>(i - static_cast<int64_t>(kb) * ld);
+        dst[i] = m < M ? src[static_cast<int64_t>(m) * KB + kb] : 0.f;
+    }
+}
+
 } // namespace host
 } // namespace fp8bs
 
@@ -204,23 +268,27 @@ int fp8bs_gemm(const void *A, const float *a_scale, const void *B, const float *
     DeviceState *st;
     if ((rc = ensure_device(dev, st)))
         return rc;
-    const Config cfg = choose_config(1, M, N, K, st->num_sms);
+    Config cfg = choose_config(1, M, N, K, st->num_sms);
+    if (!override_config(1, 3, cfg))
+        return FP8BS_ERR_SHAPE;
+    const bool pair = cfg.kind == 3;
     const int KB = K / 128;
     const uint64_t ld_sa = static_cast<uint64_t>(fp8bs_a_scale_ld(M));
+    const uint32_t b_box_rows = pair ? cfg.block_n / 2 : cfg.block_n;   // a pair CTA holds half of B
     CUtensorMap tmA, tmB, tmSA, tmC;
-    if (!encode_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, A, K, M, K, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !encode_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, B, K, N, K, 128, cfg.block_n,
-                   CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !encode_2d(&tmSA, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, a_scale, ld_sa, KB, ld_sa * 4, 128, 1,
+    if (!encode_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, A, K, M, K, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, B, K, N, K, 128, b_box_rows, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_2d(&tmSA, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, a_scale, ld_sa, KB, ld_sa * 4, 128, 1,
                    CU_TENSOR_MAP_SWIZZLE_NONE) ||
-        !encode_2d(&tmC, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, C, N, M, static_cast<uint64_t>(N) * 2, kCChunkCols, 32,
+        !encode_2d(&tmC, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, C, N, M, static_cast<uint64_t>(N) * 2, kCChunkCols, 32,
                    CU_TENSOR_MAP_SWIZZLE_32B))
         return FP8BS_ERR_LAUNCH;
     GemmArgs args = {};
     args.M = M;
     args.N = N;
     args.K = K;
-    args.raster.m_tiles = (M + kBlockM - 1) / kBlockM;
+    const int tile_m = pair ? 2 * kBlockM : kBlockM;
+    args.raster.m_tiles = (M + tile_m - 1) / tile_m;
     args.raster.n_tiles = (N + cfg.block_n - 1) / cfg.block_n;
     args.raster.raster = cfg.raster;
     args.raster.group = cfg.group;
@@ -230,11 +298,16 @@ int fp8bs_gemm(const void *A, const float *a_scale, const void *B, const float *
     const int tiles = args.raster.num_tiles();
     const int grid = tiles < st->num_sms ? tiles : st->num_sms;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    cudaError_t e = cfg.block_n == 256 ? launch_blockscale<256, 4>(tmA, tmB, tmSA, tmC, args, grid, s)
-                                       : launch_blockscale<128, 6>(tmA, tmB, tmSA, tmC, args, grid, s);
+    cudaError_t e;
+    if (pair)
+        e = launch_blockscale_pair<kPairStages>(tmA, tmB, tmSA, tmC, args, st->pair_clusters, s);
+    else if (cfg.block_n == 256)
+        e = launch_blockscale<256, 4>(tmA, tmB, tmSA, tmC, args, grid, s);
+    else
+        e = launch_blockscale<128, 6>(tmA, tmB, tmSA, tmC, args, grid, s);
     if (e != cudaSuccess)
         return FP8BS_ERR_LAUNCH;
-    t_last_config = config_id(1, cfg);
+    t_last_config = config_id(cfg);
     return FP8BS_OK;
 }
 
@@ -254,12 +327,13 @@ int fp8mx_gemm_packed(const void *A, const uint8_t *a_sf, const void *B, const u
     DeviceState *st;
     if ((rc = ensure_device(dev, st)))
         return rc;
-    const Config cfg = choose_config(2, M, N, K, st->num_sms);
+    Config cfg = choose_config(2, M, N, K, st->num_sms);
+    if (!override_config(2, 2, cfg))
+        return FP8BS_ERR_SHAPE;
     CUtensorMap tmA, tmB, tmC;
-    if (!encode_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, A, K, M, K, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !encode_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, B, K, N, K, 128, cfg.block_n,
-                   CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !encode_2d(&tmC, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, C, N, M, static_cast<uint64_t>(N) * 2, kCChunkCols, 32,
+    if (!encode_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, A, K, M, K, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, B, K, N, K, 128, cfg.block_n, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_2d(&tmC, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, C, N, M, static_cast<uint64_t>(N) * 2, kCChunkCols, 32,
                    CU_TENSOR_MAP_SWIZZLE_32B))
         return FP8BS_ERR_LAUNCH;
     GemmArgs args = {};
@@ -281,7 +355,7 @@ int fp8mx_gemm_packed(const void *A, const uint8_t *a_sf, const void *B, const u
                                        : launch_mxfp8<128, 6>(tmA, tmB, tmC, args, grid, s);
     if (e != cudaSuccess)
         return FP8BS_ERR_LAUNCH;
-    t_last_config = config_id(2, cfg);
+    t_last_config = config_id(cfg);
     return FP8BS_OK;
 }
 
@@ -352,26 +426,6 @@ int64_t fp8mx_scale_index(int r, int g, int K) { return static_cast<int64_t>(r) 
 
 int fp8mx_sf_atom_offset(int r, int j) { return sf_atom_offset(r, j); }
 
-} // extern "C"
-
-namespace fp8bs {
-namespace host {
-__global__ void pack_a_scale_kernel(const float *__restrict__ src, float *__restrict__ dst, int M, int KB,
-                                    int64_t ld)
-{
-    const int64_t total = ld * KB;
-    for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
-         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-        const int kb = static_cast<int>(i / ld);
-        const int m = static_cast<int>(i - static_cast<int64_t>(kb) * ld);
-        dst[i] = m < M ? src[static_cast<int64_t>(m) * KB + kb] : 0.f;
-    }
-}
-} // namespace host
-} // namespace fp8bs
-
-extern "C" {
-
 int fp8bs_pack_a_scale(const float *a_scale_rowmajor, float *a_scale_kmajor, int M, int K, void *stream)
 {
     if (M < 0 || K < 128 || (K % 128) != 0 || K > (1 << 20))
@@ -424,7 +478,7 @@ const char *fp8bs_status_string(int status)
     case FP8BS_OK: return "ok";
     case FP8BS_ERR_NULL: return "null pointer argument";
     case FP8BS_ERR_ALIGN: return "pointer not aligned as required";
-    case FP8BS_ERR_SHAPE: return "shape outside the supported rules";
+    case FP8BS_ERR_SHAPE: return "shape (or configuration id) outside the supported rules";
     case FP8BS_ERR_UNSUPPORTED_DEVICE: return "device is not compute capability 10.3 (sm_103a)";
     case FP8BS_ERR_LAUNCH: return "tensor-map encoding or kernel launch failed";
     case FP8BS_ERR_DEVICE_TIMEOUT: return "a device-side wait exceeded its time limit";
@@ -439,25 +493,33 @@ int fp8bs_select_config(int M, int N, int K, int num_sms)
 {
     if (check_shape(M, N, K) || num_sms <= 0)
         return FP8BS_ERR_SHAPE;
-    return config_id(1, choose_config(1, M, N, K, num_sms));
+    return config_id(choose_config(1, M, N, K, num_sms));
 }
 
 int fp8mx_select_config(int M, int N, int K, int num_sms)
 {
     if (check_shape(M, N, K) || num_sms <= 0)
         return FP8BS_ERR_SHAPE;
-    return config_id(2, choose_config(2, M, N, K, num_sms));
+    return config_id(choose_config(2, M, N, K, num_sms));
+}
+
+int fp8bs_set_config_override(int config_id)
+{
+    if (config_id != 0) {
+        Config c;
+        if (!decode_config_id(config_id, c))
+            return FP8BS_ERR_SHAPE;
+    }
+    g_config_override.store(config_id);
+    return FP8BS_OK;
 }
 
 int fp8bs_launches_per_call(void) { return 1; }
 
 int fp8mx_launches_per_call(void) { return 2; }
 
-void fp8bs_set_wait_limit_ns(uint64_t ns)
-{
-    g_wait_limit_ns.store(ns ? ns : kDefaultWaitLimitNs);
-}
+void fp8bs_set_wait_limit_ns(uint64_t ns) { g_wait_limit_ns.store(ns ? ns : kDefaultWaitLimitNs); }
 
-const char *fp8bs_version(void) { return "fp8bs 0.1.0 (sm_103a)"; }
+const char *fp8bs_version(void) { return "fp8bs 0.2.0 (sm_103a)"; }
 
 } // extern "C"

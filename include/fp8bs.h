@@ -140,12 +140,19 @@ int fp8bs_get_status(void *stream);
 const char *fp8bs_status_string(int status);
 /* Identifier of the kernel configuration the last successful GEMM call on this
  * host thread launched (0 if none): kind*1000000 + block_n*1000 + stages*100 +
- * raster*10 + group_code, kind 1 = blockscale, 2 = mxfp8. */
+ * raster*10 + group_code; kind 1 = one-CTA blockscale kernel (128 x block_n
+ * tiles), 2 = mxfp8 kernel, 3 = CTA-pair blockscale kernel (256 x block_n tiles
+ * over two SMs). */
 int fp8bs_last_config_id(void);
 /* Configuration id fp8bs_gemm / fp8mx_gemm would choose for a shape on a
  * device with `num_sms` SMs (host-only, no CUDA calls). */
 int fp8bs_select_config(int M, int N, int K, int num_sms);
 int fp8mx_select_config(int M, int N, int K, int num_sms);
+/* Force the configuration of subsequent GEMM calls in this process (a valid
+ * configuration id of the matching kind; 0 restores the shape-based choice).
+ * Returns FP8BS_ERR_SHAPE for an id that names no built kernel. For tests and
+ * measurements of each kernel variant. */
+int fp8bs_set_config_override(int config_id);
 /* Number of kernels one fp8bs_gemm call launches (1). */
 int fp8bs_launches_per_call(void);
 /* Number of kernels one fp8mx_gemm call launches (2: scale pack + GEMM). */

@@ -177,6 +177,58 @@ def test_pack_a_scale_bit_exact():
         assert np.array_equal(out.cpu().numpy(), workloads.a_scale_to_kmajor(sa))
 
 
+# every built kernel configuration, forced through the override
+BS_CONFIGS = [1256411, 1128611, 3128811]      # one-CTA 128x256, one-CTA 128x128, CTA-pair 256x128
+MX_CONFIGS = [2256411, 2128611]
+
+
+@pytest.fixture
+def override():
+    import fp8_block_scaled_e4m3_gb300 as f
+    yield f.set_config_override
+    f.set_config_override(0)
+
+
+@pytest.mark.parametrize("cfg", BS_CONFIGS)
+@pytest.mark.parametrize("M,N,K", [(128, 256, 256), (300, 520, 1280), (513, 1032, 384), (1, 8, 128)])
+def test_blockscale_every_config(override, cfg, M, N, K):
+    import fp8_block_scaled_e4m3_gb300 as f
+    raster = 1 if M >= N else 0
+    override(cfg - (cfg // 10 % 10) * 10 + raster * 10)
+    x = workloads.make_blockscale_inputs(M, N, K, seed=cfg % 97 + M)
+    got = run_blockscale(x.A, x.a_scale, x.B, x.b_scale)
+    assert f.last_config_id() == cfg - (cfg // 10 % 10) * 10 + raster * 10
+    compare(got, oracle.blockscale(x.A, x.a_scale, x.B, x.b_scale), f"bs cfg {cfg} {M}x{N}x{K}")
+
+
+@pytest.mark.parametrize("cfg", BS_CONFIGS)
+def test_blockscale_every_config_integer_exact(override, cfg):
+    override(cfg)
+    rng = np.random.Generator(np.random.PCG64(5))
+    M, N, K = 384, 640, 512
+    A = _int_codes(rng.integers(-2, 3, size=(M, K)))
+    B = _int_codes(rng.integers(-2, 3, size=(N, K)))
+    sa = np.ldexp(np.float32(1), rng.integers(-3, 4, size=(M, K // 128))).astype(np.float32)
+    sb = np.ldexp(np.float32(1), rng.integers(-3, 4, size=((N + 127) // 128, K // 128))).astype(np.float32)
+    assert np.array_equal(run_blockscale(A, sa, B, sb), oracle.blockscale(A, sa, B, sb))
+
+
+@pytest.mark.parametrize("cfg", MX_CONFIGS)
+@pytest.mark.parametrize("M,N,K", [(300, 520, 1280), (129, 136, 256)])
+def test_mxfp8_every_config(override, cfg, M, N, K):
+    override(cfg)
+    x = workloads.make_mxfp8_inputs(M, N, K, seed=cfg % 89 + M)
+    compare(run_mxfp8(x.A, x.a_e8m0, x.B, x.b_e8m0), oracle.mxfp8(x.A, x.a_e8m0, x.B, x.b_e8m0),
+            f"mx cfg {cfg} {M}x{N}x{K}")
+
+
+def test_config_override_rejects_unbuilt_ids():
+    import fp8_block_scaled_e4m3_gb300 as f
+    with pytest.raises(f.Fp8bsError):
+        f.set_config_override(1999911)
+    f.set_config_override(0)
+
+
 def _packed_reference(e8m0, K):
     """The packed scale layout written out from its definition in include/fp8bs.h."""
     rows = e8m0.shape[0]
