@@ -47,6 +47,7 @@ _SIGS = {
     "fp8bs_launches_per_call": (_i, []),
     "fp8bs_set_wait_limit_ns": (None, [ctypes.c_uint64]),
     "fp8bs_set_config_override": (_i, [_i]),
+    "fp8bs_device_info": (_i, [_p, _p]),
     "fp8bs_version": (ctypes.c_char_p, []),
 }
 for _name, (_res, _args) in _SIGS.items():
@@ -211,6 +212,13 @@ def decode_config(cid: int) -> dict:
     return {"kind": {1: "blockscale", 2: "mxfp8", 3: "blockscale_pair"}.get(cid // 1000000, "?"),
             "block_n": (cid // 1000) % 1000,
             "stages": (cid // 100) % 10, "raster": (cid // 10) % 10, "group": cid % 10}
+
+
+def device_info() -> dict:
+    """SM count and resident CTA pairs of the current device (as the library sees them)."""
+    a, b = ctypes.c_int(0), ctypes.c_int(0)
+    _check(_lib.fp8bs_device_info(ctypes.byref(a), ctypes.byref(b)), "fp8bs_device_info")
+    return {"num_sms": a.value, "pair_clusters": b.value}
 
 
 def set_config_override(config_id: int) -> None:

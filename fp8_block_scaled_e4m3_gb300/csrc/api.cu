@@ -156,17 +156,12 @@ Config choose_config(int kind, int M, int N, int K, int num_sms)
     // Stream the larger operand once past a resident set of panels of the smaller one.
     c.raster = ((long)M >= (long)N) ? 1 : 0;
     c.group = 1;
-    if (kind == 1) {
-        // Blockscale: the CTA-pair kernel. Its four TMEM partial buffers per CTA
-        // let the MMA run ahead of the fp32 promote, which the two buffers of a
-        // one-CTA 128 x 256 tile cannot (the promote's FMAs cost about half the
-        // MMA time per SM).
-        c.kind = 3;
-        c.block_n = 128;
-        c.stages = kPairStages;
-        return c;
-    }
-    c.kind = 2;
+    // Blockscale and MXFP8 alike: wide one-CTA tiles (128 x 256), which keep
+    // shared-memory operand traffic at 96 B/clk per SM and give each tcgen05.mma
+    // 128 clocks of work (narrower MMAs are issue-bound). The narrow tile only
+    // when the wide one leaves most SMs idle. The CTA-pair blockscale kernel
+    // (kind 3) measured slower on every shape and is selectable by override.
+    c.kind = kind;
     // Wide tiles (128 x 256) keep shared-memory operand traffic at 96 B/clk per
     // SM; the narrow tile only when the wide one leaves most SMs idle.
     const long tiles256 = (long)((M + 127) / 128) * ((N + 255) / 256);
@@ -511,6 +506,20 @@ int fp8bs_set_config_override(int config_id)
             return FP8BS_ERR_SHAPE;
     }
     g_config_override.store(config_id);
+    return FP8BS_OK;
+}
+
+int fp8bs_device_info(int *num_sms, int *pair_clusters)
+{
+    int dev;
+    DeviceState *st;
+    int rc = ensure_device(dev, st);
+    if (rc)
+        return rc;
+    if (num_sms)
+        *num_sms = st->num_sms;
+    if (pair_clusters)
+        *pair_clusters = st->pair_clusters;
     return FP8BS_OK;
 }
 

@@ -15,15 +15,18 @@
 //
 // Per CTA, 12 warps (3 warpgroups):
 //   warp 0      TMA producer: own A rows and own B half of a K block into stage
-//               s; the bytes are counted on the even CTA's full[s] barrier; the
-//               a_scale slice [128] goes to a local ring.
+//               s. Both CTAs' bytes complete on the even CTA's full[s] barrier,
+//               which the even CTA's producer alone arms with the pair's total
+//               (the odd CTA's copies may land first: the barrier cannot complete
+//               before that arrive). The a_scale slice [128] goes to a local ring.
 //   warp 1      TMEM allocation for the pair (both CTAs) and, in the even CTA
 //               only, the single-thread MMA issuer; tcgen05.commit multicasts the
 //               stage release and "partial ready" to both CTAs.
 //   warps 2,3   idle (complete warpgroup 0, which gives its registers away).
 //   warps 4..11 promote + epilogue for this CTA's 128 rows: thread = one row,
 //               64 columns; releases a partial buffer on the even CTA's
-//               tempty barrier (16 arrivals: 8 warps from each CTA).
+//               tempty barrier (16 arrivals: 8 warps from each CTA; the odd
+//               CTA's are relaxed remote arrives, see mbar_arrive_cluster_relaxed).
 #include "common.cuh"
 
 namespace fp8bs {
@@ -91,7 +94,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
-            ptx::mbar_init(full_bar(s), 2);                 // both producers' expect_tx (even CTA's copy is used)
+            ptx::mbar_init(full_bar(s), 1);                 // even CTA's producer (expect_tx of both CTAs' bytes)
             ptx::mbar_init(empty_bar(s), 1);                // multicast MMA commit
         }
         for (int b = 0; b < kPairNBuf; ++b) {
@@ -140,7 +143,8 @@ __global__ void __launch_bounds__(kPairThreads, 1)
                         break;
                     }
                     const uint32_t leader_full = ptx::mapa_shared(full_bar(s), 0);
-                    ptx::mbar_arrive_expect_tx_cluster(leader_full, L::A_BYTES + L::B_BYTES);
+                    if (rank == 0)
+                        ptx::mbar_arrive_expect_tx(full_bar(s), 2 * (L::A_BYTES + L::B_BYTES));
                     ptx::tma_load_2d_pair(sbase + L::OFF_A + s * L::A_BYTES, &tmA, leader_full, kb * kBlockK, row0);
                     ptx::tma_load_2d_pair(sbase + L::OFF_B + s * L::B_BYTES, &tmB, leader_full, kb * kBlockK, brow0);
                     ptx::mbar_arrive_expect_tx(sa_full_bar(a), L::SA_BYTES);
@@ -264,7 +268,10 @@ __global__ void __launch_bounds__(kPairThreads, 1)
                 ptx::tc_fence_before();
                 __syncwarp();
                 if (lane == 0) {
-                    ptx::mbar_arrive_cluster(ptx::mapa_shared(tempty_bar(buf), 0));
+                    if (rank == 0)
+                        ptx::mbar_arrive(tempty_bar(buf));
+                    else
+                        ptx::mbar_arrive_cluster_relaxed(ptx::mapa_shared(tempty_bar(buf), 0));
                     ptx::mbar_arrive(sa_empty_bar(a));
                 }
 #pragma unroll

@@ -153,6 +153,9 @@ int fp8mx_select_config(int M, int N, int K, int num_sms);
  * Returns FP8BS_ERR_SHAPE for an id that names no built kernel. For tests and
  * measurements of each kernel variant. */
 int fp8bs_set_config_override(int config_id);
+/* SM count of the current device and the number of two-CTA clusters of the
+ * CTA-pair kernel that can be resident at once (its persistent grid size). */
+int fp8bs_device_info(int *num_sms, int *pair_clusters);
 /* Number of kernels one fp8bs_gemm call launches (1). */
 int fp8bs_launches_per_call(void);
 /* Number of kernels one fp8mx_gemm call launches (2: scale pack + GEMM). */

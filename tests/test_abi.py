@@ -96,11 +96,12 @@ def test_sf_atom_layout_is_a_bijection(lib):
 
 def test_config_selection(lib):
     # wide tiles for the large shapes, the narrow tile when a wide grid would starve the SMs
-    # blockscale: the CTA-pair kernel (256 x 128 pair tiles) for every shape class
-    for M, N, K in [(4096, 2048, 7168), (16384, 1536, 7168), (16384, 7168, 768), (4096, 65536, 1536),
-                    (256, 512, 512)]:
+    # blockscale: wide one-CTA tiles for the large shape classes, the narrow tile
+    # when a wide grid would starve the SMs
+    for M, N, K in [(4096, 2048, 7168), (16384, 1536, 7168), (16384, 7168, 768), (4096, 65536, 1536)]:
         c = lib.decode_config(lib.select_config("bs", M, N, K, 152))
-        assert c["kind"] == "blockscale_pair" and c["block_n"] == 128 and c["stages"] == 8
+        assert c["kind"] == "blockscale" and c["block_n"] == 256 and c["stages"] == 4
+    assert lib.decode_config(lib.select_config("bs", 256, 512, 512, 152))["block_n"] == 128
     # mxfp8: wide tiles, the narrow tile when the wide grid would starve the SMs
     assert lib.decode_config(lib.select_config("mx", 16384, 5120, 2048, 152))["block_n"] == 256
     assert lib.decode_config(lib.select_config("mx", 256, 512, 512, 152))["block_n"] == 128

@@ -163,7 +163,7 @@ def test_repeat_calls_bitwise_identical_and_config_recorded():
     cid = f.last_config_id()
     b = run_blockscale(x.A, x.a_scale, x.B, x.b_scale)
     assert np.array_equal(a, b)
-    assert f.decode_config(cid)["kind"] == "blockscale"
+    assert f.decode_config(cid)["kind"].startswith("blockscale")
 
 
 def test_pack_a_scale_bit_exact():
