@@ -33,6 +33,8 @@ _SIGS = {
     "fp8mx_packed_scale_bytes": (_i64, [_i, _i]),
     "fp8mx_pack_scales": (_i, [_p, _p, _i, _i, _p]),
     "fp8mx_launches_per_call": (_i, []),
+    "fp8mx_gemm_noalloc": (_i, [_p, _p, _p, _p, _p, _i, _i, _i, _p]),
+    "fp8mx_noalloc_scratch_bytes": (_i64, []),
     "fp8bs_a_scale_ld": (_i64, [_i]),
     "fp8bs_a_scale_index": (_i64, [_i, _i, _i]),
     "fp8bs_b_scale_index": (_i64, [_i, _i, _i]),
@@ -57,7 +59,7 @@ for _name, (_res, _args) in _SIGS.items():
 
 STATUS = {0: "FP8BS_OK", -1: "FP8BS_ERR_NULL", -2: "FP8BS_ERR_ALIGN", -3: "FP8BS_ERR_SHAPE",
           -4: "FP8BS_ERR_UNSUPPORTED_DEVICE", -5: "FP8BS_ERR_LAUNCH", -6: "FP8BS_ERR_DEVICE_TIMEOUT",
-          -7: "FP8BS_ERR_CUDA"}
+          -7: "FP8BS_ERR_CUDA", -8: "FP8BS_ERR_SCRATCH_TOO_SMALL"}
 
 
 class Fp8bsError(RuntimeError):

@@ -478,6 +478,8 @@ const char *fp8bs_status_string(int status)
     case FP8BS_ERR_LAUNCH: return "tensor-map encoding or kernel launch failed";
     case FP8BS_ERR_DEVICE_TIMEOUT: return "a device-side wait exceeded its time limit";
     case FP8BS_ERR_CUDA: return "CUDA runtime error";
+    case FP8BS_ERR_SCRATCH_TOO_SMALL:
+        return "the packed scales exceed the fixed scratch array of fp8mx_gemm_noalloc";
     default: return "unknown status";
     }
 }
@@ -530,5 +532,128 @@ int fp8mx_launches_per_call(void) { return 2; }
 void fp8bs_set_wait_limit_ns(uint64_t ns) { g_wait_limit_ns.store(ns ? ns : kDefaultWaitLimitNs); }
 
 const char *fp8bs_version(void) { return "fp8bs 0.2.0 (sm_103a)"; }
+
+} // extern "C"
+
+// ---------------------------------------------------------------------------
+// Allocation-free MXFP8 entry point (fp8mx_gemm_noalloc). Its packed-scale
+// scratch is this fixed device array instead of a pool allocation. The array
+// exists in every device context that loads the library, until the process
+// exits. Host code must not pass the symbol itself to a kernel (on the host it
+// only names a stand-in); the set-up below fetches its device address once per
+// device with that device current.
+
+namespace fp8bs {
+namespace host {
+
+constexpr size_t kNoAllocScratchBytes = size_t(8) << 20;   // 8 MiB: packed scales of A and B together
+static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
+
+struct NoAllocDevice {
+    bool ready = false;
+    int status = FP8BS_OK;
+    int num_sms = 0;
+    int *status_ptr = nullptr;
+    uint8_t *scratch = nullptr;   // device address of g_noalloc_scratch
+};
+NoAllocDevice g_noalloc_dev[kMaxDevices];
+
+// Once per device, with that device current; allocates nothing.
+int noalloc_setup(int &dev, NoAllocDevice *&nd)
+{
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
+        return FP8BS_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_mutex);
+    nd = &g_noalloc_dev[dev];
+    if (nd->ready)
+        return nd->status;
+    nd->ready = true;
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&nd->num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return nd->status = FP8BS_ERR_CUDA;
+    if (major != 10 || minor != 3)
+        return nd->status = FP8BS_ERR_UNSUPPORTED_DEVICE;
+    if (cudaGetSymbolAddress(reinterpret_cast<void **>(&nd->status_ptr), g_status_word) != cudaSuccess)
+        return nd->status = FP8BS_ERR_CUDA;
+    if (cudaGetSymbolAddress(reinterpret_cast<void **>(&nd->scratch), g_noalloc_scratch) != cudaSuccess ||
+        !nd->scratch)
+        return nd->status = FP8BS_ERR_CUDA;
+    if (!g_encode) {
+        cudaDriverEntryPointQueryResult q;
+        void *fn = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess || !fn)
+            return nd->status = FP8BS_ERR_CUDA;
+        g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+    }
+    return nd->status = FP8BS_OK;
+}
+
+} // namespace host
+} // namespace fp8bs
+
+extern "C" {
+
+int64_t fp8mx_noalloc_scratch_bytes(void) { return static_cast<int64_t>(kNoAllocScratchBytes); }
+
+int fp8mx_gemm_noalloc(const void *A, const uint8_t *a_e8m0, const void *B, const uint8_t *b_e8m0, void *C, int M,
+                       int N, int K, void *stream)
+{
+    int rc = check_shape(M, N, K);
+    if (rc)
+        return rc;
+    if (M == 0)
+        return FP8BS_OK;
+    if (!A || !a_e8m0 || !B || !b_e8m0 || !C)
+        return FP8BS_ERR_NULL;
+    if (!aligned(A, 16) || !aligned(a_e8m0, 4) || !aligned(B, 16) || !aligned(b_e8m0, 4) || !aligned(C, 16))
+        return FP8BS_ERR_ALIGN;
+    const size_t a_bytes = static_cast<size_t>(fp8mx_packed_scale_bytes(M, K));
+    const size_t b_bytes = static_cast<size_t>(fp8mx_packed_scale_bytes(N, K));
+    if (a_bytes + b_bytes > kNoAllocScratchBytes)
+        return FP8BS_ERR_SCRATCH_TOO_SMALL;
+    int dev;
+    NoAllocDevice *nd;
+    if ((rc = noalloc_setup(dev, nd)))
+        return rc;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    uint8_t *a_sf = nd->scratch;             // every byte used is rewritten by the pack kernel
+    uint8_t *b_sf = nd->scratch + a_bytes;   // a_bytes is a multiple of 512
+    rc = launch_pack_scales(a_e8m0, a_sf, M, b_e8m0, b_sf, N, K, nd->num_sms, s);
+    if (rc)
+        return rc;
+    Config cfg = choose_config(2, M, N, K, nd->num_sms);
+    if (!override_config(2, 2, cfg))
+        return FP8BS_ERR_SHAPE;
+    CUtensorMap tmA, tmB, tmC;
+    if (!encode_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, A, K, M, K, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, B, K, N, K, 128, cfg.block_n, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_2d(&tmC, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, C, N, M, static_cast<uint64_t>(N) * 2, kCChunkCols, 32,
+                   CU_TENSOR_MAP_SWIZZLE_32B))
+        return FP8BS_ERR_LAUNCH;
+    GemmArgs args = {};
+    args.M = M;
+    args.N = N;
+    args.K = K;
+    args.raster.m_tiles = (M + kBlockM - 1) / kBlockM;
+    args.raster.n_tiles = (N + cfg.block_n - 1) / cfg.block_n;
+    args.raster.raster = cfg.raster;
+    args.raster.group = cfg.group;
+    args.a_sf = a_sf;
+    args.b_sf = b_sf;
+    args.status = nd->status_ptr;
+    args.wait_limit_ns = g_wait_limit_ns.load();
+    const int tiles = args.raster.num_tiles();
+    const int grid = tiles < nd->num_sms ? tiles : nd->num_sms;
+    cudaError_t e = cfg.block_n == 256 ? launch_mxfp8<256, 4>(tmA, tmB, tmC, args, grid, s)
+                                       : launch_mxfp8<128, 6>(tmA, tmB, tmC, args, grid, s);
+    if (e != cudaSuccess)
+        return FP8BS_ERR_LAUNCH;
+    t_last_config = config_id(cfg);
+    return FP8BS_OK;
+}
 
 } // extern "C"

@@ -31,7 +31,8 @@ typedef enum {
     FP8BS_ERR_UNSUPPORTED_DEVICE = -4, /* current device is not compute capability 10.3       */
     FP8BS_ERR_LAUNCH = -5,             /* the kernel launch or tensor-map encoding failed     */
     FP8BS_ERR_DEVICE_TIMEOUT = -6,     /* a device wait ran out of time (status word)         */
-    FP8BS_ERR_CUDA = -7                /* another CUDA runtime error                          */
+    FP8BS_ERR_CUDA = -7,               /* another CUDA runtime error                          */
+    FP8BS_ERR_SCRATCH_TOO_SMALL = -8   /* fp8mx_gemm_noalloc: problem exceeds its fixed scratch */
 } fp8bs_status;
 
 /*
@@ -108,6 +109,33 @@ int64_t fp8mx_packed_scale_bytes(int rows, int K);
  * rows past `rows` are zero. Asynchronous on `stream`, one kernel.
  */
 int fp8mx_pack_scales(const uint8_t *e8m0, uint8_t *packed, int rows, int K, void *stream);
+
+/*
+ * MXFP8 GEMM that allocates nothing (the source pages have no counterpart;
+ * this is a library-integration entry point). Same arguments, result and
+ * shape rules as fp8mx_gemm.
+ *
+ * For callers that must not allocate device memory on the calling path:
+ * engines that reserve all device memory up front and own the allocator (an
+ * allocation here could fail or fragment their arena), plugins inside a host
+ * framework that hands them no allocator, and code on latency-critical paths
+ * that forbids allocator calls. fp8mx_gemm takes its packed-scale workspace
+ * from a memory pool; this entry point uses a fixed device array of
+ * fp8mx_noalloc_scratch_bytes() bytes (8 MiB) built into the library instead,
+ * which every GPU that loads the library holds until the process exits.
+ *
+ * Limit: fp8mx_packed_scale_bytes(M, K) + fp8mx_packed_scale_bytes(N, K) must
+ * not exceed that size, else FP8BS_ERR_SCRATCH_TOO_SMALL (checked on the host,
+ * before anything runs). All calls share the one array: two calls whose kernels
+ * overlap on the GPU (e.g. on different streams without ordering between them)
+ * race on it. The first call on a device looks up the array's device address
+ * (no allocation); make that first call before any stream capture.
+ * Launches two kernels on `stream` (scale pack, GEMM), like fp8mx_gemm.
+ */
+int fp8mx_gemm_noalloc(const void *A, const uint8_t *a_e8m0, const void *B, const uint8_t *b_e8m0, void *C,
+                       int M, int N, int K, void *stream);
+/* Size in bytes of the fixed scratch array fp8mx_gemm_noalloc uses (8 MiB). */
+int64_t fp8mx_noalloc_scratch_bytes(void);
 
 /* ---- layout helpers (bit-exact; host functions, no CUDA calls) ---------- */
 
