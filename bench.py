@@ -56,6 +56,8 @@ def parse():
     p.add_argument("--cpu-seconds", type=float, default=12.0, help="target CPU time of the oracle sample")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--warmup-seconds", type=float, default=1.0,
+                   help="minimum warm-up duration (clock sampling); 0 for profiler runs")
     return p.parse_args()
 
 
@@ -260,7 +262,7 @@ def run_ours(args):
     # sampler (started above, stopped after the timed loop) sees steady-state clocks.
     t_w = time.perf_counter()
     n_w = 0
-    while n_w < max(args.warmup, 3) or time.perf_counter() - t_w < 1.0:
+    while n_w < max(args.warmup, 3) or time.perf_counter() - t_w < args.warmup_seconds:
         flush.fill_(1)
         step()
         n_w += 1
@@ -283,6 +285,24 @@ def run_ours(args):
     clocks = sampler.stop() if sampler else None
     per_ms = [a.elapsed_time(b) for a, b in ev]
     ms = statistics.mean(per_ms)
+    kernel_ms = ms
+    if kind == "mx":
+        # The dominant kernel alone (the GEMM on packed scales, without the
+        # scale-pack launch), same protocol: L2 flush, CUDA events on the stream.
+        a_sf = f.pack_mx_scales(d[1], K)
+        b_sf = f.pack_mx_scales(d[3], K)
+        for _ in range(3):
+            f.gemm_mxfp8_packed(d[0], a_sf, d[2], b_sf, C=C)
+        kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(args.steps)]
+        for i in range(args.steps):
+            flush.fill_(1)
+            kev[i][0].record(stream)
+            f.gemm_mxfp8_packed(d[0], a_sf, d[2], b_sf, C=C)
+            kev[i][1].record(stream)
+        torch.cuda.synchronize()
+        kernel_ms = statistics.mean(a.elapsed_time(b) for a, b in kev)
+        assert f.get_status() == 0
     if pg:
         t = torch.tensor([ms], device="cuda")
         pg.all_reduce(t, op=pg.ReduceOp.MAX)
@@ -292,15 +312,15 @@ def run_ours(args):
     flops = 2.0 * M * N * K
     value = world * flops / (ms * 1e-3) / 1e12
     peaks = load_peaks()
-    kernel_tflops = flops / (ms * 1e-3) / 1e12
+    kernel_tflops = flops / (kernel_ms * 1e-3) / 1e12
     traffic = profiled_traffic(kind, args.workload)
     roofline = {"bound": "tensor", "achieved": kernel_tflops, "peak": peaks["fp8_tflops"], "unit": "TFLOP/s",
                 "frac": kernel_tflops / peaks["fp8_tflops"], "traffic": traffic,
                 "peak_source": f"{peaks['source']}: 2 x MEASURED_PEAKS bf16_tflops (fp8/bf16 nominal ratio 2)"
                 if peaks["source"] == "measured" else "fallback 2 x 1900 TFLOP/s bf16",
                 "algorithmic_bytes": algorithmic_bytes(kind, M, N, K),
-                "hbm_time_frac": (algorithmic_bytes(kind, M, N, K) / (peaks["hbm_gbs"] * 1e9)) / (ms * 1e-3),
-                "kernel": KERNEL_NAMES[kind]}
+                "hbm_time_frac": (algorithmic_bytes(kind, M, N, K) / (peaks["hbm_gbs"] * 1e9)) / (kernel_ms * 1e-3),
+                "kernel": KERNEL_NAMES[kind], "kernel_ms": kernel_ms}
 
     e2e = None
     if not args.no_e2e:
@@ -321,7 +341,9 @@ def run_ours(args):
                        "parallelism": f"{world} independent replicas (weak scaling)",
                        "wall_s_timed_loop": wall, "warmup_steps_run": n_w, "ms_min": min(per_ms),
                        "ms_median": statistics.median(per_ms)},
-            "roofline": roofline, "gpu_launches": args.steps * f.lib().fp8bs_launches_per_call(),
+            "roofline": roofline,
+            "gpu_launches": args.steps * (f.lib().fp8bs_launches_per_call() if kind == "bs"
+                                          else f.lib().fp8mx_launches_per_call()),
             "clocks": clocks, "e2e": e2e, "cpu_baseline": cpu}
     if rank == 0:
         print(json.dumps(line), flush=True)
