@@ -170,6 +170,21 @@ def dist_setup(args):
     return world, rank, local
 
 
+def max_over_ranks(ms, pg, torch, device):
+    """The slowest rank's time (every rank gets it); `pg` is torch.distributed or None."""
+    if pg is None:
+        return ms
+    t = torch.tensor([float(ms)], dtype=torch.float64, device=device)
+    pg.all_reduce(t, op=pg.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate_tflops(world, flops_per_rank, ms):
+    """Whole-job throughput: every rank runs one GEMM of `flops_per_rank` per step
+    (weak scaling, no exchange), the job's step time is the slowest rank's."""
+    return world * flops_per_rank / (ms * 1e-3) / 1e12
+
+
 def make_device_inputs(kind, M, N, K, seed, torch):
     x = workloads.make_inputs(kind, M, N, K, seed)
     dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
@@ -284,7 +299,7 @@ def run_ours(args):
     wall = time.perf_counter() - wall0
     clocks = sampler.stop() if sampler else None
     per_ms = [a.elapsed_time(b) for a, b in ev]
-    ms = statistics.mean(per_ms)
+    ms = max_over_ranks(statistics.mean(per_ms), pg, torch, "cuda")
     kernel_ms = ms
     if kind == "mx":
         # The dominant kernel alone (the GEMM on packed scales, without the
@@ -303,14 +318,10 @@ def run_ours(args):
         torch.cuda.synchronize()
         kernel_ms = statistics.mean(a.elapsed_time(b) for a, b in kev)
         assert f.get_status() == 0
-    if pg:
-        t = torch.tensor([ms], device="cuda")
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        ms = float(t.item())
     assert f.get_status() == 0
 
     flops = 2.0 * M * N * K
-    value = world * flops / (ms * 1e-3) / 1e12
+    value = aggregate_tflops(world, flops, ms)
     peaks = load_peaks()
     kernel_tflops = flops / (kernel_ms * 1e-3) / 1e12
     traffic = profiled_traffic(kind, args.workload)

@@ -110,6 +110,13 @@ bool encode_2d(CUtensorMap *tm, CUtensorMapDataType dt, const void *base, uint64
                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Teardown waits (for work already issued) keep at least the default limit.
+unsigned long long teardown_limit()
+{
+    const unsigned long long w = g_wait_limit_ns.load();
+    return w > kDefaultWaitLimitNs ? w : kDefaultWaitLimitNs;
+}
+
 bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
 int check_shape(int M, int N, int K)
@@ -290,6 +297,7 @@ int fp8bs_gemm(const void *A, const float *a_scale, const void *B, const float *
     args.b_scale = b_scale;
     args.status = st->status_ptr;
     args.wait_limit_ns = g_wait_limit_ns.load();
+    args.teardown_limit_ns = teardown_limit();
     const int tiles = args.raster.num_tiles();
     const int grid = tiles < st->num_sms ? tiles : st->num_sms;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -343,6 +351,7 @@ int fp8mx_gemm_packed(const void *A, const uint8_t *a_sf, const void *B, const u
     args.b_sf = b_sf;
     args.status = st->status_ptr;
     args.wait_limit_ns = g_wait_limit_ns.load();
+    args.teardown_limit_ns = teardown_limit();
     const int tiles = args.raster.num_tiles();
     const int grid = tiles < st->num_sms ? tiles : st->num_sms;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -646,6 +655,7 @@ int fp8mx_gemm_noalloc(const void *A, const uint8_t *a_e8m0, const void *B, cons
     args.b_sf = b_sf;
     args.status = nd->status_ptr;
     args.wait_limit_ns = g_wait_limit_ns.load();
+    args.teardown_limit_ns = teardown_limit();
     const int tiles = args.raster.num_tiles();
     const int grid = tiles < nd->num_sms ? tiles : nd->num_sms;
     cudaError_t e = cfg.block_n == 256 ? launch_mxfp8<256, 4>(tmA, tmB, tmC, args, grid, s)

@@ -55,7 +55,8 @@ struct GemmArgs {
     const uint8_t *a_sf;       // mxfp8: packed scale atoms of A
     const uint8_t *b_sf;       // mxfp8: packed scale atoms of B
     int *status;               // per-device status word
-    unsigned long long wait_limit_ns;
+    unsigned long long wait_limit_ns;       // limit of every pipeline wait
+    unsigned long long teardown_limit_ns;   // limit of the waits for work already in flight (>= 1 s)
 };
 
 // Byte offset of (row r in 0..127, group j in 0..3) in a 512-byte scale-factor
@@ -89,14 +90,17 @@ __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, vola
     return true;
 }
 
-// Wait used only while tearing down: no abort check, same time limit.
+// Wait used only while tearing down, for copies or MMAs this CTA already
+// issued (they complete on their own): no abort check, and a limit of its own
+// that is never shorter than a second, so that an aborted CTA does not exit
+// while its own asynchronous work still targets its shared or tensor memory.
 __device__ __forceinline__ void wait_teardown(uint32_t bar, uint32_t parity, const GemmArgs &a)
 {
     if (ptx::mbar_try_wait(bar, parity))
         return;
     const uint64_t t0 = ptx::globaltimer();
     while (!ptx::mbar_try_wait(bar, parity)) {
-        if (ptx::globaltimer() - t0 > a.wait_limit_ns) {
+        if (ptx::globaltimer() - t0 > a.teardown_limit_ns) {
             atomicExch(a.status, kStatusTimeout);
             return;
         }

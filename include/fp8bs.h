@@ -189,7 +189,10 @@ int fp8bs_launches_per_call(void);
 /* Number of kernels one fp8mx_gemm call launches (2: scale pack + GEMM). */
 int fp8mx_launches_per_call(void);
 /* Set the per-wait device time limit in nanoseconds (default 2e9) used by
- * subsequent launches from this process; 0 restores the default. */
+ * subsequent launches from this process; 0 restores the default. A pipeline
+ * wait that exceeds it makes the kernel record FP8BS_ERR_DEVICE_TIMEOUT, stop
+ * issuing work, wait (with a limit of at least the default) for the copies and
+ * MMAs it already issued, free its tensor memory and return. */
 void fp8bs_set_wait_limit_ns(uint64_t ns);
 /* Library version string. */
 const char *fp8bs_version(void);
