@@ -148,7 +148,10 @@ bool decode_config_id(int id, Config &c)
     c.group = id % 10;
     if (c.group < 1 || c.raster > 1)
         return false;
-    if (c.kind == 1 || c.kind == 2)
+    if (c.kind == 1)
+        return (c.block_n == 256 && c.stages == 4) || (c.block_n == 128 && c.stages == 6) ||
+               (c.block_n == 160 && c.stages == 5);
+    if (c.kind == 2)
         return (c.block_n == 256 && c.stages == 4) || (c.block_n == 128 && c.stages == 6);
     if (c.kind == 3)
         return c.block_n == 128 && c.stages == kPairStages;
@@ -306,6 +309,8 @@ int fp8bs_gemm(const void *A, const float *a_scale, const void *B, const float *
         e = launch_blockscale_pair<kPairStages>(tmA, tmB, tmSA, tmC, args, st->pair_clusters, s);
     else if (cfg.block_n == 256)
         e = launch_blockscale<256, 4>(tmA, tmB, tmSA, tmC, args, grid, s);
+    else if (cfg.block_n == 160)
+        e = launch_blockscale<160, 5>(tmA, tmB, tmSA, tmC, args, grid, s);
     else
         e = launch_blockscale<128, 6>(tmA, tmB, tmSA, tmC, args, grid, s);
     if (e != cudaSuccess)

@@ -178,7 +178,7 @@ def test_pack_a_scale_bit_exact():
 
 
 # every built kernel configuration, forced through the override
-BS_CONFIGS = [1256411, 1128611, 3128811]      # one-CTA 128x256, one-CTA 128x128, CTA-pair 256x128
+BS_CONFIGS = [1256411, 1160511, 1128611, 3128811]   # one-CTA 128x256, 128x160, 128x128, CTA-pair 256x128
 MX_CONFIGS = [2256411, 2128611]
 
 
