@@ -272,7 +272,7 @@ __global__ void __launch_bounds__(kBsThreads, 1)
                 ptx::tc_fence_after();
                 const float sa = reinterpret_cast<const float *>(smem + L::OFF_SA + a * L::SA_BYTES)[row];
                 const float scale_lo = sa * sb_lo;
-                const float scale_hi = sa * sb_hi;
+                const float scale_hi = kTwoBlocks ? sa * sb_hi : scale_lo;
                 const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                                        static_cast<uint32_t>(buf * BN + wg * HALF);
                 if constexpr (kEarlyRelease) {
@@ -295,27 +295,29 @@ __global__ void __launch_bounds__(kBsThreads, 1)
                             acc[kChunk * c + j] = fmaf(__uint_as_float(part[kChunk * c + j]), sc, acc[kChunk * c + j]);
                     }
                 } else {
+                    // One N block per slice (BN = 256): two 64-column rounds; the
+                    // buffer is released as soon as the second round is loaded.
+                    static_assert(!kTwoBlocks && HALF == 128, "wide-tile promote");
 #pragma unroll
-                    for (int h = 0; h < HALF / 64; ++h) {
-                        uint32_t part[64];
-#pragma unroll
-                        for (int c = 0; c < 4; ++c)
-                            ptx::tmem_ld_32x32b_x16(taddr + h * 64 + kChunk * c, part + kChunk * c);
+                    for (int h = 0; h < 2; ++h) {
+                        uint32_t r0[32], r1[32];
+                        ptx::tmem_ld_32x32b_x32(taddr + h * 64, r0);
+                        ptx::tmem_ld_32x32b_x32(taddr + h * 64 + 32, r1);
                         ptx::tmem_wait_ld();
-#pragma unroll
-                        for (int c = 0; c < 4; ++c) {
-                            const float sc = ((hi_mask >> (4 * h + c)) & 1u) ? scale_hi : scale_lo;
-#pragma unroll
-                            for (int j = 0; j < kChunk; ++j)
-                                acc[h * 64 + kChunk * c + j] =
-                                    fmaf(__uint_as_float(part[kChunk * c + j]), sc, acc[h * 64 + kChunk * c + j]);
+                        if (h == 1) {
+                            ptx::tc_fence_before();
+                            __syncwarp();
+                            if (lane == 0) {
+                                ptx::mbar_arrive(tempty_bar(buf));
+                                ptx::mbar_arrive(sa_empty_bar(a));
+                            }
                         }
-                    }
-                    ptx::tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) {
-                        ptx::mbar_arrive(tempty_bar(buf));
-                        ptx::mbar_arrive(sa_empty_bar(a));
+#pragma unroll
+                        for (int j = 0; j < 32; ++j)
+                            acc[h * 64 + j] = fmaf(__uint_as_float(r0[j]), scale_lo, acc[h * 64 + j]);
+#pragma unroll
+                        for (int j = 0; j < 32; ++j)
+                            acc[h * 64 + 32 + j] = fmaf(__uint_as_float(r1[j]), scale_lo, acc[h * 64 + 32 + j]);
                     }
                 }
             }
