@@ -213,7 +213,8 @@ def select_config(kind: str, M: int, N: int, K: int, num_sms: int) -> int:
 def decode_config(cid: int) -> dict:
     return {"kind": {1: "blockscale", 2: "mxfp8", 3: "blockscale_pair"}.get(cid // 1000000, "?"),
             "block_n": (cid // 1000) % 1000,
-            "stages": (cid // 100) % 10, "raster": (cid // 10) % 10, "group": cid % 10}
+            "stages": (cid // 100) % 10, "raster": (cid // 10) % 10,
+            "schedule": {1: "tile", 2: "stream_k"}.get(cid % 10, "?")}
 
 
 def device_info() -> dict:

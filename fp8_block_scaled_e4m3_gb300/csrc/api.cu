@@ -47,6 +47,7 @@ std::mutex g_mutex;
 DeviceState g_dev[kMaxDevices];
 std::atomic<unsigned long long> g_wait_limit_ns{kDefaultWaitLimitNs};
 std::atomic<int> g_config_override{0};
+std::atomic<unsigned long long> g_sk_token{0};   // stream-K hand-off tokens, unique per call
 thread_local int t_last_config = 0;
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
@@ -128,14 +129,14 @@ int check_shape(int M, int N, int K)
 
 // Kernel configuration. kind 1: one-CTA blockscale kernel, 2: MXFP8 kernel,
 // 3: CTA-pair blockscale kernel (256 x 128 tiles over two SMs).
+// sched 1: one CTA per tile; 2: stream-K (blockscale one-CTA kernel only).
 struct Config {
-    int kind, block_n, stages, raster, group;
+    int kind, block_n, stages, raster, sched;
 };
 
 int config_id(const Config &c)
 {
-    const int gcode = c.group >= 9 ? 9 : c.group;
-    return c.kind * 1000000 + c.block_n * 1000 + c.stages * 100 + c.raster * 10 + gcode;
+    return c.kind * 1000000 + c.block_n * 1000 + c.stages * 100 + c.raster * 10 + c.sched;
 }
 
 // Only the instantiated kernels are valid configurations.
@@ -145,8 +146,8 @@ bool decode_config_id(int id, Config &c)
     c.block_n = (id / 1000) % 1000;
     c.stages = (id / 100) % 10;
     c.raster = (id / 10) % 10;
-    c.group = id % 10;
-    if (c.group < 1 || c.raster > 1)
+    c.sched = id % 10;
+    if (c.sched < 1 || c.sched > 2 || c.raster > 1 || (c.sched == 2 && c.kind != 1))
         return false;
     if (c.kind == 1)
         return (c.block_n == 256 && c.stages == 4) || (c.block_n == 128 && c.stages == 6) ||
@@ -161,11 +162,10 @@ bool decode_config_id(int id, Config &c)
 // Shape class -> configuration, from (M, N, K) only.
 Config choose_config(int kind, int M, int N, int K, int num_sms)
 {
-    (void)K;
     Config c;
     // Stream the larger operand once past a resident set of panels of the smaller one.
     c.raster = ((long)M >= (long)N) ? 1 : 0;
-    c.group = 1;
+    c.sched = 1;
     // Blockscale and MXFP8 alike: wide one-CTA tiles (128 x 256), which keep
     // shared-memory operand traffic at 96 B/clk per SM and give each tcgen05.mma
     // 128 clocks of work (narrower MMAs are issue-bound). The narrow tile only
@@ -181,6 +181,16 @@ Config choose_config(int kind, int M, int N, int K, int num_sms)
     } else {
         c.block_n = 256;
         c.stages = 4;
+    }
+    // Blockscale: stream-K when one CTA per tile would leave more than 8% of the
+    // SM-time of the last wave idle (e.g. 256 tiles on 152 SMs: 2 waves, 84%
+    // busy), and there are at least two K blocks to share.
+    const long long tiles = (long long)((M + 127) / 128) * ((N + c.block_n - 1) / c.block_n);
+    const long long units = tiles * (K / 128);
+    if (kind == 1 && tiles > 0 && K / 128 >= 2 && units < (1ll << 31) && num_sms > 0) {
+        const long long waves = (tiles + num_sms - 1) / num_sms;
+        if ((double)tiles < 0.92 * (double)(waves * num_sms))
+            c.sched = 2;
     }
     return c;
 }
@@ -296,14 +306,34 @@ int fp8bs_gemm(const void *A, const float *a_scale, const void *B, const float *
     args.raster.m_tiles = (M + tile_m - 1) / tile_m;
     args.raster.n_tiles = (N + cfg.block_n - 1) / cfg.block_n;
     args.raster.raster = cfg.raster;
-    args.raster.group = cfg.group;
+    args.raster.group = 1;
     args.b_scale = b_scale;
     args.status = st->status_ptr;
     args.wait_limit_ns = g_wait_limit_ns.load();
     args.teardown_limit_ns = teardown_limit();
     const int tiles = args.raster.num_tiles();
-    const int grid = tiles < st->num_sms ? tiles : st->num_sms;
+    int grid = tiles < st->num_sms ? tiles : st->num_sms;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
+    void *ws = nullptr;
+    if (cfg.sched == 2 && !pair) {
+        // Stream-K workspace from the stream-ordered pool: one fp32 partial tile
+        // and kEpiWarps flags per CTA. Fresh or reused memory never holds this
+        // call's token, and finishers reset the flags they consume.
+        const long long units = static_cast<long long>(tiles) * KB;
+        if (units >= (1ll << 31))
+            return FP8BS_ERR_SHAPE;
+        grid = units < st->num_sms ? static_cast<int>(units) : st->num_sms;
+        const size_t slot = static_cast<size_t>(kBlockM) * cfg.block_n * sizeof(float);
+        const size_t bytes = static_cast<size_t>(grid) * (slot + kEpiWarps * sizeof(unsigned long long));
+        if (cudaMallocFromPoolAsync(&ws, bytes, st->pool, s) != cudaSuccess)
+            return FP8BS_ERR_CUDA;
+        args.sk = 1;
+        args.sk_partial = static_cast<float *>(ws);
+        args.sk_flags = reinterpret_cast<unsigned long long *>(static_cast<char *>(ws) + grid * slot);
+        args.sk_token = g_sk_token.fetch_add(1) + 1;
+    } else if (cfg.sched == 2) {
+        return FP8BS_ERR_SHAPE;
+    }
     cudaError_t e;
     if (pair)
         e = launch_blockscale_pair<kPairStages>(tmA, tmB, tmSA, tmC, args, st->pair_clusters, s);
@@ -313,6 +343,8 @@ int fp8bs_gemm(const void *A, const float *a_scale, const void *B, const float *
         e = launch_blockscale<160, 5>(tmA, tmB, tmSA, tmC, args, grid, s);
     else
         e = launch_blockscale<128, 6>(tmA, tmB, tmSA, tmC, args, grid, s);
+    if (ws && cudaFreeAsync(ws, s) != cudaSuccess && e == cudaSuccess)
+        e = cudaErrorUnknown;
     if (e != cudaSuccess)
         return FP8BS_ERR_LAUNCH;
     t_last_config = config_id(cfg);
@@ -351,7 +383,7 @@ int fp8mx_gemm_packed(const void *A, const uint8_t *a_sf, const void *B, const u
     args.raster.m_tiles = (M + kBlockM - 1) / kBlockM;
     args.raster.n_tiles = (N + cfg.block_n - 1) / cfg.block_n;
     args.raster.raster = cfg.raster;
-    args.raster.group = cfg.group;
+    args.raster.group = 1;
     args.a_sf = a_sf;
     args.b_sf = b_sf;
     args.status = st->status_ptr;
@@ -655,7 +687,7 @@ int fp8mx_gemm_noalloc(const void *A, const uint8_t *a_e8m0, const void *B, cons
     args.raster.m_tiles = (M + kBlockM - 1) / kBlockM;
     args.raster.n_tiles = (N + cfg.block_n - 1) / cfg.block_n;
     args.raster.raster = cfg.raster;
-    args.raster.group = cfg.group;
+    args.raster.group = 1;
     args.a_sf = a_sf;
     args.b_sf = b_sf;
     args.status = nd->status_ptr;

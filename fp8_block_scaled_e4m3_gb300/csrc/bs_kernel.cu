@@ -6,6 +6,15 @@
 // unscaled and apply the arbitrary fp32 block scales in software after it, one
 // promote per K block, because those scales are not powers of two).
 //
+// Work schedule (WorkSpan in common.cuh): one CTA per tile, or stream-K, where
+// every CTA takes an equal share of the (tile, K block) units, so a partial last
+// wave of tiles leaves no SM idle. A tile cut between CTAs is summed by the CTA
+// holding its first K block: the others publish their scaled fp32 partials
+// (global workspace, one release flag per promote warp) before anything else,
+// and the finisher adds them after its own last K block. Sums stay in fp32 and
+// every partial is scaled before it is added, so the result is the same sum
+// in another order.
+//
 // Persistent, warp-specialised, one CTA per SM, 12 warps (3 warpgroups):
 //   warp 0      TMA producer: A tile [128 x 128] e4m3 and B tile [BN x 128] e4m3 of
 //               one K block into stage s of a STAGES-deep shared-memory ring
@@ -78,7 +87,6 @@ __global__ void __launch_bounds__(kBsThreads, 1)
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int KB = args.K / kBlockK;
-    const int num_tiles = args.raster.num_tiles();
 
     auto full_bar = [&](int s) { return sbase + L::OFF_BAR + 8u * s; };
     auto empty_bar = [&](int s) { return sbase + L::OFF_BAR + 8u * (STAGES + s); };
@@ -124,27 +132,26 @@ __global__ void __launch_bounds__(kBsThreads, 1)
             ptx::prefetch_tmap(&tmA);
             ptx::prefetch_tmap(&tmB);
             ptx::prefetch_tmap(&tmSA);
+            WorkSpan span;
+            span.init(args, KB);
             int it = 0;
-            bool ok = true;
-            for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
-                int mb, nb;
-                args.raster.coords(t, mb, nb);
-                for (int kb = 0; kb < KB; ++kb, ++it) {
-                    const int s = it % STAGES;
-                    const uint32_t ph = (it / STAGES) & 1;
-                    const int a = it % kSaSlots;
-                    const uint32_t aph = (it / kSaSlots) & 1;
-                    if (!wait_bounded(empty_bar(s), ph ^ 1, abort_flag, args) ||
-                        !wait_bounded(sa_empty_bar(a), aph ^ 1, abort_flag, args)) {
-                        ok = false;
-                        break;
-                    }
-                    ptx::mbar_arrive_expect_tx(full_bar(s), L::A_BYTES + L::B_BYTES);
-                    ptx::tma_load_2d(sbase + L::OFF_A + s * L::A_BYTES, &tmA, full_bar(s), kb * kBlockK, mb * kBlockM);
-                    ptx::tma_load_2d(sbase + L::OFF_B + s * L::B_BYTES, &tmB, full_bar(s), kb * kBlockK, nb * BN);
-                    ptx::mbar_arrive_expect_tx(sa_full_bar(a), L::SA_BYTES);
-                    ptx::tma_load_2d(sbase + L::OFF_SA + a * L::SA_BYTES, &tmSA, sa_full_bar(a), mb * kBlockM, kb);
-                }
+            int t, kb, mb = 0, nb = 0;
+            span.step(0, t, kb);
+            for (; it < span.total; ++it, span.advance(t, kb)) {
+                if (it == 0 || kb == 0)
+                    args.raster.coords(t, mb, nb);
+                const int s = it % STAGES;
+                const uint32_t ph = (it / STAGES) & 1;
+                const int a = it % kSaSlots;
+                const uint32_t aph = (it / kSaSlots) & 1;
+                if (!wait_bounded(empty_bar(s), ph ^ 1, abort_flag, args) ||
+                    !wait_bounded(sa_empty_bar(a), aph ^ 1, abort_flag, args))
+                    break;
+                ptx::mbar_arrive_expect_tx(full_bar(s), L::A_BYTES + L::B_BYTES);
+                ptx::tma_load_2d(sbase + L::OFF_A + s * L::A_BYTES, &tmA, full_bar(s), kb * kBlockK, mb * kBlockM);
+                ptx::tma_load_2d(sbase + L::OFF_B + s * L::B_BYTES, &tmB, full_bar(s), kb * kBlockK, nb * BN);
+                ptx::mbar_arrive_expect_tx(sa_full_bar(a), L::SA_BYTES);
+                ptx::tma_load_2d(sbase + L::OFF_SA + a * L::SA_BYTES, &tmSA, sa_full_bar(a), mb * kBlockM, kb);
             }
             // Every load issued must have landed before the CTA exits.
             for (int s = 0; s < STAGES; ++s) {
@@ -162,29 +169,25 @@ __global__ void __launch_bounds__(kBsThreads, 1)
         // --------------------------------------------------------- MMA issuer
         if (lane == 0) {
             constexpr uint32_t idesc = ptx::idesc_f8f6f4_e4m3(kBlockM, BN);
-            int it = 0;
-            bool ok = true;
-            for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
-                for (int kb = 0; kb < KB; ++kb, ++it) {
-                    const int s = it % STAGES;
-                    const uint32_t ph = (it / STAGES) & 1;
-                    const int buf = it % L::NBUF;
-                    const uint32_t tph = (it / L::NBUF) & 1;
-                    if (!wait_bounded(tempty_bar(buf), tph ^ 1, abort_flag, args) ||
-                        !wait_bounded(full_bar(s), ph, abort_flag, args)) {
-                        ok = false;
-                        break;
-                    }
-                    ptx::tc_fence_after();
-                    const uint64_t adesc = ptx::desc_kmajor_sw128(sbase + L::OFF_A + s * L::A_BYTES);
-                    const uint64_t bdesc = ptx::desc_kmajor_sw128(sbase + L::OFF_B + s * L::B_BYTES);
-                    const uint32_t d = tmem_base + static_cast<uint32_t>(buf * BN);
+            WorkSpan span;
+            span.init(args, KB);
+            for (int it = 0; it < span.total; ++it) {
+                const int s = it % STAGES;
+                const uint32_t ph = (it / STAGES) & 1;
+                const int buf = it % L::NBUF;
+                const uint32_t tph = (it / L::NBUF) & 1;
+                if (!wait_bounded(tempty_bar(buf), tph ^ 1, abort_flag, args) ||
+                    !wait_bounded(full_bar(s), ph, abort_flag, args))
+                    break;
+                ptx::tc_fence_after();
+                const uint64_t adesc = ptx::desc_kmajor_sw128(sbase + L::OFF_A + s * L::A_BYTES);
+                const uint64_t bdesc = ptx::desc_kmajor_sw128(sbase + L::OFF_B + s * L::B_BYTES);
+                const uint32_t d = tmem_base + static_cast<uint32_t>(buf * BN);
 #pragma unroll
-                    for (int kk = 0; kk < kBlockK / kMmaK; ++kk)
-                        ptx::mma_f8f6f4(d, adesc + 2 * kk, bdesc + 2 * kk, idesc, kk > 0 ? 1u : 0u);
-                    ptx::tc_commit(empty_bar(s));
-                    ptx::tc_commit(tfull_bar(buf));
-                }
+                for (int kk = 0; kk < kBlockK / kMmaK; ++kk)
+                    ptx::mma_f8f6f4(d, adesc + 2 * kk, bdesc + 2 * kk, idesc, kk > 0 ? 1u : 0u);
+                ptx::tc_commit(empty_bar(s));
+                ptx::tc_commit(tfull_bar(buf));
             }
             // No MMA may still be running when the tensor memory is freed.
             ptx::tc_commit(mma_done_bar);
@@ -206,14 +209,12 @@ __global__ void __launch_bounds__(kBsThreads, 1)
         const int row = q * 32 + lane;               // row of the tile
         const int NB = (args.N + 127) / 128;
         const uint32_t cstage = sbase + L::OFF_C + ew * kCStageBytes;
-        const int my_tiles = static_cast<int>(blockIdx.x) < num_tiles
-                                 ? (num_tiles - static_cast<int>(blockIdx.x) + static_cast<int>(gridDim.x) - 1) /
-                                       static_cast<int>(gridDim.x)
-                                 : 0;
-        const int total = my_tiles * KB;
+        WorkSpan span;
+        span.init(args, KB);
+        const int total = span.total;
 
-        // b_scale of flattened step g (tile g/KB of this CTA, K block g%KB) for
-        // the (at most two) 128-column N blocks of this thread's columns. Lane l
+        // b_scale of flattened step g for the (at most two) 128-column N blocks
+        // of this thread's columns. Lane l
         // of the warp loads step 32*b + l of batch b; the value for step g is
         // taken with a shuffle. Batch b+1 is requested when batch b starts, so
         // its loads have 32 K blocks to land.
@@ -222,10 +223,9 @@ __global__ void __launch_bounds__(kBsThreads, 1)
             hi = 0.f;
             if (g >= total)
                 return;
-            const int ti = g / KB;
-            const int kb = g - ti * KB;
-            int mb, nb;
-            args.raster.coords(static_cast<int>(blockIdx.x) + ti * static_cast<int>(gridDim.x), mb, nb);
+            int t, kb, mb, nb;
+            span.step(g, t, kb);
+            args.raster.coords(t, mb, nb);
             const int nblk = (nb * BN + wg * HALF) >> 7;
             if (nblk < NB)
                 lo = ptx::ldg_nc_f32(args.b_scale + static_cast<size_t>(nblk) * KB + kb);
@@ -239,20 +239,29 @@ __global__ void __launch_bounds__(kBsThreads, 1)
         float acc[HALF];
         int it = 0;
         bool ok = true;
-        for (int t = blockIdx.x; t < num_tiles; t += gridDim.x) {
-            int mb, nb;
-            args.raster.coords(t, mb, nb);
-            // chunks of 16 columns that lie in the second N block of the slice
-            const int col0 = nb * BN + wg * HALF;
+        while (it < total) {
+            // One segment: steps seg_start .. seg_end-1, the K blocks kb0.. of one
+            // tile. Only the two step indices stay live across the K loop; the
+            // tile and its coordinates are recomputed after it.
+            const int seg_start = it;
+            int seg_end;
             uint32_t hi_mask = 0;
+            {
+                int t, kb0, mb, nb;
+                span.step(it, t, kb0);
+                seg_end = it + ((KB - kb0) < (total - it) ? (KB - kb0) : (total - it));
+                args.raster.coords(t, mb, nb);
+                // chunks of 16 columns that lie in the second N block of the slice
+                const int col0 = nb * BN + wg * HALF;
 #pragma unroll
             for (int c = 0; c < NCH; ++c)
-                if (((col0 + kChunk * c) >> 7) != (col0 >> 7))
-                    hi_mask |= 1u << c;
+                    if (((col0 + kChunk * c) >> 7) != (col0 >> 7))
+                        hi_mask |= 1u << c;
+            }
 #pragma unroll
             for (int j = 0; j < HALF; ++j)
                 acc[j] = 0.f;
-            for (int kb = 0; kb < KB; ++kb, ++it) {
+            for (; it < seg_end; ++it) {
                 const float sb_lo = __shfl_sync(0xffffffffu, sb_cur_lo, it & 31);
                 const float sb_hi = __shfl_sync(0xffffffffu, sb_cur_hi, it & 31);
                 if ((it & 31) == 31) {
@@ -323,6 +332,56 @@ __global__ void __launch_bounds__(kBsThreads, 1)
             }
             if (!ok)
                 break;
+            int t, kb0, mb, nb, kb_last;
+            span.step(seg_start, t, kb0);
+            span.step(seg_end - 1, mb, kb_last);   // mb: scratch
+            args.raster.coords(t, mb, nb);
+            // Stream-K hand-off, warp by warp: warp ew of every CTA owns the same
+            // 32 rows x HALF columns of a tile, in slot layout [column/4][row].
+            const size_t slice = static_cast<size_t>(wg * HALF / 4) * kBlockM + static_cast<size_t>(row);
+            if (kb0 > 0) {
+                // Head of a tile begun by an earlier CTA: publish the scaled partial.
+                float *dst = args.sk_partial + static_cast<size_t>(blockIdx.x) * (BN * kBlockM) + 4 * slice;
+#pragma unroll
+                for (int j = 0; j < HALF; j += 4)
+                    ptx::st_global_v4_f32(dst + static_cast<size_t>(j / 4) * kBlockM * 4, acc[j], acc[j + 1], acc[j + 2],
+                                          acc[j + 3]);
+                __threadfence();
+                __syncwarp();
+                if (lane == 0)
+                    ptx::st_release_gpu_u64(args.sk_flags + static_cast<size_t>(blockIdx.x) * kEpiWarps + ew,
+                                            args.sk_token);
+                continue;
+            }
+            if (kb_last != KB - 1) {
+                // This CTA holds K block 0 of a cut tile: add the partials of the
+                // CTAs that hold the rest of it, then store the tile.
+                const int U = args.raster.num_tiles() * KB;
+                const int tile_end = (t + 1) * KB;
+                const int G = static_cast<int>(gridDim.x);
+                for (int c2 = static_cast<int>(blockIdx.x) + 1; c2 < G && WorkSpan::unit_begin(U, c2, G) < tile_end;
+                     ++c2) {
+                    unsigned long long *flag = args.sk_flags + static_cast<size_t>(c2) * kEpiWarps + ew;
+                    if (!sk_wait_flag(flag, args.sk_token, abort_flag, args)) {
+                        ok = false;
+                        break;
+                    }
+                    const float *src = args.sk_partial + static_cast<size_t>(c2) * (BN * kBlockM) + 4 * slice;
+#pragma unroll
+                    for (int j = 0; j < HALF; j += 4) {
+                        const float4 v = ptx::ld_cg_v4_f32(src + static_cast<size_t>(j / 4) * kBlockM * 4);
+                        acc[j] += v.x;
+                        acc[j + 1] += v.y;
+                        acc[j + 2] += v.z;
+                        acc[j + 3] += v.w;
+                    }
+                    __syncwarp();
+                    if (lane == 0)
+                        *reinterpret_cast<volatile unsigned long long *>(flag) = 0ull;   // ready for the next call
+                }
+                if (!ok)
+                    break;
+            }
             const int x0 = nb * BN + wg * HALF;
             const int y0 = mb * kBlockM + q * 32;
 #pragma unroll

@@ -57,6 +57,72 @@ struct GemmArgs {
     int *status;               // per-device status word
     unsigned long long wait_limit_ns;       // limit of every pipeline wait
     unsigned long long teardown_limit_ns;   // limit of the waits for work already in flight (>= 1 s)
+    // Stream-K schedule of the blockscale kernel (sk != 0): partial tiles are
+    // handed from the CTA that computed them to the CTA that stores the tile.
+    float *sk_partial;                // [gridDim.x][BN/4][128] float4: one partial tile per CTA
+    unsigned long long *sk_flags;     // [gridDim.x]: sk_token once that CTA's partial is written
+    unsigned long long sk_token;      // unique per call; a finisher resets the flag to 0
+    int sk;
+};
+
+// The work of one CTA as flattened steps g = 0 .. total-1, step g being K block
+// kb of tile t (tile order of TileRaster).
+//   sk == 0: one CTA per tile, tiles blockIdx.x, blockIdx.x + gridDim.x, ...
+//   sk != 0: stream-K. The units u = t * KB + kb are cut into gridDim.x
+//            contiguous, equal (to one unit) ranges; CTA c takes [u_c, u_c+1),
+//            u_c = floor(c * U / gridDim.x). A tile cut between CTAs is finished
+//            (scaled partials added, C stored) by the CTA that holds its K block
+//            0, which is that CTA's last segment; the CTAs after it write their
+//            partials first thing, so the finisher never waits in practice.
+struct WorkSpan {
+    int u0;      // first unit (stream-K; tiles * KB < 2^31 is checked by the host)
+    int total;   // steps of this CTA
+    int KB;
+    int sk;
+
+    __device__ __forceinline__ static int unit_begin(int U, int c, int G)
+    {
+        return static_cast<int>((static_cast<long long>(c) * U) / G);
+    }
+
+    __device__ __forceinline__ void init(const GemmArgs &a, int KB_)
+    {
+        KB = KB_;
+        sk = a.sk;
+        const int c = static_cast<int>(blockIdx.x);
+        const int G = static_cast<int>(gridDim.x);
+        const int tiles = a.raster.num_tiles();
+        if (sk) {
+            const int U = tiles * KB;
+            u0 = unit_begin(U, c, G);
+            total = unit_begin(U, c + 1, G) - u0;
+        } else {
+            u0 = 0;
+            total = c < tiles ? ((tiles - c + G - 1) / G) * KB : 0;
+        }
+    }
+
+    __device__ __forceinline__ void step(int g, int &t, int &kb) const
+    {
+        if (sk) {
+            const int u = u0 + g;
+            t = u / KB;
+            kb = u - t * KB;
+        } else {
+            const int i = g / KB;
+            t = static_cast<int>(blockIdx.x) + i * static_cast<int>(gridDim.x);
+            kb = g - i * KB;
+        }
+    }
+
+    // (t, kb) of step g + 1 from that of step g.
+    __device__ __forceinline__ void advance(int &t, int &kb) const
+    {
+        if (++kb == KB) {
+            kb = 0;
+            t += sk ? 1 : static_cast<int>(gridDim.x);
+        }
+    }
 };
 
 // Byte offset of (row r in 0..127, group j in 0..3) in a 512-byte scale-factor
@@ -113,6 +179,28 @@ __device__ __forceinline__ bool wait_bounded_warp(uint32_t bar, uint32_t parity,
 {
     const bool ok = wait_bounded(bar, parity, abort_flag, a);
     return __all_sync(0xffffffffu, ok);
+}
+
+// Warp-uniform bounded wait until *flag == token, i.e. until another CTA of this
+// launch has published its partial tile. Every lane acquires the flag itself,
+// so its own later loads of the partial are ordered after the publication.
+__device__ __forceinline__ bool sk_wait_flag(const unsigned long long *flag, unsigned long long token,
+                                             volatile int *abort_flag, const GemmArgs &a)
+{
+    bool got = ptx::ld_acquire_gpu_u64(flag) == token;
+    if (!got) {
+        const uint64_t t0 = ptx::globaltimer();
+        while (!(got = (ptx::ld_acquire_gpu_u64(flag) == token))) {
+            if (*abort_flag)
+                break;
+            if (ptx::globaltimer() - t0 > a.wait_limit_ns) {
+                *abort_flag = 1;
+                atomicExch(a.status, kStatusTimeout);
+                break;
+            }
+        }
+    }
+    return __all_sync(0xffffffffu, got);
 }
 
 // Store one epilogue warp's 32 rows x 16 columns of C (row = lane) with one

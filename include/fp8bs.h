@@ -5,8 +5,9 @@
  * CUDA device addresses owned by the caller; `stream` is a cudaStream_t passed
  * as void* (NULL = the legacy default stream). Every GEMM call is asynchronous
  * on `stream`, performs no host synchronisation and no allocation after the
- * first call on a device (except fp8mx_gemm's pooled workspace, see there),
- * and can be captured in a CUDA graph.
+ * first call on a device (except the pooled workspaces of fp8mx_gemm and of
+ * fp8bs_gemm's stream-K schedule, see there), and can be captured in a CUDA
+ * graph.
  *
  * Error behaviour: functions return FP8BS_OK (0) or a negative fp8bs_status.
  * Argument errors are detected on the host before anything is launched.
@@ -56,6 +57,16 @@ typedef enum {
  * Shape rules: M >= 1; N >= 8 and N % 8 == 0; K >= 128, K % 128 == 0 and
  * K <= 1048576. Otherwise FP8BS_ERR_SHAPE. M = 0 is a no-op returning FP8BS_OK.
  * A partial last N block of 128 rows uses its own b_scale row.
+ *
+ * Schedule: one CTA per output tile, or, when that would leave more than 8% of
+ * the last wave's SM-time idle, stream-K: the (tile, K block) units are split
+ * evenly over the CTAs and a tile cut between CTAs is summed in fp32 from their
+ * scaled partials (the same sum in another order). Stream-K takes a workspace
+ * of grid * (128 * 256 * 4 + 64) bytes from a stream-ordered memory pool,
+ * allocated and freed on `stream` around the launch (allocation failure:
+ * FP8BS_ERR_CUDA). Inside a CUDA graph that workspace is reused by every
+ * replay; a replay that ends in FP8BS_ERR_DEVICE_TIMEOUT leaves the results of
+ * later replays of the same graph undefined.
  */
 int fp8bs_gemm(const void *A, const float *a_scale, const void *B, const float *b_scale, void *C,
                int M, int N, int K, void *stream);
@@ -168,9 +179,9 @@ int fp8bs_get_status(void *stream);
 const char *fp8bs_status_string(int status);
 /* Identifier of the kernel configuration the last successful GEMM call on this
  * host thread launched (0 if none): kind*1000000 + block_n*1000 + stages*100 +
- * raster*10 + group_code; kind 1 = one-CTA blockscale kernel (128 x block_n
+ * raster*10 + schedule; kind 1 = one-CTA blockscale kernel (128 x block_n
  * tiles), 2 = mxfp8 kernel, 3 = CTA-pair blockscale kernel (256 x block_n tiles
- * over two SMs). */
+ * over two SMs); schedule 1 = one CTA per tile, 2 = stream-K (kind 1 only). */
 int fp8bs_last_config_id(void);
 /* Configuration id fp8bs_gemm / fp8mx_gemm would choose for a shape on a
  * device with `num_sms` SMs (host-only, no CUDA calls). */

@@ -178,7 +178,8 @@ def test_pack_a_scale_bit_exact():
 
 
 # every built kernel configuration, forced through the override
-BS_CONFIGS = [1256411, 1160511, 1128611, 3128811]   # one-CTA 128x256, 128x160, 128x128, CTA-pair 256x128
+# one-CTA 128x256, 128x160, 128x128 (one CTA per tile, then stream-K), CTA-pair 256x128
+BS_CONFIGS = [1256411, 1160511, 1128611, 1256412, 1160512, 1128612, 3128811]
 MX_CONFIGS = [2256411, 2128611]
 
 
@@ -323,3 +324,67 @@ def test_full_blockscale_other_shapes(name):
 @pytest.mark.parametrize("N,K", [(5120, 2048), (8192, 1280)])
 def test_full_mxfp8(M, N, K):
     _check_full_size("mx", M, N, K, 0)
+
+
+# ---------------------------------------------------------------- stream-K
+@pytest.mark.parametrize("cfg", [1256412, 1128612])
+@pytest.mark.parametrize("M,N,K", [(256, 512, 7168), (130, 264, 3840)])
+def test_stream_k_tiles_cut_between_many_ctas(override, cfg, M, N, K):
+    """Few tiles and long K: each tile is shared by dozens of CTAs (every one but
+    the first publishing a partial), and ragged M/N tails sit in cut tiles."""
+    import fp8_block_scaled_e4m3_gb300 as f
+    raster = 1 if M >= N else 0
+    cid = cfg - (cfg // 10 % 10) * 10 + raster * 10
+    override(cid)
+    x = workloads.make_blockscale_inputs(M, N, K, seed=M + N)
+    got = run_blockscale(x.A, x.a_scale, x.B, x.b_scale)
+    assert f.last_config_id() == cid
+    compare(got, oracle.blockscale(x.A, x.a_scale, x.B, x.b_scale), f"stream-K {cid} {M}x{N}x{K}")
+
+
+def test_stream_k_back_to_back_calls_use_fresh_partials(override):
+    """Consecutive calls reuse the pooled workspace: each must see only its own
+    partials (per-call tokens, flags reset by the finishers)."""
+    import torch
+    import fp8_block_scaled_e4m3_gb300 as f
+    override(1256412)
+    M, N, K = 512, 768, 4096
+    xs = [workloads.make_blockscale_inputs(M, N, K, seed=s) for s in (21, 22)]
+    dev = [(to_dev(x.A), to_dev(workloads.a_scale_to_kmajor(x.a_scale)), to_dev(x.B),
+            to_dev(np.ascontiguousarray(x.b_scale))) for x in xs]
+    outs = [f.gemm_blockscale(*d) for d in (dev[0], dev[1], dev[0])]   # no sync in between
+    assert f.get_status() == 0
+    bits = [o.view(torch.int16).cpu().numpy().view(np.uint16) for o in outs]
+    for b, x in zip(bits, (xs[0], xs[1], xs[0])):
+        compare(b, oracle.blockscale(x.A, x.a_scale, x.B, x.b_scale), "stream-K back to back")
+    assert np.array_equal(bits[0], bits[2])
+
+
+def test_blockscale_cuda_graph_replay(override):
+    """Both schedules captured in a CUDA graph (the stream-K workspace becomes a
+    graph allocation) and replayed on new input contents."""
+    import torch
+    import fp8_block_scaled_e4m3_gb300 as f
+    M, N, K = 384, 640, 2048
+    for cid in (1256411, 1256412):
+        override(cid)
+        x0, x1 = (workloads.make_blockscale_inputs(M, N, K, seed=s) for s in (31, 32))
+        d = [to_dev(x0.A), to_dev(workloads.a_scale_to_kmajor(x0.a_scale)), to_dev(x0.B),
+             to_dev(np.ascontiguousarray(x0.b_scale))]
+        C = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+        f.gemm_blockscale(*d, C=C)          # first call outside the capture (device set-up)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            f.gemm_blockscale(*d, C=C)
+        for x in (x1, x0, x1):
+            d[0].copy_(to_dev(x.A))
+            d[1].copy_(to_dev(workloads.a_scale_to_kmajor(x.a_scale)))
+            d[2].copy_(to_dev(x.B))
+            d[3].copy_(to_dev(np.ascontiguousarray(x.b_scale)))
+            C.zero_()
+            g.replay()
+            assert f.get_status() == 0
+            got = C.view(torch.int16).cpu().numpy().view(np.uint16)
+            compare(got, oracle.blockscale(x.A, x.a_scale, x.B, x.b_scale), f"graph replay {cid}")
+        del g
