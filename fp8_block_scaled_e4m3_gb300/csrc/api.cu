@@ -259,6 +259,37 @@ __global__ void pack_a_scale_kernel(const float *__restrict__ src, float *__rest
     }
 }
 
+// Tensor maps, arguments and launch of the MXFP8 kernel on packed scales
+// (persistent grid of min(tiles, SMs) CTAs).
+int launch_mx(const Config &cfg, const void *A, const uint8_t *a_sf, const void *B, const uint8_t *b_sf, void *C,
+              int M, int N, int K, int *status_ptr, int num_sms, cudaStream_t s)
+{
+    CUtensorMap tmA, tmB, tmC;
+    if (!encode_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, A, K, M, K, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, B, K, N, K, 128, cfg.block_n, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_2d(&tmC, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, C, N, M, static_cast<uint64_t>(N) * 2, kCChunkCols, 32,
+                   CU_TENSOR_MAP_SWIZZLE_32B))
+        return FP8BS_ERR_LAUNCH;
+    GemmArgs args = {};
+    args.M = M;
+    args.N = N;
+    args.K = K;
+    args.raster.m_tiles = (M + kBlockM - 1) / kBlockM;
+    args.raster.n_tiles = (N + cfg.block_n - 1) / cfg.block_n;
+    args.raster.raster = cfg.raster;
+    args.raster.group = 1;
+    args.a_sf = a_sf;
+    args.b_sf = b_sf;
+    args.status = status_ptr;
+    args.wait_limit_ns = g_wait_limit_ns.load();
+    args.teardown_limit_ns = teardown_limit();
+    const int tiles = args.raster.num_tiles();
+    const int grid = tiles < num_sms ? tiles : num_sms;
+    const cudaError_t e = cfg.block_n == 256 ? launch_mxfp8<256, 4>(tmA, tmB, tmC, args, grid, s)
+                                             : launch_mxfp8<128, 6>(tmA, tmB, tmC, args, grid, s);
+    return e == cudaSuccess ? FP8BS_OK : FP8BS_ERR_LAUNCH;
+}
+
 } // namespace host
 } // namespace fp8bs
 
@@ -370,32 +401,9 @@ int fp8mx_gemm_packed(const void *A, const uint8_t *a_sf, const void *B, const u
     Config cfg = choose_config(2, M, N, K, st->num_sms);
     if (!override_config(2, 2, cfg))
         return FP8BS_ERR_SHAPE;
-    CUtensorMap tmA, tmB, tmC;
-    if (!encode_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, A, K, M, K, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !encode_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, B, K, N, K, 128, cfg.block_n, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !encode_2d(&tmC, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, C, N, M, static_cast<uint64_t>(N) * 2, kCChunkCols, 32,
-                   CU_TENSOR_MAP_SWIZZLE_32B))
-        return FP8BS_ERR_LAUNCH;
-    GemmArgs args = {};
-    args.M = M;
-    args.N = N;
-    args.K = K;
-    args.raster.m_tiles = (M + kBlockM - 1) / kBlockM;
-    args.raster.n_tiles = (N + cfg.block_n - 1) / cfg.block_n;
-    args.raster.raster = cfg.raster;
-    args.raster.group = 1;
-    args.a_sf = a_sf;
-    args.b_sf = b_sf;
-    args.status = st->status_ptr;
-    args.wait_limit_ns = g_wait_limit_ns.load();
-    args.teardown_limit_ns = teardown_limit();
-    const int tiles = args.raster.num_tiles();
-    const int grid = tiles < st->num_sms ? tiles : st->num_sms;
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-    cudaError_t e = cfg.block_n == 256 ? launch_mxfp8<256, 4>(tmA, tmB, tmC, args, grid, s)
-                                       : launch_mxfp8<128, 6>(tmA, tmB, tmC, args, grid, s);
-    if (e != cudaSuccess)
-        return FP8BS_ERR_LAUNCH;
+    if ((rc = launch_mx(cfg, A, a_sf, B, b_sf, C, M, N, K, st->status_ptr, st->num_sms,
+                        static_cast<cudaStream_t>(stream))))
+        return rc;
     t_last_config = config_id(cfg);
     return FP8BS_OK;
 }
@@ -674,31 +682,8 @@ int fp8mx_gemm_noalloc(const void *A, const uint8_t *a_e8m0, const void *B, cons
     Config cfg = choose_config(2, M, N, K, nd->num_sms);
     if (!override_config(2, 2, cfg))
         return FP8BS_ERR_SHAPE;
-    CUtensorMap tmA, tmB, tmC;
-    if (!encode_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, A, K, M, K, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !encode_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, B, K, N, K, 128, cfg.block_n, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !encode_2d(&tmC, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, C, N, M, static_cast<uint64_t>(N) * 2, kCChunkCols, 32,
-                   CU_TENSOR_MAP_SWIZZLE_32B))
-        return FP8BS_ERR_LAUNCH;
-    GemmArgs args = {};
-    args.M = M;
-    args.N = N;
-    args.K = K;
-    args.raster.m_tiles = (M + kBlockM - 1) / kBlockM;
-    args.raster.n_tiles = (N + cfg.block_n - 1) / cfg.block_n;
-    args.raster.raster = cfg.raster;
-    args.raster.group = 1;
-    args.a_sf = a_sf;
-    args.b_sf = b_sf;
-    args.status = nd->status_ptr;
-    args.wait_limit_ns = g_wait_limit_ns.load();
-    args.teardown_limit_ns = teardown_limit();
-    const int tiles = args.raster.num_tiles();
-    const int grid = tiles < nd->num_sms ? tiles : nd->num_sms;
-    cudaError_t e = cfg.block_n == 256 ? launch_mxfp8<256, 4>(tmA, tmB, tmC, args, grid, s)
-                                       : launch_mxfp8<128, 6>(tmA, tmB, tmC, args, grid, s);
-    if (e != cudaSuccess)
-        return FP8BS_ERR_LAUNCH;
+    if ((rc = launch_mx(cfg, A, a_sf, B, b_sf, C, M, N, K, nd->status_ptr, nd->num_sms, s)))
+        return rc;
     t_last_config = config_id(cfg);
     return FP8BS_OK;
 }

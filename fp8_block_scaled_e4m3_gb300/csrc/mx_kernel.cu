@@ -105,6 +105,7 @@ __global__ void __launch_bounds__(kMxThreads, 1)
         if (lane == 0) {
             ptx::prefetch_tmap(&tmA);
             ptx::prefetch_tmap(&tmB);
+            const int n_blocks = (args.N + 127) / 128;   // packed atoms per K step of B
             int it = 0;
             bool ok = true;
             for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
@@ -120,13 +121,18 @@ __global__ void __launch_bounds__(kMxThreads, 1)
                     ptx::mbar_arrive_expect_tx(full_bar(s), L::A_BYTES + L::B_BYTES + L::SF_BYTES);
                     ptx::tma_load_2d(sbase + L::OFF_A + s * L::A_BYTES, &tmA, full_bar(s), ks * kBlockK, mb * kBlockM);
                     ptx::tma_load_2d(sbase + L::OFF_B + s * L::B_BYTES, &tmB, full_bar(s), ks * kBlockK, nb * BN);
+                    // Scale atoms. A 128-row B block past N (the second half of a
+                    // 256-wide tile when N has an odd number of 128-row blocks) reads
+                    // the last real atom instead: those B rows are zero-filled by the
+                    // tensor copy and their C columns are never stored.
                     const uint32_t sf_smem = sbase + L::OFF_SF + s * L::SF_BYTES;
                     ptx::bulk_load(sf_smem, args.a_sf + (static_cast<size_t>(mb) * KS + ks) * 512, 512, full_bar(s));
 #pragma unroll
-                    for (int h = 0; h < BN / 128; ++h)
+                    for (int h = 0; h < BN / 128; ++h) {
+                        const int bblk = nb * (BN / 128) + h < n_blocks ? nb * (BN / 128) + h : n_blocks - 1;
                         ptx::bulk_load(sf_smem + L::SFA_BYTES + 512 * h,
-                                       args.b_sf + (static_cast<size_t>(nb * (BN / 128) + h) * KS + ks) * 512, 512,
-                                       full_bar(s));
+                                       args.b_sf + (static_cast<size_t>(bblk) * KS + ks) * 512, 512, full_bar(s));
+                    }
                 }
             }
             for (int s = 0; s < STAGES; ++s) {

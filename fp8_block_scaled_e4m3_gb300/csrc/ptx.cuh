@@ -123,12 +123,6 @@ __device__ __forceinline__ float ldg_nc_f32(const float *p)
 }
 
 // --------------------------------------- cross-CTA hand-off through global memory
-// Barrier over a subset of the CTA's warps (ids 1..15; id 0 is __syncthreads).
-__device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads)
-{
-    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
-}
-
 __device__ __forceinline__ void st_release_gpu_u64(unsigned long long *p, unsigned long long v)
 {
     asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
