@@ -147,7 +147,7 @@ bool decode_config_id(int id, Config &c)
     c.stages = (id / 100) % 10;
     c.raster = (id / 10) % 10;
     c.sched = id % 10;
-    if (c.sched < 1 || c.sched > 2 || c.raster > 1 || (c.sched == 2 && c.kind != 1))
+    if (c.sched < 1 || c.sched > 2 || c.raster > 1 || (c.sched == 2 && (c.kind != 1 || c.block_n != 256)))
         return false;
     if (c.kind == 1)
         return (c.block_n == 256 && c.stages == 4) || (c.block_n == 128 && c.stages == 6) ||
@@ -159,6 +159,17 @@ bool decode_config_id(int id, Config &c)
     return false;
 }
 
+// Stream-K grid: every CTA gets at least max(8, KB/4) K blocks, so a tile is
+// cut between at most about five CTAs and its finisher adds few partials.
+long long sk_grid(long long units, long long KB, int num_sms)
+{
+    const long long min_units = KB / 4 > 8 ? KB / 4 : 8;
+    long long g = units / min_units;
+    if (g > num_sms)
+        g = num_sms;
+    return g < 1 ? 1 : g;
+}
+
 // Shape class -> configuration, from (M, N, K) only.
 Config choose_config(int kind, int M, int N, int K, int num_sms)
 {
@@ -166,31 +177,34 @@ Config choose_config(int kind, int M, int N, int K, int num_sms)
     // Stream the larger operand once past a resident set of panels of the smaller one.
     c.raster = ((long)M >= (long)N) ? 1 : 0;
     c.sched = 1;
+    c.kind = kind;
     // Blockscale and MXFP8 alike: wide one-CTA tiles (128 x 256), which keep
     // shared-memory operand traffic at 96 B/clk per SM and give each tcgen05.mma
-    // 128 clocks of work (narrower MMAs are issue-bound). The narrow tile only
-    // when the wide one leaves most SMs idle. The CTA-pair blockscale kernel
-    // (kind 3) measured slower on every shape and is selectable by override.
-    c.kind = kind;
-    // Wide tiles (128 x 256) keep shared-memory operand traffic at 96 B/clk per
-    // SM; the narrow tile only when the wide one leaves most SMs idle.
-    const long tiles256 = (long)((M + 127) / 128) * ((N + 255) / 256);
+    // 128 clocks of work (narrower MMAs are issue-bound). The CTA-pair
+    // blockscale kernel (kind 3) measured slower on every shape and is
+    // selectable by override.
+    c.block_n = 256;
+    c.stages = 4;
+    const long long tiles256 = (long long)((M + 127) / 128) * ((N + 255) / 256);
+    // Blockscale: stream-K (256-wide tile) when it shortens the longest CTA's K
+    // loop by at least 8 K blocks (about 4 us at ~1000 clocks per block), which
+    // pays for the partial hand-off. E.g. 256 tiles x 56 K blocks on 152 SMs:
+    // 112 -> 95; 8 tiles x 56: 56 -> 3.
+    const long long KB = K / 128;
+    const long long units = tiles256 * KB;
+    if (kind == 1 && tiles256 > 0 && units < (1ll << 31) && num_sms > 0) {
+        const long long g = sk_grid(units, KB, num_sms);
+        const long long per_tile = (tiles256 + num_sms - 1) / num_sms * KB;   // one CTA per tile
+        const long long per_unit = (units + g - 1) / g;                       // stream-K
+        if (per_tile - per_unit >= 8) {
+            c.sched = 2;
+            return c;
+        }
+    }
+    // Otherwise the narrow tile when the wide one leaves most SMs idle.
     if (tiles256 * 2 <= num_sms) {
         c.block_n = 128;
         c.stages = 6;
-    } else {
-        c.block_n = 256;
-        c.stages = 4;
-    }
-    // Blockscale: stream-K when one CTA per tile would leave more than 8% of the
-    // SM-time of the last wave idle (e.g. 256 tiles on 152 SMs: 2 waves, 84%
-    // busy), and there are at least two K blocks to share.
-    const long long tiles = (long long)((M + 127) / 128) * ((N + c.block_n - 1) / c.block_n);
-    const long long units = tiles * (K / 128);
-    if (kind == 1 && tiles > 0 && K / 128 >= 2 && units < (1ll << 31) && num_sms > 0) {
-        const long long waves = (tiles + num_sms - 1) / num_sms;
-        if ((double)tiles < 0.92 * (double)(waves * num_sms))
-            c.sched = 2;
     }
     return c;
 }
@@ -346,14 +360,18 @@ int fp8bs_gemm(const void *A, const float *a_scale, const void *B, const float *
     int grid = tiles < st->num_sms ? tiles : st->num_sms;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     void *ws = nullptr;
-    if (cfg.sched == 2 && !pair) {
+    if (cfg.sched == 2 && !pair && cfg.block_n == 256) {
         // Stream-K workspace from the stream-ordered pool: one fp32 partial tile
         // and kEpiWarps flags per CTA. Fresh or reused memory never holds this
         // call's token, and finishers reset the flags they consume.
         const long long units = static_cast<long long>(tiles) * KB;
         if (units >= (1ll << 31))
             return FP8BS_ERR_SHAPE;
-        grid = units < st->num_sms ? static_cast<int>(units) : st->num_sms;
+        grid = static_cast<int>(sk_grid(units, KB, st->num_sms));
+        // Whole waves but the last one or two run one CTA per tile (the CTAs of
+        // a wave share A and B panels in L2); stream-K covers the rest.
+        const int full_waves = tiles / grid;
+        args.sk_dp = full_waves >= 2 ? full_waves - 1 : 0;
         const size_t slot = static_cast<size_t>(kBlockM) * cfg.block_n * sizeof(float);
         const size_t bytes = static_cast<size_t>(grid) * (slot + kEpiWarps * sizeof(unsigned long long));
         if (cudaMallocFromPoolAsync(&ws, bytes, st->pool, s) != cudaSuccess)

@@ -47,8 +47,11 @@
 namespace fp8bs {
 
 constexpr int kBsThreads = (4 + kEpiWarps) * 32;
-constexpr int kBsRegsLow = 40;
-constexpr int kBsRegsHigh = 232;
+// Register split (see the header comment): 40 / 232 for the 256-wide tile,
+// whose promote holds 128 accumulators and 64 partials per thread; 56 / 224
+// for the narrower tiles (at most 80 + 80), which gives the producer slack.
+template <int BN> constexpr int kBsRegsLow = BN == 256 ? 40 : 56;
+template <int BN> constexpr int kBsRegsHigh = BN == 256 ? 232 : 224;
 constexpr int kSaSlots = 16;   // a_scale ring depth (>= STAGES + NBUF, so it never holds back A/B)
 
 template <int BN, int STAGES>
@@ -125,7 +128,7 @@ __global__ void __launch_bounds__(kBsThreads, 1)
     const uint32_t tmem_base = *tmem_holder;
 
     if (warp < 4) {
-    ptx::setmaxnreg_dec<kBsRegsLow>();
+    ptx::setmaxnreg_dec<kBsRegsLow<BN>>();
     if (warp == 0) {
         // ------------------------------------------------------------ producer
         if (lane == 0) {
@@ -137,8 +140,8 @@ __global__ void __launch_bounds__(kBsThreads, 1)
             int it = 0;
             int t, kb, mb = 0, nb = 0;
             span.step(0, t, kb);
-            for (; it < span.total; ++it, span.advance(t, kb)) {
-                if (it == 0 || kb == 0)
+            for (; it < span.total; ++it, span.advance(it, t, kb)) {
+                if (it == 0 || kb == 0 || it == span.dp_steps)   // a new tile (a stream-K range may start mid-tile)
                     args.raster.coords(t, mb, nb);
                 const int s = it % STAGES;
                 const uint32_t ph = (it / STAGES) & 1;
@@ -195,13 +198,14 @@ __global__ void __launch_bounds__(kBsThreads, 1)
         }
     }
     } else {
-        ptx::setmaxnreg_inc<kBsRegsHigh>();
+        ptx::setmaxnreg_inc<kBsRegsHigh<BN>>();
         // ------------------------------------------------- promote + epilogue
         constexpr int HALF = BN / 2;                 // columns per thread
         constexpr int kChunk = 16;                   // columns per TMEM load / scale choice
         constexpr int NCH = HALF / kChunk;
         constexpr bool kEarlyRelease = HALF <= 80;   // the slice fits next to the accumulator
         constexpr bool kTwoBlocks = (BN % 128) != 0; // a slice may straddle two b_scale blocks
+        constexpr bool kSk = BN == 256;              // tile width with the stream-K hand-off
         static_assert(kCChunkCols == kChunk, "epilogue chunking");
         const int ew = warp - 4;                     // 0..7
         const int wg = ew >> 2;                      // column half
@@ -339,7 +343,8 @@ __global__ void __launch_bounds__(kBsThreads, 1)
             // Stream-K hand-off, warp by warp: warp ew of every CTA owns the same
             // 32 rows x HALF columns of a tile, in slot layout [column/4][row].
             const size_t slice = static_cast<size_t>(wg * HALF / 4) * kBlockM + static_cast<size_t>(row);
-            if (kb0 > 0) {
+            // (Stream-K runs with the 256-wide tile only; the host never sets it for the others.)
+            if (kSk && kb0 > 0) {
                 // Head of a tile begun by an earlier CTA: publish the scaled partial.
                 float *dst = args.sk_partial + static_cast<size_t>(blockIdx.x) * (BN * kBlockM) + 4 * slice;
 #pragma unroll
@@ -353,14 +358,16 @@ __global__ void __launch_bounds__(kBsThreads, 1)
                                             args.sk_token);
                 continue;
             }
-            if (kb_last != KB - 1) {
+            if (kSk && kb_last != KB - 1) {
                 // This CTA holds K block 0 of a cut tile: add the partials of the
                 // CTAs that hold the rest of it, then store the tile.
-                const int U = args.raster.num_tiles() * KB;
-                const int tile_end = (t + 1) * KB;
-                const int G = static_cast<int>(gridDim.x);
-                for (int c2 = static_cast<int>(blockIdx.x) + 1; c2 < G && WorkSpan::unit_begin(U, c2, G) < tile_end;
-                     ++c2) {
+                // The other CTAs of the tile: up to the one whose range holds the
+                // tile's last unit, the largest c with floor(c * U / G) <= unit.
+                const long long G = gridDim.x;
+                const long long U = static_cast<long long>(args.raster.num_tiles() - span.tile0) * KB;
+                const long long tile_end = static_cast<long long>(t + 1 - span.tile0) * KB;
+                const int c_last = static_cast<int>((tile_end * G - 1) / U);
+                for (int c2 = static_cast<int>(blockIdx.x) + 1; c2 <= c_last; ++c2) {
                     unsigned long long *flag = args.sk_flags + static_cast<size_t>(c2) * kEpiWarps + ew;
                     if (!sk_wait_flag(flag, args.sk_token, abort_flag, args)) {
                         ok = false;

@@ -63,22 +63,26 @@ struct GemmArgs {
     unsigned long long *sk_flags;     // [gridDim.x]: sk_token once that CTA's partial is written
     unsigned long long sk_token;      // unique per call; a finisher resets the flag to 0
     int sk;
+    int sk_dp;                        // stream-K: whole waves of tiles done one per CTA first
 };
 
 // The work of one CTA as flattened steps g = 0 .. total-1, step g being K block
 // kb of tile t (tile order of TileRaster).
 //   sk == 0: one CTA per tile, tiles blockIdx.x, blockIdx.x + gridDim.x, ...
-//   sk != 0: stream-K. The units u = t * KB + kb are cut into gridDim.x
-//            contiguous, equal (to one unit) ranges; CTA c takes [u_c, u_c+1),
-//            u_c = floor(c * U / gridDim.x). A tile cut between CTAs is finished
-//            (scaled partials added, C stored) by the CTA that holds its K block
-//            0, which is that CTA's last segment; the CTAs after it write their
-//            partials first thing, so the finisher never waits in practice.
+//   sk != 0: stream-K after sk_dp whole waves done one CTA per tile (so that a
+//            wave's CTAs share operand panels in L2). The units u = t' * KB + kb
+//            of the remaining tiles t' are cut into gridDim.x contiguous ranges
+//            equal to one unit; CTA c takes [u_c, u_c+1), u_c = floor(c * U /
+//            gridDim.x). A tile cut between CTAs is finished (scaled partials
+//            added, C stored) by the CTA that holds its K block 0, which is that
+//            CTA's last segment; the CTAs after it write their partials at the
+//            start of their range, so the finisher never waits in practice.
 struct WorkSpan {
-    int u0;      // first unit (stream-K; tiles * KB < 2^31 is checked by the host)
-    int total;   // steps of this CTA
+    int u0;         // first stream-K unit (tiles * KB < 2^31 is checked by the host)
+    int total;      // steps of this CTA
+    int dp_steps;   // steps done one CTA per tile, before the stream-K range (all of them without stream-K)
+    int tile0;      // first tile of the stream-K range
     int KB;
-    int sk;
 
     __device__ __forceinline__ static int unit_begin(int U, int c, int G)
     {
@@ -88,26 +92,30 @@ struct WorkSpan {
     __device__ __forceinline__ void init(const GemmArgs &a, int KB_)
     {
         KB = KB_;
-        sk = a.sk;
         const int c = static_cast<int>(blockIdx.x);
         const int G = static_cast<int>(gridDim.x);
         const int tiles = a.raster.num_tiles();
-        if (sk) {
-            const int U = tiles * KB;
+        if (a.sk) {
+            dp_steps = a.sk_dp * KB;
+            tile0 = a.sk_dp * G;
+            const int U = (tiles - tile0) * KB;
             u0 = unit_begin(U, c, G);
-            total = unit_begin(U, c + 1, G) - u0;
+            total = dp_steps + unit_begin(U, c + 1, G) - u0;
         } else {
             u0 = 0;
+            tile0 = tiles;
             total = c < tiles ? ((tiles - c + G - 1) / G) * KB : 0;
+            dp_steps = total;
         }
     }
 
     __device__ __forceinline__ void step(int g, int &t, int &kb) const
     {
-        if (sk) {
-            const int u = u0 + g;
+        if (g >= dp_steps) {
+            const int u = u0 + g - dp_steps;
             t = u / KB;
             kb = u - t * KB;
+            t += tile0;
         } else {
             const int i = g / KB;
             t = static_cast<int>(blockIdx.x) + i * static_cast<int>(gridDim.x);
@@ -115,12 +123,15 @@ struct WorkSpan {
         }
     }
 
-    // (t, kb) of step g + 1 from that of step g.
-    __device__ __forceinline__ void advance(int &t, int &kb) const
+    // (t, kb) of step g from that of step g - 1 (g >= 1).
+    __device__ __forceinline__ void advance(int g, int &t, int &kb) const
     {
         if (++kb == KB) {
             kb = 0;
-            t += sk ? 1 : static_cast<int>(gridDim.x);
+            if (g >= dp_steps)
+                step(g, t, kb);   // into or inside the stream-K range
+            else
+                t += static_cast<int>(gridDim.x);
         }
     }
 };

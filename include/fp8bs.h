@@ -58,8 +58,9 @@ typedef enum {
  * K <= 1048576. Otherwise FP8BS_ERR_SHAPE. M = 0 is a no-op returning FP8BS_OK.
  * A partial last N block of 128 rows uses its own b_scale row.
  *
- * Schedule: one CTA per output tile, or, when that would leave more than 8% of
- * the last wave's SM-time idle, stream-K: the (tile, K block) units are split
+ * Schedule: one CTA per output tile, or, when that shortens the longest CTA's
+ * loop by at least 8 K blocks (a partial last wave of tiles, or few tiles with
+ * a long K), stream-K: the (tile, K block) units are split
  * evenly over the CTAs and a tile cut between CTAs is summed in fp32 from their
  * scaled partials (the same sum in another order). Stream-K takes a workspace
  * of grid * (128 * 256 * 4 + 64) bytes from a stream-ordered memory pool,
@@ -181,7 +182,8 @@ const char *fp8bs_status_string(int status);
  * host thread launched (0 if none): kind*1000000 + block_n*1000 + stages*100 +
  * raster*10 + schedule; kind 1 = one-CTA blockscale kernel (128 x block_n
  * tiles), 2 = mxfp8 kernel, 3 = CTA-pair blockscale kernel (256 x block_n tiles
- * over two SMs); schedule 1 = one CTA per tile, 2 = stream-K (kind 1 only). */
+ * over two SMs); schedule 1 = one CTA per tile, 2 = stream-K (kind 1 with
+ * block_n 256 only). */
 int fp8bs_last_config_id(void);
 /* Configuration id fp8bs_gemm / fp8mx_gemm would choose for a shape on a
  * device with `num_sms` SMs (host-only, no CUDA calls). */

@@ -114,20 +114,21 @@ def test_config_selection(lib):
     assert L.fp8bs_set_config_override(1999911) == -3      # no such kernel
     assert L.fp8bs_set_config_override(2256412) == -3      # stream-K is blockscale-only
     assert L.fp8bs_set_config_override(1256413) == -3      # no such schedule
+    assert L.fp8bs_set_config_override(1128612) == -3      # stream-K runs with the 256-wide tile only
     assert L.fp8bs_set_config_override(0) == 0
 
 
 def test_schedule_selection(lib):
-    # Stream-K exactly when one CTA per tile leaves more than 8% of the last
-    # wave idle (and K has at least two blocks to share).
+    # Stream-K exactly when it shortens the longest CTA's K loop by >= 8 K blocks.
     sched = lambda M, N, K, sms=152: lib.decode_config(lib.select_config("bs", M, N, K, sms))["schedule"]
-    assert sched(4096, 2048, 7168) == "stream_k"      # 256 tiles on 152 SMs: 84% busy
-    assert sched(16384, 1536, 7168) == "stream_k"     # 768 tiles: 6 waves, 84% busy
-    assert sched(16384, 7168, 768) == "tile"          # 3584 tiles: 24 waves, 98% busy
-    assert sched(4096, 65536, 1536) == "tile"         # 8192 tiles: 54 waves, 99.8% busy
+    assert sched(4096, 2048, 7168) == "stream_k"      # 256 tiles x 56: 112 -> 95 K blocks
+    assert sched(16384, 1536, 7168) == "stream_k"     # 768 tiles x 56: 336 -> 283
+    assert sched(256, 512, 7168) == "stream_k"        # 8 tiles x 56: 56 -> 3
+    assert sched(16384, 7168, 768) == "tile"          # 3584 tiles x 6: 144 -> 142
+    assert sched(4096, 65536, 1536) == "tile"         # 8192 tiles x 12: 648 -> 647
     assert sched(4096, 2048, 7168, sms=128) == "tile"   # 256 tiles = 2 full waves
     assert sched(4096, 2048, 128) == "tile"           # one K block: nothing to share
-    assert sched(256, 512, 512) == "stream_k"         # 8 tiles on 152 SMs
+    assert sched(256, 512, 512) == "tile"             # 8 tiles x 4: 4 -> 1, not worth a hand-off
     # the MXFP8 kernel has one schedule
     assert lib.decode_config(lib.select_config("mx", 4096, 2048, 7168, 152))["schedule"] == "tile"
 
