@@ -406,3 +406,29 @@ def test_stream_k_after_whole_waves(override):
     rows = np.concatenate([np.arange(mb * 128, mb * 128 + 128) for mb in (0, 18, 19, 25, 39)])
     ref = oracle.blockscale(x.A[rows], x.a_scale[rows], x.B, x.b_scale)
     compare(got[rows], ref, "stream-K after whole waves")
+
+
+def test_mxfp8_cuda_graph_replay():
+    """fp8mx_gemm (scale pack + GEMM, pooled workspace) captured in a CUDA graph
+    and replayed on new input contents."""
+    import torch
+    import fp8_block_scaled_e4m3_gb300 as f
+    M, N, K = 300, 520, 1280
+    x0, x1 = (workloads.make_mxfp8_inputs(M, N, K, seed=s) for s in (41, 42))
+    d = [to_dev(x0.A), to_dev(x0.a_e8m0), to_dev(x0.B), to_dev(x0.b_e8m0)]
+    for entry in (f.gemm_mxfp8,):
+        C = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+        entry(*d, C=C)                      # first call outside the capture (device set-up)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            entry(*d, C=C)
+        for x in (x1, x0):
+            for dst, src in zip(d, (x.A, x.a_e8m0, x.B, x.b_e8m0)):
+                dst.copy_(to_dev(src))
+            C.zero_()
+            g.replay()
+            assert f.get_status() == 0
+            got = C.view(torch.int16).cpu().numpy().view(np.uint16)
+            compare(got, oracle.mxfp8(x.A, x.a_e8m0, x.B, x.b_e8m0), f"graph replay {entry.__name__}")
+        del g
