@@ -150,8 +150,7 @@ bool decode_config_id(int id, Config &c)
     if (c.sched < 1 || c.sched > 2 || c.raster > 1 || (c.sched == 2 && (c.kind != 1 || c.block_n != 256)))
         return false;
     if (c.kind == 1)
-        return (c.block_n == 256 && c.stages == 4) || (c.block_n == 128 && c.stages == 6) ||
-               (c.block_n == 160 && c.stages == 5);
+        return (c.block_n == 256 && c.stages == 4) || (c.block_n == 128 && c.stages == 6);
     if (c.kind == 2)
         return (c.block_n == 256 && c.stages == 4) || (c.block_n == 128 && c.stages == 6);
     if (c.kind == 3)
@@ -282,7 +281,7 @@ int launch_mx(const Config &cfg, const void *A, const uint8_t *a_sf, const void 
     if (!encode_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, A, K, M, K, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
         !encode_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, B, K, N, K, 128, cfg.block_n, CU_TENSOR_MAP_SWIZZLE_128B) ||
         !encode_2d(&tmC, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, C, N, M, static_cast<uint64_t>(N) * 2, kCChunkCols, 32,
-                   CU_TENSOR_MAP_SWIZZLE_32B))
+                   CU_TENSOR_MAP_SWIZZLE_64B))
         return FP8BS_ERR_LAUNCH;
     GemmArgs args = {};
     args.M = M;
@@ -341,7 +340,7 @@ int fp8bs_gemm(const void *A, const float *a_scale, const void *B, const float *
         !encode_2d(&tmSA, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, a_scale, ld_sa, KB, ld_sa * 4, 128, 1,
                    CU_TENSOR_MAP_SWIZZLE_NONE) ||
         !encode_2d(&tmC, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, C, N, M, static_cast<uint64_t>(N) * 2, kCChunkCols, 32,
-                   CU_TENSOR_MAP_SWIZZLE_32B))
+                   CU_TENSOR_MAP_SWIZZLE_64B))
         return FP8BS_ERR_LAUNCH;
     GemmArgs args = {};
     args.M = M;
@@ -388,8 +387,6 @@ int fp8bs_gemm(const void *A, const float *a_scale, const void *B, const float *
         e = launch_blockscale_pair<kPairStages>(tmA, tmB, tmSA, tmC, args, st->pair_clusters, s);
     else if (cfg.block_n == 256)
         e = launch_blockscale<256, 4>(tmA, tmB, tmSA, tmC, args, grid, s);
-    else if (cfg.block_n == 160)
-        e = launch_blockscale<160, 5>(tmA, tmB, tmSA, tmC, args, grid, s);
     else
         e = launch_blockscale<128, 6>(tmA, tmB, tmSA, tmC, args, grid, s);
     if (ws && cudaFreeAsync(ws, s) != cudaSuccess && e == cudaSuccess)

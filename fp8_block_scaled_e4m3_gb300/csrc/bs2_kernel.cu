@@ -287,7 +287,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
             const int y0 = mb * 2 * kBlockM + static_cast<int>(rank) * kBlockM + q * 32;
 #pragma unroll
             for (int c = 0; c < HALF / kCChunkCols; ++c)
-                store_c_chunk(&tmC, cstage, lane, c, acc + c * kCChunkCols, x0 + c * kCChunkCols, y0, args.M,
+                store_c_chunk(&tmC, cstage, lane, acc + c * kCChunkCols, x0 + c * kCChunkCols, y0, args.M,
                               args.N);
         }
         if (lane == 0)

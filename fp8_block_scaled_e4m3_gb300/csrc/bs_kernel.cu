@@ -24,20 +24,20 @@
 //   warp 1      TMEM allocator + single-thread MMA issuer: four
 //               tcgen05.mma.kind::f8f6f4 (M128 x BN x K32) overwrite TMEM partial
 //               buffer (kb % NBUF) with P_kb, NBUF = 512 / BN buffers (2 for
-//               BN = 256, 3 for BN = 160, 4 for BN = 128), so the MMA can run
+//               BN = 256, 4 for BN = 128), so the MMA can run
 //               NBUF-1 K blocks ahead of the promote; tcgen05.commit releases the
 //               stage and signals the buffer.
 //   warps 2,3   idle (they complete warpgroup 0, which gives its registers away)
 //   warps 4..11 promote + epilogue: warp w reads TMEM lanes 32*(w%4).., column half
-//               (w-4)/4, so each thread owns one row of C and BN/2 columns (in at
-//               most two 128-column N blocks, i.e. two b_scale values). Per K
-//               block: acc += P_kb * (sa * sb) in fp32 registers. When the
-//               thread's whole slice fits in registers (BN <= 160) it is loaded,
-//               the TMEM buffer is released, and only then promoted, so the FMAs
-//               are off the MMA's critical path; for BN = 256 the buffer is
-//               released after the last 64-column round.
-//               After the last K block: bf16 convert, 64-byte-swizzled staging,
-//               TMA store (tails clipped by the tensor map).
+//               (w-4)/4, so each thread owns one row of C and BN/2 columns, all in
+//               one 128-column N block, i.e. one b_scale value. Per K block:
+//               acc += P_kb * (sa * sb) in fp32 registers. When the thread's
+//               whole slice fits in registers (BN = 128) it is loaded, the TMEM
+//               buffer is released, and only then promoted, so the FMAs are off
+//               the MMA's critical path; for BN = 256 the buffer is released
+//               after the last 64-column round.
+//               After the last K block: bf16 convert, 64-byte-swizzled staging
+//               of 32 x 32 chunks, TMA store (tails clipped by the tensor map).
 // Registers: the launch gives 168 per thread (3 warps per SM sub-partition);
 // warpgroup 0 drops to 40 and the two promote warpgroups rise to 232, so one
 // sub-partition holds 40 + 232 + 232 = 504 <= 512 registers per lane and the
@@ -72,7 +72,7 @@ struct BsLayout {
     static constexpr int DYN_SMEM = BYTES + 1024;   // slack to align the base to 1024
     static constexpr int TMEM_COLS = 512;
     static_assert(DYN_SMEM <= 232448, "shared memory budget");
-    static_assert(BN == 128 || BN == 160 || BN == 256, "tile width");
+    static_assert(BN == 128 || BN == 256, "tile width");
 };
 
 template <int BN, int STAGES>
@@ -201,12 +201,11 @@ __global__ void __launch_bounds__(kBsThreads, 1)
         ptx::setmaxnreg_inc<kBsRegsHigh<BN>>();
         // ------------------------------------------------- promote + epilogue
         constexpr int HALF = BN / 2;                 // columns per thread
-        constexpr int kChunk = 16;                   // columns per TMEM load / scale choice
+        constexpr int kChunk = 16;                   // columns per TMEM load (narrow tile)
         constexpr int NCH = HALF / kChunk;
-        constexpr bool kEarlyRelease = HALF <= 80;   // the slice fits next to the accumulator
-        constexpr bool kTwoBlocks = (BN % 128) != 0; // a slice may straddle two b_scale blocks
+        constexpr bool kEarlyRelease = HALF <= 64;   // the slice fits next to the accumulator
         constexpr bool kSk = BN == 256;              // tile width with the stream-K hand-off
-        static_assert(kCChunkCols == kChunk, "epilogue chunking");
+        static_assert(HALF % kCChunkCols == 0, "epilogue chunking");
         const int ew = warp - 4;                     // 0..7
         const int wg = ew >> 2;                      // column half
         const int q = warp & 3;                      // TMEM lane quadrant this warp may access
@@ -217,28 +216,22 @@ __global__ void __launch_bounds__(kBsThreads, 1)
         span.init(args, KB);
         const int total = span.total;
 
-        // b_scale of flattened step g for the (at most two) 128-column N blocks
-        // of this thread's columns. Lane l
-        // of the warp loads step 32*b + l of batch b; the value for step g is
-        // taken with a shuffle. Batch b+1 is requested when batch b starts, so
-        // its loads have 32 K blocks to land.
-        auto sb_lane_load = [&](int g, float &lo, float &hi) {
-            lo = 0.f;
-            hi = 0.f;
+        // b_scale of flattened step g for the 128-column N block of this thread's
+        // columns (a slice of 64 or 128 columns never straddles two). Lane l of
+        // the warp loads step 32*b + l of batch b; the value for step g is taken
+        // with a shuffle. Batch b+1 is requested when batch b starts, so its
+        // loads have 32 K blocks to land.
+        auto sb_lane_load = [&](int g) -> float {
             if (g >= total)
-                return;
+                return 0.f;
             int t, kb, mb, nb;
             span.step(g, t, kb);
             args.raster.coords(t, mb, nb);
             const int nblk = (nb * BN + wg * HALF) >> 7;
-            if (nblk < NB)
-                lo = ptx::ldg_nc_f32(args.b_scale + static_cast<size_t>(nblk) * KB + kb);
-            if (kTwoBlocks && nblk + 1 < NB)
-                hi = ptx::ldg_nc_f32(args.b_scale + static_cast<size_t>(nblk + 1) * KB + kb);
+            return nblk < NB ? ptx::ldg_nc_f32(args.b_scale + static_cast<size_t>(nblk) * KB + kb) : 0.f;
         };
-        float sb_cur_lo, sb_cur_hi, sb_next_lo, sb_next_hi;
-        sb_lane_load(lane, sb_cur_lo, sb_cur_hi);
-        sb_lane_load(32 + lane, sb_next_lo, sb_next_hi);
+        float sb_cur = sb_lane_load(lane);
+        float sb_next = sb_lane_load(32 + lane);
 
         float acc[HALF];
         int it = 0;
@@ -249,29 +242,19 @@ __global__ void __launch_bounds__(kBsThreads, 1)
             // tile and its coordinates are recomputed after it.
             const int seg_start = it;
             int seg_end;
-            uint32_t hi_mask = 0;
             {
-                int t, kb0, mb, nb;
+                int t, kb0;
                 span.step(it, t, kb0);
                 seg_end = it + ((KB - kb0) < (total - it) ? (KB - kb0) : (total - it));
-                args.raster.coords(t, mb, nb);
-                // chunks of 16 columns that lie in the second N block of the slice
-                const int col0 = nb * BN + wg * HALF;
-#pragma unroll
-            for (int c = 0; c < NCH; ++c)
-                    if (((col0 + kChunk * c) >> 7) != (col0 >> 7))
-                        hi_mask |= 1u << c;
             }
 #pragma unroll
             for (int j = 0; j < HALF; ++j)
                 acc[j] = 0.f;
             for (; it < seg_end; ++it) {
-                const float sb_lo = __shfl_sync(0xffffffffu, sb_cur_lo, it & 31);
-                const float sb_hi = __shfl_sync(0xffffffffu, sb_cur_hi, it & 31);
+                const float sb = __shfl_sync(0xffffffffu, sb_cur, it & 31);
                 if ((it & 31) == 31) {
-                    sb_cur_lo = sb_next_lo;
-                    sb_cur_hi = sb_next_hi;
-                    sb_lane_load(it + 33 + lane, sb_next_lo, sb_next_hi);
+                    sb_cur = sb_next;
+                    sb_next = sb_lane_load(it + 33 + lane);
                 }
                 const int a = it % kSaSlots;
                 const uint32_t aph = (it / kSaSlots) & 1;
@@ -284,8 +267,7 @@ __global__ void __launch_bounds__(kBsThreads, 1)
                 }
                 ptx::tc_fence_after();
                 const float sa = reinterpret_cast<const float *>(smem + L::OFF_SA + a * L::SA_BYTES)[row];
-                const float scale_lo = sa * sb_lo;
-                const float scale_hi = kTwoBlocks ? sa * sb_hi : scale_lo;
+                const float scale = sa * sb;
                 const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                                        static_cast<uint32_t>(buf * BN + wg * HALF);
                 if constexpr (kEarlyRelease) {
@@ -301,16 +283,12 @@ __global__ void __launch_bounds__(kBsThreads, 1)
                         ptx::mbar_arrive(sa_empty_bar(a));
                     }
 #pragma unroll
-                    for (int c = 0; c < NCH; ++c) {
-                        const float sc = ((hi_mask >> c) & 1u) ? scale_hi : scale_lo;
-#pragma unroll
-                        for (int j = 0; j < kChunk; ++j)
-                            acc[kChunk * c + j] = fmaf(__uint_as_float(part[kChunk * c + j]), sc, acc[kChunk * c + j]);
-                    }
+                    for (int j = 0; j < HALF; ++j)
+                        acc[j] = fmaf(__uint_as_float(part[j]), scale, acc[j]);
                 } else {
                     // One N block per slice (BN = 256): two 64-column rounds; the
                     // buffer is released as soon as the second round is loaded.
-                    static_assert(!kTwoBlocks && HALF == 128, "wide-tile promote");
+                    static_assert(HALF == 128, "wide-tile promote");
 #pragma unroll
                     for (int h = 0; h < 2; ++h) {
                         uint32_t r0[32], r1[32];
@@ -327,10 +305,10 @@ __global__ void __launch_bounds__(kBsThreads, 1)
                         }
 #pragma unroll
                         for (int j = 0; j < 32; ++j)
-                            acc[h * 64 + j] = fmaf(__uint_as_float(r0[j]), scale_lo, acc[h * 64 + j]);
+                            acc[h * 64 + j] = fmaf(__uint_as_float(r0[j]), scale, acc[h * 64 + j]);
 #pragma unroll
                         for (int j = 0; j < 32; ++j)
-                            acc[h * 64 + 32 + j] = fmaf(__uint_as_float(r1[j]), scale_lo, acc[h * 64 + 32 + j]);
+                            acc[h * 64 + 32 + j] = fmaf(__uint_as_float(r1[j]), scale, acc[h * 64 + 32 + j]);
                     }
                 }
             }
@@ -393,7 +371,7 @@ __global__ void __launch_bounds__(kBsThreads, 1)
             const int y0 = mb * kBlockM + q * 32;
 #pragma unroll
             for (int c = 0; c < HALF / kCChunkCols; ++c)
-                store_c_chunk(&tmC, cstage, lane, c, acc + c * kCChunkCols, x0 + c * kCChunkCols, y0, args.M, args.N);
+                store_c_chunk(&tmC, cstage, lane, acc + c * kCChunkCols, x0 + c * kCChunkCols, y0, args.M, args.N);
         }
         if (lane == 0)
             ptx::bulk_wait_all();
@@ -428,8 +406,6 @@ cudaError_t launch_blockscale(const CUtensorMap &tmA, const CUtensorMap &tmB, co
 template cudaError_t launch_blockscale<256, 4>(const CUtensorMap &, const CUtensorMap &, const CUtensorMap &,
                                                const CUtensorMap &, const GemmArgs &, int, cudaStream_t);
 template cudaError_t launch_blockscale<128, 6>(const CUtensorMap &, const CUtensorMap &, const CUtensorMap &,
-                                               const CUtensorMap &, const GemmArgs &, int, cudaStream_t);
-template cudaError_t launch_blockscale<160, 5>(const CUtensorMap &, const CUtensorMap &, const CUtensorMap &,
                                                const CUtensorMap &, const GemmArgs &, int, cudaStream_t);
 
 } // namespace fp8bs

@@ -217,7 +217,7 @@ __global__ void __launch_bounds__(kMxThreads, 1)
             const int y0 = mb * kBlockM + q * 32;
 #pragma unroll
             for (int c = 0; c < HALF / kCChunkCols; ++c)
-                store_c_chunk(&tmC, cstage, lane, c, v + c * kCChunkCols, x0 + c * kCChunkCols, y0, args.M, args.N);
+                store_c_chunk(&tmC, cstage, lane, v + c * kCChunkCols, x0 + c * kCChunkCols, y0, args.M, args.N);
         }
         if (lane == 0)
             ptx::bulk_wait_all();

@@ -112,6 +112,7 @@ def test_config_selection(lib):
     assert lib.select_config("bs", 4, 12, 128, 152) == -3
     L = lib.lib()
     assert L.fp8bs_set_config_override(1999911) == -3      # no such kernel
+    assert L.fp8bs_set_config_override(1160511) == -3      # the 160-wide tile was removed
     assert L.fp8bs_set_config_override(2256412) == -3      # stream-K is blockscale-only
     assert L.fp8bs_set_config_override(1256413) == -3      # no such schedule
     assert L.fp8bs_set_config_override(1128612) == -3      # stream-K runs with the 256-wide tile only
