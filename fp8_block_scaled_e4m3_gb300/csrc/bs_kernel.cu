@@ -16,18 +16,22 @@
 // in another order.
 //
 // Persistent, warp-specialised, one CTA per SM, 12 warps (3 warpgroups):
-//   warp 0      TMA producer: A tile [128 x 128] e4m3 and B tile [BN x 128] e4m3 of
-//               one K block into stage s of a STAGES-deep shared-memory ring
+//   warps 0, 3  TMA producers, warp 0 for the even K-block steps and warp 3 for
+//               the odd ones: A tile [128 x 128] e4m3 and B tile [BN x 128] e4m3
+//               of one K block into stage s of a STAGES-deep shared-memory ring
 //               (full/empty mbarriers, a stage is freed by the MMA commit), and
 //               the a_scale slice [128] fp32 of the K block into a separate
 //               kSaSlots-deep ring freed by the promote warps.
-//   warp 1      TMEM allocator + single-thread MMA issuer: four
+//   warps 1, 2  MMA issuers (one thread each, warp 1 even steps, warp 2 odd
+//               steps; warp 1 also allocates TMEM): four
 //               tcgen05.mma.kind::f8f6f4 (M128 x BN x K32) overwrite TMEM partial
 //               buffer (kb % NBUF) with P_kb, NBUF = 512 / BN buffers (2 for
-//               BN = 256, 4 for BN = 128), so the MMA can run
-//               NBUF-1 K blocks ahead of the promote; tcgen05.commit releases the
-//               stage and signals the buffer.
-//   warps 2,3   idle (they complete warpgroup 0, which gives its registers away)
+//               BN = 256, 4 for BN = 128), so the MMA can run NBUF-1 K blocks
+//               ahead of the promote; tcgen05.commit releases the stage and
+//               signals the buffer. Issuing an MMA while the tensor pipe is busy
+//               stalls the issuer's SM sub-partition, and the promote warps on it
+//               fall behind the others; splitting the issue (and the TMA issue)
+//               over two sub-partitions halves that lag.
 //   warps 4..11 promote + epilogue: warp w reads TMEM lanes 32*(w%4).., column half
 //               (w-4)/4, so each thread owns one row of C and BN/2 columns, all in
 //               one 128-column N block, i.e. one b_scale value. Per K block:
@@ -56,6 +60,7 @@ constexpr int kSaSlots = 16;   // a_scale ring depth (>= STAGES + NBUF, so it ne
 
 template <int BN, int STAGES>
 struct BsLayout {
+    static_assert(STAGES % 2 == 0, "two producers and two MMA issuers split the steps by parity");
     static constexpr int A_BYTES = kBlockM * kBlockK;
     static constexpr int B_BYTES = BN * kBlockK;
     static constexpr int SA_BYTES = kBlockM * 4;
@@ -65,6 +70,7 @@ struct BsLayout {
     static constexpr int OFF_C = (OFF_SA + kSaSlots * SA_BYTES + 1023) / 1024 * 1024;
     static constexpr int OFF_BAR = OFF_C + kEpiWarps * kCStageBytes;
     static constexpr int NBUF = 512 / BN;        // TMEM partial buffers
+    static_assert(NBUF % 2 == 0, "two MMA issuers split the buffers by parity");
     // full[S], empty[S], tfull[NBUF], tempty[NBUF], mma_done, sa_full[kSaSlots], sa_empty[kSaSlots]
     static constexpr int NBAR = 2 * STAGES + 2 * NBUF + 1 + 2 * kSaSlots;
     static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
@@ -114,7 +120,7 @@ __global__ void __launch_bounds__(kBsThreads, 1)
             ptx::mbar_init(tfull_bar(b), 1);
             ptx::mbar_init(tempty_bar(b), kEpiWarps);
         }
-        ptx::mbar_init(mma_done_bar, 1);
+        ptx::mbar_init(mma_done_bar, 2);                  // both MMA issuers
         *abort_flag = 0;
         ptx::fence_mbar_init();
     }
@@ -129,9 +135,14 @@ __global__ void __launch_bounds__(kBsThreads, 1)
 
     if (warp < 4) {
     ptx::setmaxnreg_dec<kBsRegsLow<BN>>();
-    if (warp == 0) {
-        // ------------------------------------------------------------ producer
+    if (warp == 0 || warp == 3) {
+        // ----------------------------------------------------------- producers
+        // Warp 0 fills the stages of the even steps, warp 3 those of the odd
+        // steps (STAGES and kSaSlots are even, so each stage and a_scale slot
+        // belongs to one of them and is waited on by that thread alone, in
+        // order of its phases).
         if (lane == 0) {
+            const int par = warp == 3 ? 1 : 0;
             ptx::prefetch_tmap(&tmA);
             ptx::prefetch_tmap(&tmB);
             ptx::prefetch_tmap(&tmSA);
@@ -143,6 +154,8 @@ __global__ void __launch_bounds__(kBsThreads, 1)
             for (; it < span.total; ++it, span.advance(it, t, kb)) {
                 if (it == 0 || kb == 0 || it == span.dp_steps)   // a new tile (a stream-K range may start mid-tile)
                     args.raster.coords(t, mb, nb);
+                if ((it & 1) != par)
+                    continue;
                 const int s = it % STAGES;
                 const uint32_t ph = (it / STAGES) & 1;
                 const int a = it % kSaSlots;
@@ -157,24 +170,32 @@ __global__ void __launch_bounds__(kBsThreads, 1)
                 ptx::tma_load_2d(sbase + L::OFF_SA + a * L::SA_BYTES, &tmSA, sa_full_bar(a), mb * kBlockM, kb);
             }
             // Every load issued must have landed before the CTA exits.
-            for (int s = 0; s < STAGES; ++s) {
+            for (int s = par; s < STAGES; s += 2) {
                 const int uses = it > s ? (it - s + STAGES - 1) / STAGES : 0;
                 if (uses > 0)
                     wait_teardown(full_bar(s), (uses - 1) & 1, args);
             }
-            for (int a = 0; a < kSaSlots; ++a) {
+            for (int a = par; a < kSaSlots; a += 2) {
                 const int uses = it > a ? (it - a + kSaSlots - 1) / kSaSlots : 0;
                 if (uses > 0)
                     wait_teardown(sa_full_bar(a), (uses - 1) & 1, args);
             }
         }
-    } else if (warp == 1) {
-        // --------------------------------------------------------- MMA issuer
+    } else {
+        // -------------------------------------------------------- MMA issuers
+        // Warp 1 issues the MMAs of the even steps, warp 2 those of the odd
+        // steps (NBUF is even, so each TMEM buffer, like each stage, has one
+        // issuer). Issuing tcgen05.mma stalls the issuing warp's SM
+        // sub-partition while the tensor pipe is busy, and the promote warps
+        // beside it fall behind; two issuers halve that per sub-partition.
+        // (Three would make two threads wait on one buffer's barrier for
+        // different phases, which a parity wait cannot tell apart.)
         if (lane == 0) {
+            const int par = warp - 1;
             constexpr uint32_t idesc = ptx::idesc_f8f6f4_e4m3(kBlockM, BN);
             WorkSpan span;
             span.init(args, KB);
-            for (int it = 0; it < span.total; ++it) {
+            for (int it = par; it < span.total; it += 2) {
                 const int s = it % STAGES;
                 const uint32_t ph = (it / STAGES) & 1;
                 const int buf = it % L::NBUF;
