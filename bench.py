@@ -56,6 +56,7 @@ def parse():
     p.add_argument("--cpu-seconds", type=float, default=12.0, help="target CPU time of the oracle sample")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-twin", action="store_true", help="skip the promote-free twin timing (blockscale)")
     p.add_argument("--warmup-seconds", type=float, default=1.0,
                    help="minimum warm-up duration (clock sampling); 0 for profiler runs")
     return p.parse_args()
@@ -333,6 +334,10 @@ def run_ours(args):
                 "hbm_time_frac": (algorithmic_bytes(kind, M, N, K) / (peaks["hbm_gbs"] * 1e9)) / (kernel_ms * 1e-3),
                 "kernel": KERNEL_NAMES[kind], "kernel_ms": kernel_ms}
 
+    twin = None
+    if kind == "bs" and not args.no_twin:
+        twin = measure_twin(args, torch, f, d, C, flush, stream, flops, kernel_ms, peaks)
+
     e2e = None
     if not args.no_e2e:
         e2e = measure_e2e(args, torch, f, kind, M, N, K, host, gemm)
@@ -352,7 +357,7 @@ def run_ours(args):
                        "parallelism": f"{world} independent replicas (weak scaling)",
                        "wall_s_timed_loop": wall, "warmup_steps_run": n_w, "ms_min": min(per_ms),
                        "ms_median": statistics.median(per_ms)},
-            "roofline": roofline,
+            "roofline": roofline, "ceiling_twin": twin,
             "gpu_launches": args.steps * (f.lib().fp8bs_launches_per_call() if kind == "bs"
                                           else f.lib().fp8mx_launches_per_call()),
             "clocks": clocks, "e2e": e2e, "cpu_baseline": cpu}
@@ -361,6 +366,31 @@ def run_ours(args):
     if pg:
         pg.destroy_process_group()
     return 0
+
+
+def measure_twin(args, torch, f, d, C, flush, stream, flops, kernel_ms, peaks):
+    """The same A and B through the promote-free twin (one fp32 scale for the whole
+    tensor, applied once in the epilogue), timed with the same protocol. The gap
+    between the two kernels is what the per-block scales cost on this shape."""
+    alpha = 0.03125
+    for _ in range(3):
+        f.gemm_tensorscale(d[0], d[2], alpha, C=C)
+    assert f.get_status() == 0
+    twin_cfg = f.last_config_id()
+    n = max(3, min(args.steps, 100))
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+    for i in range(n):
+        flush.fill_(1)
+        ev[i][0].record(stream)
+        f.gemm_tensorscale(d[0], d[2], alpha, C=C)
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    assert f.get_status() == 0
+    twin_ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+    tf = flops / (twin_ms * 1e-3) / 1e12
+    return {"kernel": "fp8bs_tensorscale_kernel", "config_id": twin_cfg, "steps": n, "kernel_ms": twin_ms,
+            "achieved": tf, "frac": tf / peaks["fp8_tflops"], "unit": "TFLOP/s",
+            "scale_tax": kernel_ms / twin_ms - 1.0}
 
 
 def measure_e2e(args, torch, f, kind, M, N, K, host, gemm):

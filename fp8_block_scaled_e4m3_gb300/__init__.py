@@ -28,6 +28,7 @@ _i64 = ctypes.c_int64
 
 _SIGS = {
     "fp8bs_gemm": (_i, [_p, _p, _p, _p, _p, _i, _i, _i, _p]),
+    "fp8bs_gemm_tensorscale": (_i, [_p, _p, _p, _i, _i, _i, ctypes.c_float, _p]),
     "fp8mx_gemm": (_i, [_p, _p, _p, _p, _p, _i, _i, _i, _p]),
     "fp8mx_gemm_packed": (_i, [_p, _p, _p, _p, _p, _i, _i, _i, _p]),
     "fp8mx_packed_scale_bytes": (_i64, [_i, _i]),
@@ -131,6 +132,22 @@ def gemm_blockscale(A, a_scale, B, b_scale, C=None, stream=None):
     return C
 
 
+def gemm_tensorscale(A, B, alpha, C=None, stream=None):
+    """C[M,N] bf16 = alpha * A.B^T: the promote-free ceiling twin of gemm_blockscale
+    (same tiles and MMA work, one per-tensor scale). A: [M,K] E4M3; B: [N,K] E4M3."""
+    torch = _torch()
+    M, K = A.shape
+    N = B.shape[0]
+    if C is None:
+        C = torch.empty((M, N), dtype=torch.bfloat16, device=A.device)
+    if C.dtype != torch.bfloat16:
+        raise TypeError("C must be bfloat16")
+    rc = _lib.fp8bs_gemm_tensorscale(_fp8_ptr(A, "A", (M, K)), _fp8_ptr(B, "B", (N, K)), _dev_ptr(C, "C", (M, N)),
+                                     M, N, K, float(alpha), _stream_ptr(stream))
+    _check(rc, "fp8bs_gemm_tensorscale")
+    return C
+
+
 def gemm_mxfp8(A, a_e8m0, B, b_e8m0, C=None, stream=None):
     """C[M,N] bf16 = sum_k A[m,k] 2^(a_e8m0[m,k/32]-127) B[n,k] 2^(b_e8m0[n,k/32]-127).
 
@@ -211,7 +228,7 @@ def select_config(kind: str, M: int, N: int, K: int, num_sms: int) -> int:
 
 
 def decode_config(cid: int) -> dict:
-    return {"kind": {1: "blockscale", 2: "mxfp8", 3: "blockscale_pair"}.get(cid // 1000000, "?"),
+    return {"kind": {1: "blockscale", 2: "mxfp8", 3: "blockscale_pair", 4: "tensorscale"}.get(cid // 1000000, "?"),
             "block_n": (cid // 1000) % 1000,
             "stages": (cid // 100) % 10, "raster": (cid // 10) % 10,
             "schedule": {1: "tile", 2: "stream_k"}.get(cid % 10, "?")}

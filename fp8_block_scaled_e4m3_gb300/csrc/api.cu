@@ -25,6 +25,9 @@ cudaError_t max_pair_clusters(int *);
 template <int BN, int STAGES>
 cudaError_t launch_mxfp8(const CUtensorMap &, const CUtensorMap &, const CUtensorMap &, const GemmArgs &, int,
                          cudaStream_t);
+template <int BN, int STAGES>
+cudaError_t launch_tensorscale(const CUtensorMap &, const CUtensorMap &, const CUtensorMap &, const GemmArgs &, int,
+                               cudaStream_t);
 
 namespace host {
 
@@ -128,7 +131,8 @@ int check_shape(int M, int N, int K)
 }
 
 // Kernel configuration. kind 1: one-CTA blockscale kernel, 2: MXFP8 kernel,
-// 3: CTA-pair blockscale kernel (256 x 128 tiles over two SMs).
+// 3: CTA-pair blockscale kernel (256 x 128 tiles over two SMs), 4: tensor-scale
+// twin (the MXFP8 kernel's pipeline with plain fp8 MMAs).
 // sched 1: one CTA per tile; 2: stream-K (blockscale one-CTA kernel only).
 struct Config {
     int kind, block_n, stages, raster, sched;
@@ -151,7 +155,7 @@ bool decode_config_id(int id, Config &c)
         return false;
     if (c.kind == 1)
         return (c.block_n == 256 && c.stages == 4) || (c.block_n == 128 && c.stages == 6);
-    if (c.kind == 2)
+    if (c.kind == 2 || c.kind == 4)
         return (c.block_n == 256 && c.stages == 4) || (c.block_n == 128 && c.stages == 6);
     if (c.kind == 3)
         return c.block_n == 128 && c.stages == kPairStages;
@@ -419,6 +423,53 @@ int fp8mx_gemm_packed(const void *A, const uint8_t *a_sf, const void *B, const u
     if ((rc = launch_mx(cfg, A, a_sf, B, b_sf, C, M, N, K, st->status_ptr, st->num_sms,
                         static_cast<cudaStream_t>(stream))))
         return rc;
+    t_last_config = config_id(cfg);
+    return FP8BS_OK;
+}
+
+int fp8bs_gemm_tensorscale(const void *A, const void *B, void *C, int M, int N, int K, float alpha, void *stream)
+{
+    int rc = check_shape(M, N, K);
+    if (rc)
+        return rc;
+    if (M == 0)
+        return FP8BS_OK;
+    if (!A || !B || !C)
+        return FP8BS_ERR_NULL;
+    if (!aligned(A, 16) || !aligned(B, 16) || !aligned(C, 16))
+        return FP8BS_ERR_ALIGN;
+    int dev;
+    DeviceState *st;
+    if ((rc = ensure_device(dev, st)))
+        return rc;
+    Config cfg = choose_config(4, M, N, K, st->num_sms);
+    if (!override_config(4, 4, cfg))
+        return FP8BS_ERR_SHAPE;
+    CUtensorMap tmA, tmB, tmC;
+    if (!encode_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, A, K, M, K, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, B, K, N, K, 128, cfg.block_n, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_2d(&tmC, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, C, N, M, static_cast<uint64_t>(N) * 2, kCChunkCols, 32,
+                   CU_TENSOR_MAP_SWIZZLE_64B))
+        return FP8BS_ERR_LAUNCH;
+    GemmArgs args = {};
+    args.M = M;
+    args.N = N;
+    args.K = K;
+    args.raster.m_tiles = (M + kBlockM - 1) / kBlockM;
+    args.raster.n_tiles = (N + cfg.block_n - 1) / cfg.block_n;
+    args.raster.raster = cfg.raster;
+    args.raster.group = 1;
+    args.alpha = alpha;
+    args.status = st->status_ptr;
+    args.wait_limit_ns = g_wait_limit_ns.load();
+    args.teardown_limit_ns = teardown_limit();
+    const int tiles = args.raster.num_tiles();
+    const int grid = tiles < st->num_sms ? tiles : st->num_sms;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const cudaError_t e = cfg.block_n == 256 ? launch_tensorscale<256, 4>(tmA, tmB, tmC, args, grid, s)
+                                             : launch_tensorscale<128, 6>(tmA, tmB, tmC, args, grid, s);
+    if (e != cudaSuccess)
+        return FP8BS_ERR_LAUNCH;
     t_last_config = config_id(cfg);
     return FP8BS_OK;
 }

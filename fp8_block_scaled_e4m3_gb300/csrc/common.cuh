@@ -54,6 +54,7 @@ struct GemmArgs {
     const float *b_scale;      // blockscale: [ceil(N/128)][K/128]
     const uint8_t *a_sf;       // mxfp8: packed scale atoms of A
     const uint8_t *b_sf;       // mxfp8: packed scale atoms of B
+    float alpha;               // tensor-scale twin: C = bf16(alpha * A.B^T)
     int *status;               // per-device status word
     unsigned long long wait_limit_ns;       // limit of every pipeline wait
     unsigned long long teardown_limit_ns;   // limit of the waits for work already in flight (>= 1 s)

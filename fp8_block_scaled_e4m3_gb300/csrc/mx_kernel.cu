@@ -17,6 +17,10 @@
 //   warps 2..9   epilogue: drain the fp32 accumulator (128 columns per thread),
 //                release it to the next tile's MMAs, bf16 convert, TMA store.
 //
+// The same body, compiled without the scale atoms and with plain fp8 MMAs, is
+// the blockscale GEMM's promote-free ceiling twin: identical tiles and MMA work,
+// one per-tensor scale applied in the epilogue (fp8bs_tensorscale_kernel).
+//
 // Packed scale layout (written by fp8mx_pack_scales from the quantiser's
 // row-major [rows][K/32] bytes, which are not TMA-addressable because a row of
 // K/32 bytes is not a 16-byte multiple in general): for 128-row block rb and
@@ -29,12 +33,12 @@ namespace fp8bs {
 
 constexpr int kMxThreads = (2 + kEpiWarps) * 32;
 
-template <int BN, int STAGES>
+template <int BN, int STAGES, bool MX = true>
 struct MxLayout {
     static constexpr int A_BYTES = kBlockM * kBlockK;
     static constexpr int B_BYTES = BN * kBlockK;
-    static constexpr int SFA_BYTES = 512;            // one atom: 128 rows x 4 groups
-    static constexpr int SFB_BYTES = 512 * (BN / 128);
+    static constexpr int SFA_BYTES = MX ? 512 : 0;   // one atom: 128 rows x 4 groups
+    static constexpr int SFB_BYTES = MX ? 512 * (BN / 128) : 0;
     static constexpr int SF_BYTES = SFA_BYTES + SFB_BYTES;
     static constexpr int OFF_A = 0;
     static constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
@@ -56,12 +60,14 @@ struct MxLayout {
     static_assert(BN == 128 || BN == 256, "tile width");
 };
 
-template <int BN, int STAGES>
-__global__ void __launch_bounds__(kMxThreads, 1)
-    fp8bs_mxfp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                       const __grid_constant__ CUtensorMap tmC, const GemmArgs args)
+// Body of both kernels below. MX: block-scaled MMAs with the ue8m0 scale atoms
+// staged per K step; !MX: plain fp8 MMAs and one per-tensor scale (args.alpha)
+// applied in the epilogue, i.e. the same MMA work with no per-block scaling.
+template <int BN, int STAGES, bool MX>
+__device__ __forceinline__ void mx_gemm_body(const CUtensorMap &tmA, const CUtensorMap &tmB, const CUtensorMap &tmC,
+                                             const GemmArgs &args)
 {
-    using L = MxLayout<BN, STAGES>;
+    using L = MxLayout<BN, STAGES, MX>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_s = ptx::smem_u32(smem_raw);
     const uint32_t sbase = (raw_s + 1023u) & ~1023u;
@@ -119,6 +125,11 @@ __global__ void __launch_bounds__(kMxThreads, 1)
                         break;
                     }
                     ptx::mbar_arrive_expect_tx(full_bar(s), L::A_BYTES + L::B_BYTES + L::SF_BYTES);
+                    if constexpr (!MX) {
+                        ptx::tma_load_2d(sbase + L::OFF_A + s * L::A_BYTES, &tmA, full_bar(s), ks * kBlockK, mb * kBlockM);
+                        ptx::tma_load_2d(sbase + L::OFF_B + s * L::B_BYTES, &tmB, full_bar(s), ks * kBlockK, nb * BN);
+                        continue;
+                    }
                     ptx::tma_load_2d(sbase + L::OFF_A + s * L::A_BYTES, &tmA, full_bar(s), ks * kBlockK, mb * kBlockM);
                     ptx::tma_load_2d(sbase + L::OFF_B + s * L::B_BYTES, &tmB, full_bar(s), ks * kBlockK, nb * BN);
                     // Scale atoms. A 128-row B block past N (the second half of a
@@ -159,6 +170,16 @@ __global__ void __launch_bounds__(kMxThreads, 1)
                         break;
                     }
                     ptx::tc_fence_after();
+                    if constexpr (!MX) {
+                        constexpr uint32_t idesc = ptx::idesc_f8f6f4_e4m3(kBlockM, BN);
+                        const uint64_t adesc = ptx::desc_kmajor_sw128(sbase + L::OFF_A + s * L::A_BYTES);
+                        const uint64_t bdesc = ptx::desc_kmajor_sw128(sbase + L::OFF_B + s * L::B_BYTES);
+#pragma unroll
+                        for (int kk = 0; kk < kBlockK / kMmaK; ++kk)
+                            ptx::mma_f8f6f4(tmem_base, adesc + 2 * kk, bdesc + 2 * kk, idesc, (ks | kk) != 0 ? 1u : 0u);
+                        ptx::tc_commit(empty_bar(s));
+                        continue;
+                    }
                     const uint32_t sf_smem = sbase + L::OFF_SF + s * L::SF_BYTES;
                     const uint32_t sfa_t = tmem_base + static_cast<uint32_t>(L::SF_COL0 + s * L::SF_COLS_PER_STAGE);
                     const uint32_t sfb_t = sfa_t + 4;
@@ -206,7 +227,7 @@ __global__ void __launch_bounds__(kMxThreads, 1)
                 ptx::tmem_ld_32x32b_x32(taddr + c * 32, r);
 #pragma unroll
                 for (int j = 0; j < 32; ++j)
-                    v[c * 32 + j] = __uint_as_float(r[j]);
+                    v[c * 32 + j] = MX ? __uint_as_float(r[j]) : __uint_as_float(r[j]) * args.alpha;
             }
             ptx::tmem_wait_ld();
             ptx::tc_fence_before();
@@ -232,11 +253,30 @@ __global__ void __launch_bounds__(kMxThreads, 1)
 }
 
 template <int BN, int STAGES>
-cudaError_t launch_mxfp8(const CUtensorMap &tmA, const CUtensorMap &tmB, const CUtensorMap &tmC,
-                         const GemmArgs &args, int grid, cudaStream_t stream)
+__global__ void __launch_bounds__(kMxThreads, 1)
+    fp8bs_mxfp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                       const __grid_constant__ CUtensorMap tmC, const GemmArgs args)
 {
-    using L = MxLayout<BN, STAGES>;
-    auto kern = fp8bs_mxfp8_kernel<BN, STAGES>;
+    mx_gemm_body<BN, STAGES, true>(tmA, tmB, tmC, args);
+}
+
+// Promote-free ceiling twin of the blockscale GEMM (skill card "FlyDSL fp8
+// blockscale GEMM", section "Bottleneck diagnosis": the same kernel with one
+// per-tensor scale, i.e. identical MMA work): C = bf16(alpha * A.B^T).
+template <int BN, int STAGES>
+__global__ void __launch_bounds__(kMxThreads, 1)
+    fp8bs_tensorscale_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                             const __grid_constant__ CUtensorMap tmC, const GemmArgs args)
+{
+    mx_gemm_body<BN, STAGES, false>(tmA, tmB, tmC, args);
+}
+
+template <int BN, int STAGES, bool MX>
+cudaError_t launch_mx_or_tensorscale(const CUtensorMap &tmA, const CUtensorMap &tmB, const CUtensorMap &tmC,
+                                     const GemmArgs &args, int grid, cudaStream_t stream)
+{
+    using L = MxLayout<BN, STAGES, MX>;
+    auto kern = MX ? fp8bs_mxfp8_kernel<BN, STAGES> : fp8bs_tensorscale_kernel<BN, STAGES>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::DYN_SMEM);
     if (e != cudaSuccess)
         return e;
@@ -248,9 +288,28 @@ cudaError_t launch_mxfp8(const CUtensorMap &tmA, const CUtensorMap &tmB, const C
     return cudaLaunchKernelEx(&cfg, kern, tmA, tmB, tmC, args);
 }
 
+template <int BN, int STAGES>
+cudaError_t launch_mxfp8(const CUtensorMap &tmA, const CUtensorMap &tmB, const CUtensorMap &tmC,
+                         const GemmArgs &args, int grid, cudaStream_t stream)
+{
+    return launch_mx_or_tensorscale<BN, STAGES, true>(tmA, tmB, tmC, args, grid, stream);
+}
+
+template <int BN, int STAGES>
+cudaError_t launch_tensorscale(const CUtensorMap &tmA, const CUtensorMap &tmB, const CUtensorMap &tmC,
+                               const GemmArgs &args, int grid, cudaStream_t stream)
+{
+    return launch_mx_or_tensorscale<BN, STAGES, false>(tmA, tmB, tmC, args, grid, stream);
+}
+
 template cudaError_t launch_mxfp8<256, 4>(const CUtensorMap &, const CUtensorMap &, const CUtensorMap &,
                                           const GemmArgs &, int, cudaStream_t);
 template cudaError_t launch_mxfp8<128, 6>(const CUtensorMap &, const CUtensorMap &, const CUtensorMap &,
                                           const GemmArgs &, int, cudaStream_t);
+
+template cudaError_t launch_tensorscale<256, 4>(const CUtensorMap &, const CUtensorMap &, const CUtensorMap &,
+                                                const GemmArgs &, int, cudaStream_t);
+template cudaError_t launch_tensorscale<128, 6>(const CUtensorMap &, const CUtensorMap &, const CUtensorMap &,
+                                                const GemmArgs &, int, cudaStream_t);
 
 } // namespace fp8bs

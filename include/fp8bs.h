@@ -109,6 +109,22 @@ int fp8mx_gemm(const void *A, const uint8_t *a_e8m0, const void *B, const uint8_
 int fp8mx_gemm_packed(const void *A, const uint8_t *a_sf, const void *B, const uint8_t *b_sf, void *C,
                       int M, int N, int K, void *stream);
 
+/*
+ * Promote-free ceiling twin of fp8bs_gemm (skill card "FlyDSL fp8 blockscale
+ * GEMM", section "Bottleneck diagnosis": the same kernel with one per-tensor
+ * scale, i.e. identical MMA work):
+ *
+ *   C[m,n] = bf16( alpha * sum_k A[m,k] * B[n,k] )
+ *
+ * A, B, C and the shape rules as fp8bs_gemm; alpha is one fp32 scale. The
+ * fp32 sums run over the whole K extent in tensor memory and alpha is applied
+ * once in the epilogue. Comparing its time with fp8bs_gemm's on the same shape
+ * measures the cost of the per-block software scaling. One kernel; config ids
+ * of kind 4 (same tiles as the MXFP8 kernel).
+ */
+int fp8bs_gemm_tensorscale(const void *A, const void *B, void *C, int M, int N, int K, float alpha,
+                           void *stream);
+
 /* Size in bytes of the packed scale layout of a [rows][K/32] ue8m0 tensor:
  * ceil(rows/128) * (K/128) * 512. Negative (FP8BS_ERR_SHAPE) for bad shapes. */
 int64_t fp8mx_packed_scale_bytes(int rows, int K);
@@ -182,8 +198,8 @@ const char *fp8bs_status_string(int status);
  * host thread launched (0 if none): kind*1000000 + block_n*1000 + stages*100 +
  * raster*10 + schedule; kind 1 = one-CTA blockscale kernel (128 x block_n
  * tiles), 2 = mxfp8 kernel, 3 = CTA-pair blockscale kernel (256 x block_n tiles
- * over two SMs); schedule 1 = one CTA per tile, 2 = stream-K (kind 1 with
- * block_n 256 only). */
+ * over two SMs), 4 = tensor-scale twin (fp8bs_gemm_tensorscale); schedule 1 =
+ * one CTA per tile, 2 = stream-K (kind 1 with block_n 256 only). */
 int fp8bs_last_config_id(void);
 /* Configuration id fp8bs_gemm / fp8mx_gemm would choose for a shape on a
  * device with `num_sms` SMs (host-only, no CUDA calls). */

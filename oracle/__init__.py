@@ -104,6 +104,18 @@ def blockscale(A, a_scale, B, b_scale, rows=None, exact=False):
     return _run("oracle_blockscale", A, sa, B, sb, M, N, K, rows, exact)
 
 
+def tensorscale(A, B, alpha, rows=None):
+    """C = bf16(alpha * A.B^T), the promote-free ceiling twin (skill card "FlyDSL fp8
+    blockscale GEMM", section "Bottleneck diagnosis"). It is exactly the blockscale
+    definition with every a_scale equal to alpha and every b_scale equal to 1, so it
+    is computed by that function (same fp64 sums, one bf16 rounding)."""
+    M, K = A.shape
+    N = B.shape[0]
+    sa = np.full((M, K // 128), np.float32(alpha), dtype=np.float32)
+    sb = np.ones(((N + 127) // 128, K // 128), dtype=np.float32)
+    return blockscale(A, sa, B, sb, rows=rows)
+
+
 def blockscale_blockpartial(A, a_scale, B, b_scale, rows=None, exact=False):
     M, K = A.shape
     N = B.shape[0]

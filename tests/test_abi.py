@@ -51,6 +51,25 @@ def test_shape_rules_rejected_before_launch(lib):
         assert f(P, P, P, P, None, 4, 8, 128, None) == -1
 
 
+def test_tensorscale_entry_checks_before_launch(lib):
+    L = lib.lib()
+    f = L.fp8bs_gemm_tensorscale
+    P = ctypes.c_void_p(1 << 20)
+    one = ctypes.c_float(1.0)
+    assert f(P, P, P, 4, 8, 100, one, None) == -3         # K % 128
+    assert f(P, P, P, 4, 12, 128, one, None) == -3        # N % 8
+    assert f(P, P, P, -1, 8, 128, one, None) == -3        # M < 0
+    assert f(None, None, None, 0, 8, 128, one, None) == 0  # M == 0 is a no-op
+    assert f(None, P, P, 4, 8, 128, one, None) == -1
+    assert f(ctypes.c_void_p((1 << 20) + 8), P, P, 4, 8, 128, one, None) == -2
+    assert f(P, P, ctypes.c_void_p((1 << 20) + 8), 4, 8, 128, one, None) == -2
+    for cid in (4256411, 4128611, 4256401, 4128601):
+        assert L.fp8bs_set_config_override(cid) == 0
+        assert lib.decode_config(cid)["kind"] == "tensorscale"
+    assert L.fp8bs_set_config_override(4256412) == -3     # no stream-K twin
+    assert L.fp8bs_set_config_override(0) == 0
+
+
 def test_alignment_rejected_before_launch(lib):
     L = lib.lib()
     a16 = ctypes.c_void_p(1 << 20)

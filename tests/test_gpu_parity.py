@@ -432,3 +432,36 @@ def test_mxfp8_cuda_graph_replay():
             got = C.view(torch.int16).cpu().numpy().view(np.uint16)
             compare(got, oracle.mxfp8(x.A, x.a_e8m0, x.B, x.b_e8m0), f"graph replay {entry.__name__}")
         del g
+
+
+# ------------------------------------------------ promote-free ceiling twin
+@pytest.mark.parametrize("cfg", [4256411, 4128611])
+@pytest.mark.parametrize("M,N,K", [(300, 520, 1280), (129, 136, 256), (1, 8, 128), (640, 768, 7168)])
+def test_tensorscale_every_config(override, cfg, M, N, K):
+    import torch
+    import fp8_block_scaled_e4m3_gb300 as f
+    raster = 1 if M >= N else 0
+    cid = cfg - (cfg // 10 % 10) * 10 + raster * 10
+    override(cid)
+    x = workloads.make_blockscale_inputs(M, N, K, seed=M + K)
+    alpha = 0.0371
+    out = f.gemm_tensorscale(to_dev(x.A), to_dev(x.B), alpha)
+    assert f.get_status() == 0
+    assert f.last_config_id() == cid
+    got = out.view(torch.int16).cpu().numpy().view(np.uint16)
+    compare(got, oracle.tensorscale(x.A, x.B, alpha), f"tensorscale {cid} {M}x{N}x{K}")
+
+
+def test_tensorscale_integer_exact():
+    """Small integer codes and a power-of-two alpha: every fp32 sum is exact, so the
+    twin must equal the oracle bit for bit."""
+    import torch
+    import fp8_block_scaled_e4m3_gb300 as f
+    rng = np.random.Generator(np.random.PCG64(9))
+    M, N, K = 384, 640, 1024
+    A = _int_codes(rng.integers(-2, 3, size=(M, K)))
+    B = _int_codes(rng.integers(-2, 3, size=(N, K)))
+    out = f.gemm_tensorscale(to_dev(A), to_dev(B), 0.25)
+    assert f.get_status() == 0
+    got = out.view(torch.int16).cpu().numpy().view(np.uint16)
+    assert np.array_equal(got, oracle.tensorscale(A, B, 0.25))

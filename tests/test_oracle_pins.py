@@ -307,3 +307,23 @@ def test_row_range_matches_full():
     full = oracle.blockscale(x.A, x.a_scale, x.B, x.b_scale)
     part = oracle.blockscale(x.A, x.a_scale, x.B, x.b_scale, rows=(10, 37))
     assert np.array_equal(part, full[10:37])
+
+
+def test_tensorscale_oracle_is_the_exact_gemm_times_alpha():
+    """The twin's oracle against exact rational arithmetic: with alpha = 1 every
+    output is the correctly rounded bf16 of the exact sum of code products, and a
+    power-of-two alpha scales every output exactly."""
+    rng = np.random.Generator(np.random.PCG64(12))
+    M, N, K = 5, 7, 256
+    A = rng.integers(0, 256, size=(M, K), dtype=np.uint8)
+    B = rng.integers(0, 256, size=(N, K), dtype=np.uint8)
+    A[(A & 0x7F) == 0x7F] = 0     # no NaN codes
+    B[(B & 0x7F) == 0x7F] = 0
+    fa = [[oracle.e4m3_fraction(int(c)) for c in row] for row in A]
+    fb = [[oracle.e4m3_fraction(int(c)) for c in row] for row in B]
+    want = np.array([[oracle.fraction_to_bf16_bits(sum(x * y for x, y in zip(fa[m], fb[n])))
+                      for n in range(N)] for m in range(M)], dtype=np.uint16)
+    one = oracle.tensorscale(A, B, 1.0)
+    assert np.array_equal(one, want)
+    four = oracle.tensorscale(A, B, 4.0)
+    assert np.array_equal(oracle.bf16_bits_to_float(four), 4.0 * oracle.bf16_bits_to_float(one))
