@@ -443,8 +443,8 @@ def test_tensorscale_every_config(override, cfg, M, N, K):
     raster = 1 if M >= N else 0
     cid = cfg - (cfg // 10 % 10) * 10 + raster * 10
     override(cid)
-    x = workloads.make_blockscale_inputs(M, N, K, seed=M + K)
-    alpha = 0.0371
+    x = workloads.make_tensorscale_inputs(M, N, K, seed=M + K)
+    alpha = float(x.alpha)
     out = f.gemm_tensorscale(to_dev(x.A), to_dev(x.B), alpha)
     assert f.get_status() == 0
     assert f.last_config_id() == cid

@@ -52,6 +52,18 @@ def test_mx_quantiser_recipe():
     assert np.all((x.a_e8m0 > 100) & (x.a_e8m0 < 140))
 
 
+def test_tensorscale_quantiser_recipe():
+    x = w.make_tensorscale_inputs(70, 40, 256, seed=5)
+    # one scale per tensor: the largest |value| of each tensor maps to the code 448
+    assert (x.A & 0x7F).max() >= 0x7D and (x.B & 0x7F).max() >= 0x7D
+    assert np.all(x.A & 0x7F != 0x7F) and np.all(x.B & 0x7F != 0x7F)
+    rng = np.random.Generator(np.random.PCG64(5))
+    a = rng.standard_normal((70, 256), dtype=np.float32)
+    b = rng.standard_normal((40, 256), dtype=np.float32) * np.float32(0.02)
+    sa, sb = np.abs(a).max() / np.float32(448), np.abs(b).max() / np.float32(448)
+    assert x.alpha == np.float32(np.float32(sa) * np.float32(sb))
+
+
 def test_generators_are_deterministic():
     a = w.make_blockscale_inputs(64, 128, 256, seed=3)
     b = w.make_blockscale_inputs(64, 128, 256, seed=3)

@@ -129,6 +129,12 @@ def quantise_mxfp8(x: np.ndarray):
     return codes, e
 
 
+def quantise_tensorscale(x: np.ndarray):
+    """X fp32 -> (codes uint8, one fp32 scale amax/448 for the whole tensor)."""
+    scale = fp32_block_scale(np.array(np.abs(x).max(), dtype=np.float32))
+    return _quantise_with_scale(x, scale), np.float32(scale)
+
+
 @dataclass
 class BlockscaleInputs:
     M: int
@@ -173,6 +179,28 @@ def make_blockscale_inputs(M: int, N: int, K: int, seed: int = 0, b_std: float =
     del a
     B, sb = quantise_blockscale_b(b)
     return BlockscaleInputs(M, N, K, seed, A, sa, B, sb)
+
+
+@dataclass
+class TensorscaleInputs:
+    M: int
+    N: int
+    K: int
+    seed: int
+    A: np.ndarray        # uint8 [M,K]
+    B: np.ndarray        # uint8 [N,K]
+    alpha: np.float32    # fp32(scale_A * scale_B)
+
+
+def make_tensorscale_inputs(M: int, N: int, K: int, seed: int = 0, b_std: float = 0.02) -> TensorscaleInputs:
+    """The blockscale recipe's distributions, quantised with one scale per tensor."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    a = rng.standard_normal((M, K), dtype=np.float32)
+    b = rng.standard_normal((N, K), dtype=np.float32) * np.float32(b_std)
+    A, sa = quantise_tensorscale(a)
+    del a
+    B, sb = quantise_tensorscale(b)
+    return TensorscaleInputs(M, N, K, seed, A, B, np.float32(sa * sb))
 
 
 def make_mxfp8_inputs(M: int, N: int, K: int, seed: int = 0) -> MxInputs:
