@@ -151,7 +151,7 @@ bool decode_config_id(int id, Config &c)
     c.stages = (id / 100) % 10;
     c.raster = (id / 10) % 10;
     c.sched = id % 10;
-    if (c.sched < 1 || c.sched > 2 || c.raster > 1 || (c.sched == 2 && (c.kind != 1 || c.block_n != 256)))
+    if (c.sched < 1 || c.sched > 2 || c.raster > 1 || (c.sched == 2 && (c.kind == 3 || c.block_n != 256)))
         return false;
     if (c.kind == 1)
         return (c.block_n == 256 && c.stages == 4) || (c.block_n == 128 && c.stages == 6);
@@ -173,6 +173,38 @@ long long sk_grid(long long units, long long KB, int num_sms)
     return g < 1 ? 1 : g;
 }
 
+// Smallest saving of K steps in the longest CTA for which stream-K is chosen:
+// a blockscale K block costs ~1000 clocks and the hand-off a few thousand; an
+// MXFP8 K step costs ~700 clocks.
+constexpr long long kSkMinGainBs = 8;
+constexpr long long kSkMinGainMx = 4;
+
+// Stream-K set-up shared by the one-CTA kernels with a 256-wide tile: the grid,
+// the whole waves run one CTA per tile before the stream-K range (the CTAs of a
+// wave share A and B panels in L2), and the workspace from the stream-ordered
+// pool: one fp32 partial tile and kEpiWarps flags per CTA. Fresh or reused
+// memory never holds this call's token, and finishers reset the flags they
+// consume. The caller frees `ws` on the stream after the launch.
+int setup_stream_k(int tiles, int KB, int num_sms, cudaMemPool_t pool, cudaStream_t s, GemmArgs &args, int &grid,
+                   void *&ws)
+{
+    const long long units = static_cast<long long>(tiles) * KB;
+    if (units >= (1ll << 31) || !pool)
+        return FP8BS_ERR_SHAPE;
+    grid = static_cast<int>(sk_grid(units, KB, num_sms));
+    const int full_waves = tiles / grid;
+    args.sk_dp = full_waves >= 2 ? full_waves - 1 : 0;
+    const size_t slot = static_cast<size_t>(kBlockM) * 256 * sizeof(float);
+    const size_t bytes = static_cast<size_t>(grid) * (slot + kEpiWarps * sizeof(unsigned long long));
+    if (cudaMallocFromPoolAsync(&ws, bytes, pool, s) != cudaSuccess)
+        return FP8BS_ERR_CUDA;
+    args.sk = 1;
+    args.sk_partial = static_cast<float *>(ws);
+    args.sk_flags = reinterpret_cast<unsigned long long *>(static_cast<char *>(ws) + grid * slot);
+    args.sk_token = g_sk_token.fetch_add(1) + 1;
+    return FP8BS_OK;
+}
+
 // Shape class -> configuration, from (M, N, K) only.
 Config choose_config(int kind, int M, int N, int K, int num_sms)
 {
@@ -189,17 +221,19 @@ Config choose_config(int kind, int M, int N, int K, int num_sms)
     c.block_n = 256;
     c.stages = 4;
     const long long tiles256 = (long long)((M + 127) / 128) * ((N + 255) / 256);
-    // Blockscale: stream-K (256-wide tile) when it shortens the longest CTA's K
-    // loop by at least 8 K blocks (about 4 us at ~1000 clocks per block), which
-    // pays for the partial hand-off. E.g. 256 tiles x 56 K blocks on 152 SMs:
-    // 112 -> 95; 8 tiles x 56: 56 -> 3.
+    // Stream-K (256-wide tile) when it shortens the longest CTA's K loop by at
+    // least kSkMinGain K steps, which pays for the partial hand-off. E.g.
+    // blockscale 256 tiles x 56 K blocks on 152 SMs: 112 -> 95; 8 tiles x 56:
+    // 56 -> 3. The tensor-scale twin follows the blockscale rule, so that the two
+    // run the same tiles.
     const long long KB = K / 128;
     const long long units = tiles256 * KB;
-    if (kind == 1 && tiles256 > 0 && units < (1ll << 31) && num_sms > 0) {
+    const long long min_gain = kind == 2 ? kSkMinGainMx : kSkMinGainBs;
+    if (tiles256 > 0 && units < (1ll << 31) && num_sms > 0) {
         const long long g = sk_grid(units, KB, num_sms);
         const long long per_tile = (tiles256 + num_sms - 1) / num_sms * KB;   // one CTA per tile
         const long long per_unit = (units + g - 1) / g;                       // stream-K
-        if (per_tile - per_unit >= 8) {
+        if (per_tile - per_unit >= min_gain) {
             c.sched = 2;
             return c;
         }
@@ -277,9 +311,10 @@ __global__ void pack_a_scale_kernel(const float *__restrict__ src, float *__rest
 }
 
 // Tensor maps, arguments and launch of the MXFP8 kernel on packed scales
-// (persistent grid of min(tiles, SMs) CTAs).
+// (cfg.kind 2) or of the tensor-scale twin (cfg.kind 4, no scale atoms, one
+// alpha): a persistent grid of min(tiles, SMs) CTAs, or the stream-K grid.
 int launch_mx(const Config &cfg, const void *A, const uint8_t *a_sf, const void *B, const uint8_t *b_sf, void *C,
-              int M, int N, int K, int *status_ptr, int num_sms, cudaStream_t s)
+              int M, int N, int K, float alpha, int *status_ptr, int num_sms, cudaMemPool_t pool, cudaStream_t s)
 {
     CUtensorMap tmA, tmB, tmC;
     if (!encode_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, A, K, M, K, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
@@ -297,13 +332,29 @@ int launch_mx(const Config &cfg, const void *A, const uint8_t *a_sf, const void 
     args.raster.group = 1;
     args.a_sf = a_sf;
     args.b_sf = b_sf;
+    args.alpha = alpha;
     args.status = status_ptr;
     args.wait_limit_ns = g_wait_limit_ns.load();
     args.teardown_limit_ns = teardown_limit();
     const int tiles = args.raster.num_tiles();
-    const int grid = tiles < num_sms ? tiles : num_sms;
-    const cudaError_t e = cfg.block_n == 256 ? launch_mxfp8<256, 4>(tmA, tmB, tmC, args, grid, s)
-                                             : launch_mxfp8<128, 6>(tmA, tmB, tmC, args, grid, s);
+    int grid = tiles < num_sms ? tiles : num_sms;
+    void *ws = nullptr;
+    if (cfg.sched == 2) {
+        if (cfg.block_n != 256)
+            return FP8BS_ERR_SHAPE;
+        const int rc = setup_stream_k(tiles, K / 128, num_sms, pool, s, args, grid, ws);
+        if (rc)
+            return rc;
+    }
+    cudaError_t e;
+    if (cfg.kind == 4)
+        e = cfg.block_n == 256 ? launch_tensorscale<256, 4>(tmA, tmB, tmC, args, grid, s)
+                               : launch_tensorscale<128, 6>(tmA, tmB, tmC, args, grid, s);
+    else
+        e = cfg.block_n == 256 ? launch_mxfp8<256, 4>(tmA, tmB, tmC, args, grid, s)
+                               : launch_mxfp8<128, 6>(tmA, tmB, tmC, args, grid, s);
+    if (ws && cudaFreeAsync(ws, s) != cudaSuccess && e == cudaSuccess)
+        e = cudaErrorUnknown;
     return e == cudaSuccess ? FP8BS_OK : FP8BS_ERR_LAUNCH;
 }
 
@@ -363,28 +414,11 @@ int fp8bs_gemm(const void *A, const float *a_scale, const void *B, const float *
     int grid = tiles < st->num_sms ? tiles : st->num_sms;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     void *ws = nullptr;
-    if (cfg.sched == 2 && !pair && cfg.block_n == 256) {
-        // Stream-K workspace from the stream-ordered pool: one fp32 partial tile
-        // and kEpiWarps flags per CTA. Fresh or reused memory never holds this
-        // call's token, and finishers reset the flags they consume.
-        const long long units = static_cast<long long>(tiles) * KB;
-        if (units >= (1ll << 31))
+    if (cfg.sched == 2) {
+        if (pair || cfg.block_n != 256)
             return FP8BS_ERR_SHAPE;
-        grid = static_cast<int>(sk_grid(units, KB, st->num_sms));
-        // Whole waves but the last one or two run one CTA per tile (the CTAs of
-        // a wave share A and B panels in L2); stream-K covers the rest.
-        const int full_waves = tiles / grid;
-        args.sk_dp = full_waves >= 2 ? full_waves - 1 : 0;
-        const size_t slot = static_cast<size_t>(kBlockM) * cfg.block_n * sizeof(float);
-        const size_t bytes = static_cast<size_t>(grid) * (slot + kEpiWarps * sizeof(unsigned long long));
-        if (cudaMallocFromPoolAsync(&ws, bytes, st->pool, s) != cudaSuccess)
-            return FP8BS_ERR_CUDA;
-        args.sk = 1;
-        args.sk_partial = static_cast<float *>(ws);
-        args.sk_flags = reinterpret_cast<unsigned long long *>(static_cast<char *>(ws) + grid * slot);
-        args.sk_token = g_sk_token.fetch_add(1) + 1;
-    } else if (cfg.sched == 2) {
-        return FP8BS_ERR_SHAPE;
+        if ((rc = setup_stream_k(tiles, KB, st->num_sms, st->pool, s, args, grid, ws)))
+            return rc;
     }
     cudaError_t e;
     if (pair)
@@ -420,7 +454,7 @@ int fp8mx_gemm_packed(const void *A, const uint8_t *a_sf, const void *B, const u
     Config cfg = choose_config(2, M, N, K, st->num_sms);
     if (!override_config(2, 2, cfg))
         return FP8BS_ERR_SHAPE;
-    if ((rc = launch_mx(cfg, A, a_sf, B, b_sf, C, M, N, K, st->status_ptr, st->num_sms,
+    if ((rc = launch_mx(cfg, A, a_sf, B, b_sf, C, M, N, K, 1.f, st->status_ptr, st->num_sms, st->pool,
                         static_cast<cudaStream_t>(stream))))
         return rc;
     t_last_config = config_id(cfg);
@@ -445,31 +479,9 @@ int fp8bs_gemm_tensorscale(const void *A, const void *B, void *C, int M, int N, 
     Config cfg = choose_config(4, M, N, K, st->num_sms);
     if (!override_config(4, 4, cfg))
         return FP8BS_ERR_SHAPE;
-    CUtensorMap tmA, tmB, tmC;
-    if (!encode_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, A, K, M, K, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !encode_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, B, K, N, K, 128, cfg.block_n, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !encode_2d(&tmC, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, C, N, M, static_cast<uint64_t>(N) * 2, kCChunkCols, 32,
-                   CU_TENSOR_MAP_SWIZZLE_64B))
-        return FP8BS_ERR_LAUNCH;
-    GemmArgs args = {};
-    args.M = M;
-    args.N = N;
-    args.K = K;
-    args.raster.m_tiles = (M + kBlockM - 1) / kBlockM;
-    args.raster.n_tiles = (N + cfg.block_n - 1) / cfg.block_n;
-    args.raster.raster = cfg.raster;
-    args.raster.group = 1;
-    args.alpha = alpha;
-    args.status = st->status_ptr;
-    args.wait_limit_ns = g_wait_limit_ns.load();
-    args.teardown_limit_ns = teardown_limit();
-    const int tiles = args.raster.num_tiles();
-    const int grid = tiles < st->num_sms ? tiles : st->num_sms;
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-    const cudaError_t e = cfg.block_n == 256 ? launch_tensorscale<256, 4>(tmA, tmB, tmC, args, grid, s)
-                                             : launch_tensorscale<128, 6>(tmA, tmB, tmC, args, grid, s);
-    if (e != cudaSuccess)
-        return FP8BS_ERR_LAUNCH;
+    if ((rc = launch_mx(cfg, A, nullptr, B, nullptr, C, M, N, K, alpha, st->status_ptr, st->num_sms, st->pool,
+                        static_cast<cudaStream_t>(stream))))
+        return rc;
     t_last_config = config_id(cfg);
     return FP8BS_OK;
 }
@@ -739,16 +751,17 @@ int fp8mx_gemm_noalloc(const void *A, const uint8_t *a_e8m0, const void *B, cons
     NoAllocDevice *nd;
     if ((rc = noalloc_setup(dev, nd)))
         return rc;
+    Config cfg = choose_config(2, M, N, K, nd->num_sms);
+    if (!override_config(2, 2, cfg))
+        return FP8BS_ERR_SHAPE;
+    cfg.sched = 1;   // stream-K needs a workspace: one CTA per tile here
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     uint8_t *a_sf = nd->scratch;             // every byte used is rewritten by the pack kernel
     uint8_t *b_sf = nd->scratch + a_bytes;   // a_bytes is a multiple of 512
     rc = launch_pack_scales(a_e8m0, a_sf, M, b_e8m0, b_sf, N, K, nd->num_sms, s);
     if (rc)
         return rc;
-    Config cfg = choose_config(2, M, N, K, nd->num_sms);
-    if (!override_config(2, 2, cfg))
-        return FP8BS_ERR_SHAPE;
-    if ((rc = launch_mx(cfg, A, a_sf, B, b_sf, C, M, N, K, nd->status_ptr, nd->num_sms, s)))
+    if ((rc = launch_mx(cfg, A, a_sf, B, b_sf, C, M, N, K, 1.f, nd->status_ptr, nd->num_sms, nullptr, s)))
         return rc;
     t_last_config = config_id(cfg);
     return FP8BS_OK;

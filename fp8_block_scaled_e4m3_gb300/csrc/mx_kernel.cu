@@ -7,15 +7,22 @@
 // (scale_vec::1X: one scale byte per row per 32-wide K slice) accumulates over
 // the whole K extent in tensor memory.
 //
-// Persistent, warp-specialised, one CTA per SM, 10 warps:
+// Persistent, warp-specialised, one CTA per SM, 12 warps:
 //   warp 0       TMA producer: A [128 x 128] and B [BN x 128] e4m3 per 128-wide K
 //                step, plus the step's scale-factor atoms (512 bytes per 128 rows)
 //                from the packed scale layout, all on one mbarrier.
 //   warp 1       TMEM allocator + single-thread issuer: tcgen05.cp of the atoms
 //                into TMEM (32x128b.warpx4), then four block-scaled MMAs (scale
 //                byte id = the 32-wide slice inside the step).
-//   warps 2..9   epilogue: drain the fp32 accumulator (128 columns per thread),
-//                release it to the next tile's MMAs, bf16 convert, TMA store.
+//   warps 2, 3   idle (they complete the control warpgroup of the register split).
+//   warps 4..11  epilogue: drain the fp32 accumulator (BN/2 columns per thread),
+//                release it to the next accumulation, bf16 convert, TMA store.
+//
+// Work schedule (WorkSpan in common.cuh), as in the blockscale kernel: one CTA
+// per tile, or stream-K for shapes whose last wave of tiles is partial. A tile
+// cut between CTAs is accumulated in pieces; the CTAs holding its later K steps
+// publish their fp32 partial sums, and the CTA holding K step 0 adds them
+// before it stores the tile.
 //
 // The same body, compiled without the scale atoms and with plain fp8 MMAs, is
 // the blockscale GEMM's promote-free ceiling twin: identical tiles and MMA work,
@@ -31,7 +38,14 @@
 
 namespace fp8bs {
 
-constexpr int kMxThreads = (2 + kEpiWarps) * 32;
+constexpr int kMxThreads = (4 + kEpiWarps) * 32;
+// Register split (setmaxnreg) out of the launch allotment of 384 threads x 168:
+// the control warpgroup drops to kMxRegsLow, the two epilogue warpgroups rise
+// to kMxRegsHigh (128 * 64 + 256 * 216 <= 384 * 168). The epilogue holds a
+// thread's 128 accumulator columns in registers through the stream-K hand-off.
+constexpr int kMxRegsLow = 64;
+constexpr int kMxRegsHigh = 216;
+static_assert(128 * kMxRegsLow + 256 * kMxRegsHigh <= kMxThreads * 168, "register split");
 
 template <int BN, int STAGES, bool MX = true>
 struct MxLayout {
@@ -106,32 +120,30 @@ __device__ __forceinline__ void mx_gemm_body(const CUtensorMap &tmA, const CUten
     ptx::tc_fence_after();
     const uint32_t tmem_base = *tmem_holder;
 
+    if (warp < 4) {
+    ptx::setmaxnreg_dec<kMxRegsLow>();
     if (warp == 0) {
         // ------------------------------------------------------------ producer
         if (lane == 0) {
             ptx::prefetch_tmap(&tmA);
             ptx::prefetch_tmap(&tmB);
             const int n_blocks = (args.N + 127) / 128;   // packed atoms per K step of B
+            WorkSpan span;
+            span.init(args, KS);
             int it = 0;
-            bool ok = true;
-            for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
-                int mb, nb;
-                args.raster.coords(t, mb, nb);
-                for (int ks = 0; ks < KS; ++ks, ++it) {
-                    const int s = it % STAGES;
-                    const uint32_t ph = (it / STAGES) & 1;
-                    if (!wait_bounded(empty_bar(s), ph ^ 1, abort_flag, args)) {
-                        ok = false;
-                        break;
-                    }
-                    ptx::mbar_arrive_expect_tx(full_bar(s), L::A_BYTES + L::B_BYTES + L::SF_BYTES);
-                    if constexpr (!MX) {
-                        ptx::tma_load_2d(sbase + L::OFF_A + s * L::A_BYTES, &tmA, full_bar(s), ks * kBlockK, mb * kBlockM);
-                        ptx::tma_load_2d(sbase + L::OFF_B + s * L::B_BYTES, &tmB, full_bar(s), ks * kBlockK, nb * BN);
-                        continue;
-                    }
-                    ptx::tma_load_2d(sbase + L::OFF_A + s * L::A_BYTES, &tmA, full_bar(s), ks * kBlockK, mb * kBlockM);
-                    ptx::tma_load_2d(sbase + L::OFF_B + s * L::B_BYTES, &tmB, full_bar(s), ks * kBlockK, nb * BN);
+            int t, ks, mb = 0, nb = 0;
+            span.step(0, t, ks);
+            for (; it < span.total; ++it, span.advance(it, t, ks)) {
+                if (it == 0 || ks == 0 || it == span.dp_steps)   // a new tile (a stream-K range may start mid-tile)
+                    args.raster.coords(t, mb, nb);
+                const int s = it % STAGES;
+                const uint32_t ph = (it / STAGES) & 1;
+                if (!wait_bounded(empty_bar(s), ph ^ 1, abort_flag, args))
+                    break;
+                ptx::mbar_arrive_expect_tx(full_bar(s), L::A_BYTES + L::B_BYTES + L::SF_BYTES);
+                ptx::tma_load_2d(sbase + L::OFF_A + s * L::A_BYTES, &tmA, full_bar(s), ks * kBlockK, mb * kBlockM);
+                ptx::tma_load_2d(sbase + L::OFF_B + s * L::B_BYTES, &tmB, full_bar(s), ks * kBlockK, nb * BN);
+                if constexpr (MX) {
                     // Scale atoms. A 128-row B block past N (the second half of a
                     // 256-wide tile when N has an odd number of 128-row blocks) reads
                     // the last real atom instead: those B rows are zero-filled by the
@@ -154,15 +166,21 @@ __device__ __forceinline__ void mx_gemm_body(const CUtensorMap &tmA, const CUten
         }
     } else if (warp == 1) {
         // ------------------------------------------------------ MMA issuer
+        // One accumulation per segment: the K steps of one tile in this CTA's
+        // range (a whole tile, or a piece of a tile cut by stream-K).
         if (lane == 0) {
-            int it = 0;
+            WorkSpan span;
+            span.init(args, KS);
             bool ok = true;
-            int titer = 0;
-            for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x, ++titer) {
-                if (!wait_bounded(acc_empty_bar, (titer & 1) ^ 1, abort_flag, args))
+            for (int it = 0, sg = 0; it < span.total && ok; ++sg) {
+                int t, ks0;
+                span.step(it, t, ks0);
+                const int seg_end = it + ((KS - ks0) < (span.total - it) ? (KS - ks0) : (span.total - it));
+                if (!wait_bounded(acc_empty_bar, (sg & 1) ^ 1, abort_flag, args))
                     break;
                 ptx::tc_fence_after();
-                for (int ks = 0; ks < KS; ++ks, ++it) {
+                const int seg_start = it;
+                for (; it < seg_end; ++it) {
                     const int s = it % STAGES;
                     const uint32_t ph = (it / STAGES) & 1;
                     if (!wait_bounded(full_bar(s), ph, abort_flag, args)) {
@@ -176,7 +194,8 @@ __device__ __forceinline__ void mx_gemm_body(const CUtensorMap &tmA, const CUten
                         const uint64_t bdesc = ptx::desc_kmajor_sw128(sbase + L::OFF_B + s * L::B_BYTES);
 #pragma unroll
                         for (int kk = 0; kk < kBlockK / kMmaK; ++kk)
-                            ptx::mma_f8f6f4(tmem_base, adesc + 2 * kk, bdesc + 2 * kk, idesc, (ks | kk) != 0 ? 1u : 0u);
+                            ptx::mma_f8f6f4(tmem_base, adesc + 2 * kk, bdesc + 2 * kk, idesc,
+                                            (it != seg_start || kk != 0) ? 1u : 0u);
                         ptx::tc_commit(empty_bar(s));
                         continue;
                     }
@@ -194,7 +213,7 @@ __device__ __forceinline__ void mx_gemm_body(const CUtensorMap &tmA, const CUten
                     for (int kk = 0; kk < kBlockK / kMmaK; ++kk)
                         ptx::mma_mxf8f6f4(tmem_base, adesc + 2 * kk, bdesc + 2 * kk,
                                           ptx::idesc_mxf8f6f4_e4m3(kBlockM, BN, kk, kk), sfa_t, sfb_t,
-                                          (ks | kk) != 0 ? 1u : 0u);
+                                          (it != seg_start || kk != 0) ? 1u : 0u);
                     ptx::tc_commit(empty_bar(s));
                 }
                 if (!ok)
@@ -204,18 +223,28 @@ __device__ __forceinline__ void mx_gemm_body(const CUtensorMap &tmA, const CUten
             ptx::tc_commit(mma_done_bar);
             wait_teardown(mma_done_bar, 0, args);
         }
+    }
     } else {
+        ptx::setmaxnreg_inc<kMxRegsHigh>();
         // ------------------------------------------------------ epilogue
         constexpr int HALF = BN / 2;
-        const int ew = warp - 2;                // 0..7
+        constexpr bool kSk = BN == 256;         // tile width with the stream-K hand-off
+        const int ew = warp - 4;                // 0..7
         const int wg = ew >> 2;
         const int q = warp & 3;
+        const int row = q * 32 + lane;          // row of the tile
         const uint32_t cstage = sbase + L::OFF_C + ew * kCStageBytes;
-        int titer = 0;
-        for (int t = blockIdx.x; t < num_tiles; t += gridDim.x, ++titer) {
-            int mb, nb;
+        WorkSpan span;
+        span.init(args, KS);
+        bool ok = true;
+        for (int it = 0, sg = 0; it < span.total; ++sg) {
+            int t, ks0, mb, nb;
+            span.step(it, t, ks0);
+            const int len = (KS - ks0) < (span.total - it) ? (KS - ks0) : (span.total - it);
+            const int ks_last = ks0 + len - 1;
+            it += len;
             args.raster.coords(t, mb, nb);
-            if (!wait_bounded_warp(acc_full_bar, titer & 1, abort_flag, args))
+            if (!wait_bounded_warp(acc_full_bar, sg & 1, abort_flag, args))
                 break;
             ptx::tc_fence_after();
             float v[HALF];
@@ -227,13 +256,65 @@ __device__ __forceinline__ void mx_gemm_body(const CUtensorMap &tmA, const CUten
                 ptx::tmem_ld_32x32b_x32(taddr + c * 32, r);
 #pragma unroll
                 for (int j = 0; j < 32; ++j)
-                    v[c * 32 + j] = MX ? __uint_as_float(r[j]) : __uint_as_float(r[j]) * args.alpha;
+                    v[c * 32 + j] = __uint_as_float(r[j]);
             }
             ptx::tmem_wait_ld();
             ptx::tc_fence_before();
             __syncwarp();
             if (lane == 0)
                 ptx::mbar_arrive(acc_empty_bar);
+            // Stream-K hand-off, warp by warp, as in the blockscale kernel: warp
+            // ew of every CTA owns the same 32 rows x HALF columns of a tile, in
+            // slot layout [column/4][row] of float4.
+            const size_t slice = static_cast<size_t>(wg * HALF / 4) * kBlockM + static_cast<size_t>(row);
+            if (kSk && ks0 > 0) {
+                // Head of a tile begun by an earlier CTA: publish the partial.
+                float *dst = args.sk_partial + static_cast<size_t>(blockIdx.x) * (BN * kBlockM) + 4 * slice;
+#pragma unroll
+                for (int j = 0; j < HALF; j += 4)
+                    ptx::st_global_v4_f32(dst + static_cast<size_t>(j / 4) * kBlockM * 4, v[j], v[j + 1], v[j + 2],
+                                          v[j + 3]);
+                __threadfence();
+                __syncwarp();
+                if (lane == 0)
+                    ptx::st_release_gpu_u64(args.sk_flags + static_cast<size_t>(blockIdx.x) * kEpiWarps + ew,
+                                            args.sk_token);
+                continue;
+            }
+            if (kSk && ks_last != KS - 1) {
+                // This CTA holds K step 0 of a cut tile: add the partials of the
+                // CTAs up to the one whose range holds the tile's last unit.
+                const long long G = gridDim.x;
+                const long long U = static_cast<long long>(num_tiles - span.tile0) * KS;
+                const long long tile_end = static_cast<long long>(t + 1 - span.tile0) * KS;
+                const int c_last = static_cast<int>((tile_end * G - 1) / U);
+                for (int c2 = static_cast<int>(blockIdx.x) + 1; c2 <= c_last; ++c2) {
+                    unsigned long long *flag = args.sk_flags + static_cast<size_t>(c2) * kEpiWarps + ew;
+                    if (!sk_wait_flag(flag, args.sk_token, abort_flag, args)) {
+                        ok = false;
+                        break;
+                    }
+                    const float *src = args.sk_partial + static_cast<size_t>(c2) * (BN * kBlockM) + 4 * slice;
+#pragma unroll
+                    for (int j = 0; j < HALF; j += 4) {
+                        const float4 p = ptx::ld_cg_v4_f32(src + static_cast<size_t>(j / 4) * kBlockM * 4);
+                        v[j] += p.x;
+                        v[j + 1] += p.y;
+                        v[j + 2] += p.z;
+                        v[j + 3] += p.w;
+                    }
+                    __syncwarp();
+                    if (lane == 0)
+                        *reinterpret_cast<volatile unsigned long long *>(flag) = 0ull;   // ready for the next call
+                }
+                if (!ok)
+                    break;
+            }
+            if constexpr (!MX) {
+#pragma unroll
+                for (int j = 0; j < HALF; ++j)
+                    v[j] *= args.alpha;
+            }
             const int x0 = nb * BN + wg * HALF;
             const int y0 = mb * kBlockM + q * 32;
 #pragma unroll

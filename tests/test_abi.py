@@ -63,10 +63,10 @@ def test_tensorscale_entry_checks_before_launch(lib):
     assert f(None, P, P, 4, 8, 128, one, None) == -1
     assert f(ctypes.c_void_p((1 << 20) + 8), P, P, 4, 8, 128, one, None) == -2
     assert f(P, P, ctypes.c_void_p((1 << 20) + 8), 4, 8, 128, one, None) == -2
-    for cid in (4256411, 4128611, 4256401, 4128601):
+    for cid in (4256411, 4128611, 4256401, 4128601, 4256412):
         assert L.fp8bs_set_config_override(cid) == 0
         assert lib.decode_config(cid)["kind"] == "tensorscale"
-    assert L.fp8bs_set_config_override(4256412) == -3     # no stream-K twin
+    assert L.fp8bs_set_config_override(4128612) == -3     # stream-K with the 256-wide tile only
     assert L.fp8bs_set_config_override(0) == 0
 
 
@@ -132,7 +132,9 @@ def test_config_selection(lib):
     L = lib.lib()
     assert L.fp8bs_set_config_override(1999911) == -3      # no such kernel
     assert L.fp8bs_set_config_override(1160511) == -3      # the 160-wide tile was removed
-    assert L.fp8bs_set_config_override(2256412) == -3      # stream-K is blockscale-only
+    assert L.fp8bs_set_config_override(2128612) == -3      # stream-K runs with the 256-wide tile only
+    assert L.fp8bs_set_config_override(4128612) == -3
+    assert L.fp8bs_set_config_override(3128812) == -3      # no stream-K for the CTA pair
     assert L.fp8bs_set_config_override(1256413) == -3      # no such schedule
     assert L.fp8bs_set_config_override(1128612) == -3      # stream-K runs with the 256-wide tile only
     assert L.fp8bs_set_config_override(0) == 0
@@ -149,8 +151,14 @@ def test_schedule_selection(lib):
     assert sched(4096, 2048, 7168, sms=128) == "tile"   # 256 tiles = 2 full waves
     assert sched(4096, 2048, 128) == "tile"           # one K block: nothing to share
     assert sched(256, 512, 512) == "tile"             # 8 tiles x 4: 4 -> 1, not worth a hand-off
-    # the MXFP8 kernel has one schedule
-    assert lib.decode_config(lib.select_config("mx", 4096, 2048, 7168, 152))["schedule"] == "tile"
+    # MXFP8: stream-K when it saves >= 4 K steps (128 wide) in the longest CTA
+    mx = lambda M, N, K, sms=152: lib.decode_config(lib.select_config("mx", M, N, K, sms))["schedule"]
+    assert mx(1024, 5120, 2048) == "stream_k"         # 160 tiles x 16: 32 -> 17
+    assert mx(2048, 8192, 1280) == "stream_k"         # 512 tiles x 10: 40 -> 34
+    assert mx(32, 5120, 2048) == "stream_k"           # 20 tiles x 16: 16 -> 3 (decode)
+    assert mx(16384, 5120, 2048) == "tile"            # 2560 tiles x 16: 272 -> 270
+    assert mx(1024, 8192, 1280) == "tile"             # 256 tiles x 10: 20 -> 17
+    assert mx(256, 512, 512) == "tile"
 
 
 def test_status_strings(lib):

@@ -180,7 +180,7 @@ def test_pack_a_scale_bit_exact():
 # every built kernel configuration, forced through the override
 # one-CTA 128x256, 128x128 (one CTA per tile), 128x256 stream-K, CTA-pair 256x128
 BS_CONFIGS = [1256411, 1128611, 1256412, 3128811]
-MX_CONFIGS = [2256411, 2128611]
+MX_CONFIGS = [2256411, 2128611, 2256412]
 
 
 @pytest.fixture
@@ -408,11 +408,13 @@ def test_stream_k_after_whole_waves(override):
     compare(got[rows], ref, "stream-K after whole waves")
 
 
-def test_mxfp8_cuda_graph_replay():
-    """fp8mx_gemm (scale pack + GEMM, pooled workspace) captured in a CUDA graph
-    and replayed on new input contents."""
+@pytest.mark.parametrize("cid", [2256401, 2256402])
+def test_mxfp8_cuda_graph_replay(override, cid):
+    """fp8mx_gemm (scale pack + GEMM, pooled workspace; stream-K workspace too)
+    captured in a CUDA graph and replayed on new input contents."""
     import torch
     import fp8_block_scaled_e4m3_gb300 as f
+    override(cid)
     M, N, K = 300, 520, 1280
     x0, x1 = (workloads.make_mxfp8_inputs(M, N, K, seed=s) for s in (41, 42))
     d = [to_dev(x0.A), to_dev(x0.a_e8m0), to_dev(x0.B), to_dev(x0.b_e8m0)]
@@ -434,8 +436,52 @@ def test_mxfp8_cuda_graph_replay():
         del g
 
 
+@pytest.mark.parametrize("M,N,K", [(256, 512, 7168), (130, 264, 3840), (1100, 776, 2048), (32, 5120, 2048),
+                                   (1, 520, 1280)])
+def test_mxfp8_stream_k_tiles_cut_between_many_ctas(override, M, N, K):
+    """MXFP8 under stream-K: few tiles (decode-like M included), each accumulated
+    in pieces by several CTAs; ragged tails inside cut tiles."""
+    import fp8_block_scaled_e4m3_gb300 as f
+    cid = 2256402 + (10 if M >= N else 0)
+    override(cid)
+    x = workloads.make_mxfp8_inputs(M, N, K, seed=M + N + 5)
+    got = run_mxfp8(x.A, x.a_e8m0, x.B, x.b_e8m0)
+    assert f.last_config_id() == cid
+    compare(got, oracle.mxfp8(x.A, x.a_e8m0, x.B, x.b_e8m0), f"mx stream-K {M}x{N}x{K}")
+
+
+def test_mxfp8_stream_k_back_to_back_calls(override):
+    import torch
+    import fp8_block_scaled_e4m3_gb300 as f
+    override(2256402)
+    M, N, K = 256, 1024, 4096
+    xs = [workloads.make_mxfp8_inputs(M, N, K, seed=s) for s in (51, 52)]
+    dev = [(to_dev(x.A), to_dev(x.a_e8m0), to_dev(x.B), to_dev(x.b_e8m0)) for x in xs]
+    outs = [f.gemm_mxfp8(*d) for d in (dev[0], dev[1], dev[0])]   # no sync in between
+    assert f.get_status() == 0
+    bits = [o.view(torch.int16).cpu().numpy().view(np.uint16) for o in outs]
+    for b, x in zip(bits, (xs[0], xs[1], xs[0])):
+        compare(b, oracle.mxfp8(x.A, x.a_e8m0, x.B, x.b_e8m0), "mx stream-K back to back")
+    assert np.array_equal(bits[0], bits[2])
+
+
+def test_mxfp8_stream_k_after_whole_waves():
+    """320 tiles of 16 K steps on 152 SMs: one wave one CTA per tile, then
+    stream-K over the rest (ranges start mid-tile); whole row blocks from both."""
+    import fp8_block_scaled_e4m3_gb300 as f
+    M, N, K = 5120, 2048, 2048
+    if f.device_info()["num_sms"] != 152:
+        pytest.skip("the wave split below is worked out for 152 SMs")
+    assert f.decode_config(f.select_config("mx", M, N, K, 152))["schedule"] == "stream_k"
+    x = workloads.make_mxfp8_inputs(M, N, K, seed=78)
+    got = run_mxfp8(x.A, x.a_e8m0, x.B, x.b_e8m0)
+    assert f.last_config_id() == 2256412
+    rows = np.concatenate([np.arange(mb * 128, mb * 128 + 128) for mb in (0, 18, 19, 25, 39)])
+    compare(got[rows], oracle.mxfp8(x.A[rows], x.a_e8m0[rows], x.B, x.b_e8m0), "mx stream-K after whole waves")
+
+
 # ------------------------------------------------ promote-free ceiling twin
-@pytest.mark.parametrize("cfg", [4256411, 4128611])
+@pytest.mark.parametrize("cfg", [4256411, 4128611, 4256412])
 @pytest.mark.parametrize("M,N,K", [(300, 520, 1280), (129, 136, 256), (1, 8, 128), (640, 768, 7168)])
 def test_tensorscale_every_config(override, cfg, M, N, K):
     import torch
