@@ -194,6 +194,12 @@ int setup_stream_k(int tiles, int KB, int num_sms, cudaMemPool_t pool, cudaStrea
     grid = static_cast<int>(sk_grid(units, KB, num_sms));
     const int full_waves = tiles / grid;
     args.sk_dp = full_waves >= 2 ? full_waves - 1 : 0;
+    // Every CTA must hold at least one unit of the stream-K range: a finisher
+    // waits for each CTA after it up to the one holding its tile's last unit.
+    // (True by construction: the range has at least a wave of tiles, or grid <=
+    // units / 8.)
+    if (static_cast<long long>(tiles - args.sk_dp * grid) * KB < grid)
+        return FP8BS_ERR_SHAPE;
     const size_t slot = static_cast<size_t>(kBlockM) * 256 * sizeof(float);
     const size_t bytes = static_cast<size_t>(grid) * (slot + kEpiWarps * sizeof(unsigned long long));
     if (cudaMallocFromPoolAsync(&ws, bytes, pool, s) != cudaSuccess)

@@ -368,7 +368,9 @@ __global__ void __launch_bounds__(kBsThreads, 1)
                 for (int j = 0; j < HALF; j += 4)
                     ptx::st_global_v4_f32(dst + static_cast<size_t>(j / 4) * kBlockM * 4, acc[j], acc[j + 1], acc[j + 2],
                                           acc[j + 3]);
-                __threadfence();
+                // The warp barrier orders every lane's stores before lane 0's
+                // release store of the flag, and a release is cumulative: a
+                // finisher that acquires the flag sees the whole slice.
                 __syncwarp();
                 if (lane == 0)
                     ptx::st_release_gpu_u64(args.sk_flags + static_cast<size_t>(blockIdx.x) * kEpiWarps + ew,
