@@ -173,11 +173,17 @@ long long sk_grid(long long units, long long KB, int num_sms)
     return g < 1 ? 1 : g;
 }
 
-// Smallest saving of K steps in the longest CTA for which stream-K is chosen:
-// a blockscale K block costs ~1000 clocks and the hand-off a few thousand; an
-// MXFP8 K step costs ~700 clocks.
-constexpr long long kSkMinGainBs = 8;
-constexpr long long kSkMinGainMx = 4;
+// Smallest saving of K steps in the longest CTA for which stream-K is chosen.
+// The hand-off costs 5-12 us per launch whatever the shape (publishing a 128 KB
+// fp32 partial takes ~3.5 us, the finisher's add ~1.5 us, and each CTA has an
+// extra segment boundary), against ~0.5 us per blockscale K block and ~0.35 us
+// per MXFP8 K step. Measured on 152 SMs (tile vs stream-K, us): blockscale
+// 16384x1536x7168 179/159 (saving 53), 8192x2048x7168 122/110 (35),
+// 1024x2048x7168 35.5/32.5 (32), 4096x2048x7168 66.2/67.3 (17),
+// 2048x2048x7168 37.6/40.7 (8); MXFP8 1024x5120x2048 28.4/26.4 (15),
+// 4096x5120x2048 48.9/48.9 (12), 2048x8192x1280 34.5/36.6 (6).
+constexpr long long kSkMinGainBs = 20;
+constexpr long long kSkMinGainMx = 13;
 
 // Stream-K set-up shared by the one-CTA kernels with a 256-wide tile: the grid,
 // the whole waves run one CTA per tile before the stream-K range (the CTAs of a
@@ -229,7 +235,7 @@ Config choose_config(int kind, int M, int N, int K, int num_sms)
     const long long tiles256 = (long long)((M + 127) / 128) * ((N + 255) / 256);
     // Stream-K (256-wide tile) when it shortens the longest CTA's K loop by at
     // least kSkMinGain K steps, which pays for the partial hand-off. E.g.
-    // blockscale 256 tiles x 56 K blocks on 152 SMs: 112 -> 95; 8 tiles x 56:
+    // blockscale 768 tiles x 56 K blocks on 152 SMs: 336 -> 283; 8 tiles x 56:
     // 56 -> 3. The tensor-scale twin follows the blockscale rule, so that the two
     // run the same tiles.
     const long long KB = K / 128;

@@ -6,8 +6,7 @@
  * as void* (NULL = the legacy default stream). Every GEMM call is asynchronous
  * on `stream`, performs no host synchronisation and no allocation after the
  * first call on a device (except the pooled workspaces of fp8mx_gemm and of
- * fp8bs_gemm's stream-K schedule, see there), and can be captured in a CUDA
- * graph.
+ * the stream-K schedule, see fp8bs_gemm), and can be captured in a CUDA graph.
  *
  * Error behaviour: functions return FP8BS_OK (0) or a negative fp8bs_status.
  * Argument errors are detected on the host before anything is launched.
@@ -59,8 +58,8 @@ typedef enum {
  * A partial last N block of 128 rows uses its own b_scale row.
  *
  * Schedule: one CTA per output tile, or, when that shortens the longest CTA's
- * loop by at least 8 K blocks (a partial last wave of tiles, or few tiles with
- * a long K), stream-K: the (tile, K block) units are split
+ * loop by at least 20 K blocks (a partial last wave of tiles, or few tiles
+ * with a long K), stream-K: the (tile, K block) units are split
  * evenly over the CTAs and a tile cut between CTAs is summed in fp32 from their
  * scaled partials (the same sum in another order). Stream-K takes a workspace
  * of grid * (128 * 256 * 4 + 64) bytes from a stream-ordered memory pool,
@@ -98,8 +97,9 @@ int fp8mx_gemm(const void *A, const uint8_t *a_e8m0, const void *B, const uint8_
                int M, int N, int K, void *stream);
 
 /*
- * MXFP8 GEMM on scale factors already in the packed layout (no allocation,
- * one kernel). The PR above keeps its scale shuffles as separate weight-prep
+ * MXFP8 GEMM on scale factors already in the packed layout (one kernel; no
+ * allocation except the stream-K workspace, chosen as for fp8bs_gemm when it
+ * saves at least 13 K steps of 128, same size, pool and graph caveat). The PR above keeps its scale shuffles as separate weight-prep
  * helpers for the same reason: the kernel wants a layout the quantiser does
  * not produce.
  *   a_sf  fp8mx_packed_scale_bytes(M, K) bytes, 16-byte aligned, from fp8mx_pack_scales.
@@ -120,7 +120,8 @@ int fp8mx_gemm_packed(const void *A, const uint8_t *a_sf, const void *B, const u
  * fp32 sums run over the whole K extent in tensor memory and alpha is applied
  * once in the epilogue. Comparing its time with fp8bs_gemm's on the same shape
  * measures the cost of the per-block software scaling. One kernel; config ids
- * of kind 4 (same tiles as the MXFP8 kernel).
+ * of kind 4 (the MXFP8 kernel's tiles, fp8bs_gemm's schedule rule and
+ * stream-K workspace).
  */
 int fp8bs_gemm_tensorscale(const void *A, const void *B, void *C, int M, int N, int K, float alpha,
                            void *stream);
@@ -150,7 +151,8 @@ int fp8mx_pack_scales(const uint8_t *e8m0, uint8_t *packed, int rows, int K, voi
  * that forbids allocator calls. fp8mx_gemm takes its packed-scale workspace
  * from a memory pool; this entry point uses a fixed device array of
  * fp8mx_noalloc_scratch_bytes() bytes (8 MiB) built into the library instead,
- * which every GPU that loads the library holds until the process exits.
+ * which every GPU that loads the library holds until the process exits. It
+ * always runs one CTA per tile (stream-K would need a workspace).
  *
  * Limit: fp8mx_packed_scale_bytes(M, K) + fp8mx_packed_scale_bytes(N, K) must
  * not exceed that size, else FP8BS_ERR_SCRATCH_TOO_SMALL (checked on the host,
@@ -199,7 +201,7 @@ const char *fp8bs_status_string(int status);
  * raster*10 + schedule; kind 1 = one-CTA blockscale kernel (128 x block_n
  * tiles), 2 = mxfp8 kernel, 3 = CTA-pair blockscale kernel (256 x block_n tiles
  * over two SMs), 4 = tensor-scale twin (fp8bs_gemm_tensorscale); schedule 1 =
- * one CTA per tile, 2 = stream-K (kind 1 with block_n 256 only). */
+ * one CTA per tile, 2 = stream-K (kinds 1, 2 and 4 with block_n 256 only). */
 int fp8bs_last_config_id(void);
 /* Configuration id fp8bs_gemm / fp8mx_gemm would choose for a shape on a
  * device with `num_sms` SMs (host-only, no CUDA calls). */

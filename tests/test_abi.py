@@ -141,23 +141,26 @@ def test_config_selection(lib):
 
 
 def test_schedule_selection(lib):
-    # Stream-K exactly when it shortens the longest CTA's K loop by >= 8 K blocks.
+    # Stream-K exactly when it shortens the longest CTA's K loop by >= 20 K
+    # blocks (blockscale) or >= 13 K steps (MXFP8).
     sched = lambda M, N, K, sms=152: lib.decode_config(lib.select_config("bs", M, N, K, sms))["schedule"]
-    assert sched(4096, 2048, 7168) == "stream_k"      # 256 tiles x 56: 112 -> 95 K blocks
-    assert sched(16384, 1536, 7168) == "stream_k"     # 768 tiles x 56: 336 -> 283
+    assert sched(16384, 1536, 7168) == "stream_k"     # 768 tiles x 56: 336 -> 283 K blocks
+    assert sched(8192, 2048, 7168) == "stream_k"      # 512 tiles x 56: 224 -> 189
     assert sched(256, 512, 7168) == "stream_k"        # 8 tiles x 56: 56 -> 3
+    assert sched(4096, 2048, 7168) == "tile"          # 256 tiles x 56: 112 -> 95
+    assert sched(2048, 2048, 7168) == "tile"          # 128 tiles x 56: 56 -> 48
     assert sched(16384, 7168, 768) == "tile"          # 3584 tiles x 6: 144 -> 142
     assert sched(4096, 65536, 1536) == "tile"         # 8192 tiles x 12: 648 -> 647
-    assert sched(4096, 2048, 7168, sms=128) == "tile"   # 256 tiles = 2 full waves
+    assert sched(16384, 1536, 7168, sms=128) == "tile"  # 768 tiles = 6 full waves
     assert sched(4096, 2048, 128) == "tile"           # one K block: nothing to share
     assert sched(256, 512, 512) == "tile"             # 8 tiles x 4: 4 -> 1, not worth a hand-off
-    # MXFP8: stream-K when it saves >= 4 K steps (128 wide) in the longest CTA
     mx = lambda M, N, K, sms=152: lib.decode_config(lib.select_config("mx", M, N, K, sms))["schedule"]
     assert mx(1024, 5120, 2048) == "stream_k"         # 160 tiles x 16: 32 -> 17
-    assert mx(2048, 8192, 1280) == "stream_k"         # 512 tiles x 10: 40 -> 34
-    assert mx(32, 5120, 2048) == "stream_k"           # 20 tiles x 16: 16 -> 3 (decode)
+    assert mx(2048, 5120, 2048) == "stream_k"         # 320 tiles x 16: 48 -> 34
+    assert mx(4096, 5120, 2048) == "tile"             # 640 tiles x 16: 80 -> 68
+    assert mx(2048, 8192, 1280) == "tile"             # 512 tiles x 10: 40 -> 34
+    assert mx(32, 5120, 2048) == "tile"               # 20 tiles x 16: 16 -> 8
     assert mx(16384, 5120, 2048) == "tile"            # 2560 tiles x 16: 272 -> 270
-    assert mx(1024, 8192, 1280) == "tile"             # 256 tiles x 10: 20 -> 17
     assert mx(256, 512, 512) == "tile"
 
 
