@@ -338,6 +338,10 @@ def run_ours(args):
     if kind == "bs" and not args.no_twin:
         twin = measure_twin(args, torch, f, d, C, flush, stream, flops, kernel_ms, peaks)
 
+    e4m3 = None
+    if kind == "bs" and not args.no_twin and N % 16 == 0:
+        e4m3 = measure_e4m3out(args, torch, f, d, flush, stream, flops, kernel_ms, peaks, M, N)
+
     e2e = None
     if not args.no_e2e:
         e2e = measure_e2e(args, torch, f, kind, M, N, K, host, gemm)
@@ -357,7 +361,7 @@ def run_ours(args):
                        "parallelism": f"{world} independent replicas (weak scaling)",
                        "wall_s_timed_loop": wall, "warmup_steps_run": n_w, "ms_min": min(per_ms),
                        "ms_median": statistics.median(per_ms)},
-            "roofline": roofline, "ceiling_twin": twin,
+            "roofline": roofline, "ceiling_twin": twin, "e4m3_out": e4m3,
             "gpu_launches": args.steps * (f.lib().fp8bs_launches_per_call() if kind == "bs"
                                           else f.lib().fp8mx_launches_per_call()),
             "clocks": clocks, "e2e": e2e, "cpu_baseline": cpu}
@@ -391,6 +395,30 @@ def measure_twin(args, torch, f, d, C, flush, stream, flops, kernel_ms, peaks):
     return {"kernel": "fp8bs_tensorscale_kernel", "config_id": twin_cfg, "steps": n, "kernel_ms": twin_ms,
             "achieved": tf, "frac": tf / peaks["fp8_tflops"], "unit": "TFLOP/s",
             "scale_tax": kernel_ms / twin_ms - 1.0}
+
+
+def measure_e4m3out(args, torch, f, d, flush, stream, flops, kernel_ms, peaks, M, N):
+    """The same GEMM with the E4M3 output epilogue (C8 = e4m3(c_scale * C), one
+    byte per element instead of two), timed with the same protocol."""
+    C8 = torch.empty((M, N), dtype=torch.uint8, device="cuda")
+    c_scale = 32.0
+    for _ in range(3):
+        f.gemm_blockscale_e4m3out(d[0], d[1], d[2], d[3], c_scale, C8=C8)
+    assert f.get_status() == 0
+    n = max(3, min(args.steps, 100))
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+    for i in range(n):
+        flush.fill_(1)
+        ev[i][0].record(stream)
+        f.gemm_blockscale_e4m3out(d[0], d[1], d[2], d[3], c_scale, C8=C8)
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    assert f.get_status() == 0
+    ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+    tf = flops / (ms * 1e-3) / 1e12
+    return {"kernel": "fp8bs_blockscale_kernel (E4M3 C)", "config_id": f.last_config_id(), "steps": n,
+            "kernel_ms": ms, "achieved": tf, "frac": tf / peaks["fp8_tflops"], "unit": "TFLOP/s",
+            "c_bytes": M * N, "speedup_vs_bf16_c": kernel_ms / ms}
 
 
 def measure_e2e(args, torch, f, kind, M, N, K, host, gemm):

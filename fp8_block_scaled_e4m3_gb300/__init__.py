@@ -29,6 +29,7 @@ _i64 = ctypes.c_int64
 _SIGS = {
     "fp8bs_gemm": (_i, [_p, _p, _p, _p, _p, _i, _i, _i, _p]),
     "fp8bs_gemm_tensorscale": (_i, [_p, _p, _p, _i, _i, _i, ctypes.c_float, _p]),
+    "fp8bs_gemm_e4m3out": (_i, [_p, _p, _p, _p, _p, ctypes.c_float, _i, _i, _i, _p]),
     "fp8mx_gemm": (_i, [_p, _p, _p, _p, _p, _i, _i, _i, _p]),
     "fp8mx_gemm_packed": (_i, [_p, _p, _p, _p, _p, _i, _i, _i, _p]),
     "fp8mx_packed_scale_bytes": (_i64, [_i, _i]),
@@ -130,6 +131,27 @@ def gemm_blockscale(A, a_scale, B, b_scale, C=None, stream=None):
                          _dev_ptr(C, "C", (M, N)), M, N, K, _stream_ptr(stream))
     _check(rc, "fp8bs_gemm")
     return C
+
+
+def gemm_blockscale_e4m3out(A, a_scale, B, b_scale, c_scale, C8=None, stream=None):
+    """C8[M,N] E4M3 codes (uint8) = e4m3(c_scale * the blockscale GEMM's fp32 sum),
+    rounded to nearest even and saturated at +-448; decode(C8) / c_scale recovers C.
+    Arguments as gemm_blockscale; N must be a multiple of 16."""
+    torch = _torch()
+    M, K = A.shape
+    N = B.shape[0]
+    if C8 is None:
+        C8 = torch.empty((M, N), dtype=torch.uint8, device=A.device)
+    if a_scale.dtype != torch.float32 or b_scale.dtype != torch.float32:
+        raise TypeError("scales must be float32")
+    if C8.dtype not in (torch.uint8, torch.float8_e4m3fn):
+        raise TypeError("C8 must be uint8 or float8_e4m3fn")
+    rc = _lib.fp8bs_gemm_e4m3out(_fp8_ptr(A, "A", (M, K)), _dev_ptr(a_scale, "a_scale", (K // 128, a_scale_ld(M))),
+                                 _fp8_ptr(B, "B", (N, K)),
+                                 _dev_ptr(b_scale, "b_scale", ((N + 127) // 128, K // 128)),
+                                 _dev_ptr(C8, "C8", (M, N)), float(c_scale), M, N, K, _stream_ptr(stream))
+    _check(rc, "fp8bs_gemm_e4m3out")
+    return C8
 
 
 def gemm_tensorscale(A, B, alpha, C=None, stream=None):

@@ -133,7 +133,7 @@ int check_shape(int M, int N, int K)
 // Kernel configuration. kind 1: one-CTA blockscale kernel, 2: MXFP8 kernel,
 // 3: CTA-pair blockscale kernel (256 x 128 tiles over two SMs), 4: tensor-scale
 // twin (the MXFP8 kernel's pipeline with plain fp8 MMAs).
-// sched 1: one CTA per tile; 2: stream-K (blockscale one-CTA kernel only).
+// sched 1: one CTA per tile; 2: stream-K (256-wide tile of kinds 1, 2 and 4).
 struct Config {
     int kind, block_n, stages, raster, sched;
 };
@@ -370,20 +370,15 @@ int launch_mx(const Config &cfg, const void *A, const uint8_t *a_sf, const void 
     return e == cudaSuccess ? FP8BS_OK : FP8BS_ERR_LAUNCH;
 }
 
-} // namespace host
-} // namespace fp8bs
-
-using namespace fp8bs;
-using namespace fp8bs::host;
-
-extern "C" {
-
-int fp8bs_gemm(const void *A, const float *a_scale, const void *B, const float *b_scale, void *C, int M, int N,
-               int K, void *stream)
+// The blockscale GEMM with a bf16 (c_e4m3 == false) or an E4M3 C.
+int blockscale_gemm(const void *A, const float *a_scale, const void *B, const float *b_scale, void *C, bool c_e4m3,
+                    float c_scale, int M, int N, int K, void *stream)
 {
     int rc = check_shape(M, N, K);
     if (rc)
         return rc;
+    if (c_e4m3 && (N % 16) != 0)   // the E4M3 rows of C must be whole 16-byte units for the tensor copies
+        return FP8BS_ERR_SHAPE;
     if (M == 0)
         return FP8BS_OK;
     if (!A || !a_scale || !B || !b_scale || !C)
@@ -398,6 +393,8 @@ int fp8bs_gemm(const void *A, const float *a_scale, const void *B, const float *
     if (!override_config(1, 3, cfg))
         return FP8BS_ERR_SHAPE;
     const bool pair = cfg.kind == 3;
+    if (pair && c_e4m3)
+        return FP8BS_ERR_SHAPE;   // the CTA-pair kernel stores bf16 only
     const int KB = K / 128;
     const uint64_t ld_sa = static_cast<uint64_t>(fp8bs_a_scale_ld(M));
     const uint32_t b_box_rows = pair ? cfg.block_n / 2 : cfg.block_n;   // a pair CTA holds half of B
@@ -406,13 +403,17 @@ int fp8bs_gemm(const void *A, const float *a_scale, const void *B, const float *
         !encode_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, B, K, N, K, 128, b_box_rows, CU_TENSOR_MAP_SWIZZLE_128B) ||
         !encode_2d(&tmSA, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, a_scale, ld_sa, KB, ld_sa * 4, 128, 1,
                    CU_TENSOR_MAP_SWIZZLE_NONE) ||
-        !encode_2d(&tmC, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, C, N, M, static_cast<uint64_t>(N) * 2, kCChunkCols, 32,
-                   CU_TENSOR_MAP_SWIZZLE_64B))
+        !(c_e4m3 ? encode_2d(&tmC, CU_TENSOR_MAP_DATA_TYPE_UINT8, C, N, M, static_cast<uint64_t>(N), 64, 32,
+                             CU_TENSOR_MAP_SWIZZLE_64B)
+                 : encode_2d(&tmC, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, C, N, M, static_cast<uint64_t>(N) * 2,
+                             kCChunkCols, 32, CU_TENSOR_MAP_SWIZZLE_64B)))
         return FP8BS_ERR_LAUNCH;
     GemmArgs args = {};
     args.M = M;
     args.N = N;
     args.K = K;
+    args.c_e4m3 = c_e4m3 ? 1 : 0;
+    args.c_scale = c_scale;
     const int tile_m = pair ? 2 * kBlockM : kBlockM;
     args.raster.m_tiles = (M + tile_m - 1) / tile_m;
     args.raster.n_tiles = (N + cfg.block_n - 1) / cfg.block_n;
@@ -445,6 +446,26 @@ int fp8bs_gemm(const void *A, const float *a_scale, const void *B, const float *
         return FP8BS_ERR_LAUNCH;
     t_last_config = config_id(cfg);
     return FP8BS_OK;
+}
+
+} // namespace host
+} // namespace fp8bs
+
+using namespace fp8bs;
+using namespace fp8bs::host;
+
+extern "C" {
+
+int fp8bs_gemm(const void *A, const float *a_scale, const void *B, const float *b_scale, void *C, int M, int N,
+               int K, void *stream)
+{
+    return blockscale_gemm(A, a_scale, B, b_scale, C, false, 1.f, M, N, K, stream);
+}
+
+int fp8bs_gemm_e4m3out(const void *A, const float *a_scale, const void *B, const float *b_scale, void *C8,
+                       float c_scale, int M, int N, int K, void *stream)
+{
+    return blockscale_gemm(A, a_scale, B, b_scale, C8, true, c_scale, M, N, K, stream);
 }
 
 int fp8mx_gemm_packed(const void *A, const uint8_t *a_sf, const void *B, const uint8_t *b_sf, void *C, int M,

@@ -55,6 +55,8 @@ struct GemmArgs {
     const uint8_t *a_sf;       // mxfp8: packed scale atoms of A
     const uint8_t *b_sf;       // mxfp8: packed scale atoms of B
     float alpha;               // tensor-scale twin: C = bf16(alpha * A.B^T)
+    int c_e4m3;                // blockscale: C is E4M3, c_scale * sum rounded to nearest, saturated
+    float c_scale;
     int *status;               // per-device status word
     unsigned long long wait_limit_ns;       // limit of every pipeline wait
     unsigned long long teardown_limit_ns;   // limit of the waits for work already in flight (>= 1 s)
@@ -237,6 +239,38 @@ __device__ __forceinline__ void store_c_chunk(const CUtensorMap *tmC, uint32_t s
         const uint32_t w3 = ptx::pack_bf16x2(v[j * 8 + 6], v[j * 8 + 7]);
         const int phys = j ^ ((lane >> 1) & 3);
         ptx::st_shared_v4(stage + lane * 64 + phys * 16, w0, w1, w2, w3);
+    }
+    ptx::fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+        if (x < N && y < M)
+            ptx::tma_store_2d(tmC, stage, x, y);
+        ptx::bulk_commit();
+    }
+}
+
+// E4M3 output: one epilogue warp's 32 rows x 64 columns through the same 2 KiB
+// staging buffer and 64-byte swizzle as store_c_chunk (a row of 64 bytes), one
+// TMA store. Each value is multiplied by `scale` in fp32 and rounded to the
+// nearest E4M3 value (ties to even), saturating at +-448: the store side of the
+// fp8 partial of skill card "FlyDSL prefill MoE stage-2 fp8 partial"
+// (procedure step 2); the consumer multiplies by 1/scale.
+__device__ __forceinline__ void store_c8_chunk(const CUtensorMap *tmC, uint32_t stage, int lane, const float *v,
+                                               float scale, int x, int y, int M, int N)
+{
+    if (lane == 0)
+        ptx::bulk_wait_read_all();
+    __syncwarp();
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        uint32_t w[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const float *u = v + j * 16 + q * 4;
+            w[q] = ptx::pack_e4m3x4(u[0] * scale, u[1] * scale, u[2] * scale, u[3] * scale);
+        }
+        const int phys = j ^ ((lane >> 1) & 3);
+        ptx::st_shared_v4(stage + lane * 64 + phys * 16, w[0], w[1], w[2], w[3]);
     }
     ptx::fence_proxy_async_smem();
     __syncwarp();

@@ -72,6 +72,27 @@ int fp8bs_gemm(const void *A, const float *a_scale, const void *B, const float *
                int M, int N, int K, void *stream);
 
 /*
+ * fp8bs_gemm with an E4M3 C (epilogue fusion that halves the C write; the
+ * store side of skill card "FlyDSL prefill MoE stage-2 fp8 partial",
+ * procedure steps 2 and 5):
+ *
+ *   C8[m,n] = e4m3( c_scale * sum_kb P_kb[m,n] * a_scale[m,kb] * b_scale[n/128,kb] )
+ *
+ * The sum is the fp32 value fp8bs_gemm rounds to bf16; it is multiplied by
+ * c_scale in fp32 and rounded to the nearest E4M3FN value (ties to even),
+ * saturating at +-448 (a NaN stays NaN). A consumer recovers the value as
+ * decode(C8) / c_scale: c_scale is the single source of truth for both sides,
+ * passed as an argument (choose it so that |C| * c_scale sits mid-range in
+ * E4M3, e.g. 16 / rms(C)).
+ *   C8  E4M3 [M][N] row-major, written, 16-byte aligned.
+ * Other arguments, schedule and errors as fp8bs_gemm; in addition N % 16 == 0
+ * (FP8BS_ERR_SHAPE otherwise), and a forced CTA-pair configuration is rejected
+ * (FP8BS_ERR_SHAPE: that kernel stores bf16 only).
+ */
+int fp8bs_gemm_e4m3out(const void *A, const float *a_scale, const void *B, const float *b_scale, void *C8,
+                       float c_scale, int M, int N, int K, void *stream);
+
+/*
  * MXFP8 GEMM (PR "1x32 ue8m0 (MXFP8) 8-wave FlyDSL GEMM for gfx950", sections
  * "Why it is faster" and "Correctness"): both operands E4M3 with one ue8m0
  * scale 2^(e-127) per row and 32-wide K group g = k/32:

@@ -116,6 +116,53 @@ def tensorscale(A, B, alpha, rows=None):
     return blockscale(A, sa, B, sb, rows=rows)
 
 
+def e4m3_encode(y) -> np.ndarray:
+    """fp32 values -> OCP E4M3FN codes (uint8), rounded to the nearest
+    representable value with ties to the even mantissa, saturating at +-448;
+    the sign of a value that rounds to zero is kept (0x80 for -0).
+
+    From the format definition: a normal E4M3 value in the binade
+    [2^E, 2^(E+1)), E = -6..8, is a multiple of 2^(E-3) (three fraction
+    bits); below 2^-6 the values are the subnormal multiples of 2^-9. So the
+    nearest value is rint(|y| / quantum) * quantum (numpy's rint rounds half
+    to even, and the quotient of an fp32 by a power of two is exact in fp64);
+    a quotient of 16 lands on 2^(E+1), the first value of the next binade.
+    This is the store-side conversion of the fp8 partial in skill card "FlyDSL
+    prefill MoE stage-2 fp8 partial", procedure step 2, with the saturation
+    of the conversion the kernel uses (values past 448 are clamped, no NaN is
+    produced from a finite value)."""
+    y = np.asarray(y, dtype=np.float32).astype(np.float64)
+    if np.isnan(y).any():
+        raise ValueError("NaN input")
+    a = np.abs(y)
+    _, e = np.frexp(a)                       # a in [2^(e-1), 2^e)
+    E = np.maximum(e - 1, -6)                # binade; the subnormals share the quantum of E = -6
+    quantum = np.ldexp(1.0, E - 3)
+    v = np.minimum(np.rint(a / quantum) * quantum, 448.0)
+    # value -> code
+    code = np.zeros(a.shape, dtype=np.int64)
+    sub = v < 2.0 ** -6
+    code[sub] = np.rint(v[sub] / 2.0 ** -9).astype(np.int64)           # exponent field 0
+    nv = v[~sub]
+    _, e2 = np.frexp(nv)
+    E2 = e2 - 1                                                        # nv in [2^E2, 2^(E2+1))
+    mant = np.rint(nv / np.ldexp(1.0, E2 - 3)).astype(np.int64) - 8     # 0..7
+    code[~sub] = ((E2 + 7) << 3) | mant
+    code |= np.where(np.signbit(y), 0x80, 0)
+    return code.astype(np.uint8)
+
+
+def blockscale_e4m3out(A, a_scale, B, b_scale, c_scale, rows=None):
+    """The blockscale GEMM with an E4M3 C: codes = e4m3(c_scale * C), C the
+    exact sum rounded to fp32 and multiplied by the fp32 c_scale in fp32, the
+    precision in which the kernel takes the same decision (its sum is fp32).
+    Returns (codes uint8 [rows, N], y float32 [rows, N]: the value that was
+    rounded, for judging ties near a rounding boundary)."""
+    _, exact = blockscale(A, a_scale, B, b_scale, rows=rows, exact=True)
+    y = (exact.astype(np.float32) * np.float32(c_scale)).astype(np.float32)
+    return e4m3_encode(y), y
+
+
 def blockscale_blockpartial(A, a_scale, B, b_scale, rows=None, exact=False):
     M, K = A.shape
     N = B.shape[0]

@@ -70,6 +70,18 @@ def test_tensorscale_entry_checks_before_launch(lib):
     assert L.fp8bs_set_config_override(0) == 0
 
 
+def test_e4m3out_entry_checks_before_launch(lib):
+    L = lib.lib()
+    f = L.fp8bs_gemm_e4m3out
+    P = ctypes.c_void_p(1 << 20)
+    one = ctypes.c_float(1.0)
+    assert f(P, P, P, P, P, one, 4, 24, 128, None) == -3        # N % 16 (E4M3 rows of whole 16-byte units)
+    assert f(P, P, P, P, P, one, 4, 32, 100, None) == -3        # K % 128
+    assert f(None, None, None, None, None, one, 0, 32, 128, None) == 0
+    assert f(None, P, P, P, P, one, 4, 32, 128, None) == -1
+    assert f(P, P, P, P, ctypes.c_void_p((1 << 20) + 8), one, 4, 32, 128, None) == -2
+
+
 def test_alignment_rejected_before_launch(lib):
     L = lib.lib()
     a16 = ctypes.c_void_p(1 << 20)

@@ -9,7 +9,7 @@ import pytest
 
 import oracle
 import workloads
-from gpu_util import compare, run_blockscale, run_mxfp8, to_dev
+from gpu_util import compare, compare_e4m3, run_blockscale, run_mxfp8, to_dev
 
 pytestmark = pytest.mark.gpu
 
@@ -512,3 +512,76 @@ def test_tensorscale_integer_exact():
     assert f.get_status() == 0
     got = out.view(torch.int16).cpu().numpy().view(np.uint16)
     assert np.array_equal(got, oracle.tensorscale(A, B, 0.25))
+
+
+# ------------------------------------------------ E4M3 output (epilogue fusion)
+def _c_scale(x, rows=None):
+    """16 / rms(C) rounded to a power of two, from the oracle's bf16 result: the
+    pre-store values sit mid-range in E4M3."""
+    ref = oracle.bf16_bits_to_float(oracle.blockscale(x.A, x.a_scale, x.B, x.b_scale, rows=rows)).astype(np.float64)
+    rms = float(np.sqrt(np.mean(ref ** 2))) or 1.0
+    return float(2.0 ** np.round(np.log2(16.0 / rms)))
+
+
+def _run_e4m3out(x, c_scale):
+    import torch
+    import fp8_block_scaled_e4m3_gb300 as f
+    out = f.gemm_blockscale_e4m3out(to_dev(x.A), to_dev(workloads.a_scale_to_kmajor(x.a_scale)), to_dev(x.B),
+                                    to_dev(np.ascontiguousarray(x.b_scale)), c_scale)
+    assert f.get_status() == 0
+    return out.cpu().numpy()
+
+
+@pytest.mark.parametrize("cfg", [1256411, 1128611, 1256412])
+@pytest.mark.parametrize("M,N,K", [(300, 528, 1280), (129, 144, 256), (1, 16, 128), (640, 768, 7168)])
+def test_blockscale_e4m3out_every_config(override, cfg, M, N, K):
+    import fp8_block_scaled_e4m3_gb300 as f
+    raster = 1 if M >= N else 0
+    cid = cfg - (cfg // 10 % 10) * 10 + raster * 10
+    override(cid)
+    x = workloads.make_blockscale_inputs(M, N, K, seed=M + 3 * N)
+    s = _c_scale(x)
+    got = _run_e4m3out(x, s)
+    assert f.last_config_id() == cid
+    codes, y = oracle.blockscale_e4m3out(x.A, x.a_scale, x.B, x.b_scale, s)
+    compare_e4m3(got, codes, y, s, f"e4m3out {cid} {M}x{N}x{K}")
+
+
+def test_blockscale_e4m3out_saturates():
+    """A c_scale far too large: every output of magnitude > 448 / c_scale is +-448."""
+    x = workloads.make_blockscale_inputs(256, 512, 512, seed=9)
+    s = _c_scale(x) * 64
+    got = _run_e4m3out(x, s)
+    codes, y = oracle.blockscale_e4m3out(x.A, x.a_scale, x.B, x.b_scale, s)
+    assert (np.abs(y) > 448).mean() > 0.1
+    assert np.all((got[np.abs(y) > 464] & 0x7F) == 0x7E)
+    compare_e4m3(got, codes, y, s, "e4m3out saturating")
+
+
+def test_blockscale_e4m3out_full_size_sampled_rows():
+    """16384x7168x768 (the K-light layer whose C write the fp8 store halves):
+    sampled whole rows against the oracle. C has rms ~0.02 * sqrt(768) = 0.55,
+    so c_scale = 32 puts it mid-range."""
+    M, N, K = 16384, 7168, 768
+    x = workloads.make_blockscale_inputs(M, N, K, seed=0)
+    rng = np.random.Generator(np.random.PCG64(123))
+    rows = np.sort(rng.choice(M, 48, replace=False))
+    s = 32.0
+    got = _run_e4m3out(x, s)
+    codes, y = oracle.blockscale_e4m3out(x.A[rows], x.a_scale[rows], x.B, x.b_scale, s)
+    compare_e4m3(got[rows], codes, y, s, "e4m3out 16384x7168x768")
+
+
+def test_e4m3out_feeds_the_next_gemm_with_one_scale():
+    """The consumer side: C8 is the A operand of a second blockscale GEMM whose
+    a_scale is 1/c_scale everywhere (the same scale, one source of truth)."""
+    M, N1, K1, N2 = 256, 1024, 2048, 384
+    x = workloads.make_blockscale_inputs(M, N1, K1, seed=44)
+    z = workloads.make_blockscale_inputs(1, N2, N1, seed=46)      # its B: [N2, N1] with 128x128 block scales
+    s = _c_scale(x)
+    c8 = _run_e4m3out(x, s)
+    codes, y = oracle.blockscale_e4m3out(x.A, x.a_scale, x.B, x.b_scale, s)
+    compare_e4m3(c8, codes, y, s, "first GEMM")
+    sa2 = np.full((M, N1 // 128), np.float32(1.0 / s), dtype=np.float32)
+    got = run_blockscale(c8, sa2, z.B, z.b_scale)
+    compare(got, oracle.blockscale(codes, sa2, z.B, z.b_scale), "E4M3 C as the next A")

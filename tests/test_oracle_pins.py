@@ -327,3 +327,69 @@ def test_tensorscale_oracle_is_the_exact_gemm_times_alpha():
     assert np.array_equal(one, want)
     four = oracle.tensorscale(A, B, 4.0)
     assert np.array_equal(oracle.bf16_bits_to_float(four), 4.0 * oracle.bf16_bits_to_float(one))
+
+
+# ---- E4M3 output (the fp8 store of skill card "FlyDSL prefill MoE stage-2 fp8 partial")
+
+def _e4m3_values():
+    """The 126 positive finite E4M3FN values by code (1..126), from torch's decoder."""
+    torch = pytest.importorskip("torch")
+    return torch.arange(256, dtype=torch.uint8).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+
+
+def test_e4m3_encoder_round_trips_every_finite_code():
+    vals = _e4m3_values()
+    codes = np.array([c for c in range(256) if not np.isnan(vals[c])], dtype=np.uint8)
+    assert np.array_equal(oracle.e4m3_encode(vals[codes].astype(np.float32)), codes)
+
+
+def test_e4m3_encoder_ties_go_to_even_and_neighbours_to_nearest():
+    vals = _e4m3_values()
+    for c in range(0, 126):
+        lo, hi = vals[c], vals[c + 1]
+        mid = np.float32((lo + hi) / 2)            # exact: E4M3 midpoints have 5 significant bits
+        assert float(mid) == (lo + hi) / 2
+        even = c if c % 2 == 0 else c + 1
+        assert oracle.e4m3_encode(np.array([mid]))[0] == even, c
+        below = np.nextafter(mid, np.float32(0))
+        above = np.nextafter(mid, np.float32(1e9))
+        assert oracle.e4m3_encode(np.array([below]))[0] == c
+        assert oracle.e4m3_encode(np.array([above]))[0] == c + 1
+        assert oracle.e4m3_encode(np.array([-mid]))[0] == 0x80 | even
+
+
+def test_e4m3_encoder_saturates_and_keeps_the_sign_of_zero():
+    big = np.array([448.0, 449.0, 463.9, 464.0, 1e6, 3e38], dtype=np.float32)
+    assert np.all(oracle.e4m3_encode(big) == 0x7E)
+    assert np.all(oracle.e4m3_encode(-big) == 0xFE)
+    tiny = np.array([0.0, 2.0 ** -11, -0.0, -(2.0 ** -11)], dtype=np.float32)   # below half the smallest subnormal
+    assert list(oracle.e4m3_encode(tiny)) == [0x00, 0x00, 0x80, 0x80]
+
+
+def test_e4m3_encoder_matches_torch_cast_in_range():
+    torch = pytest.importorskip("torch")
+    rng = np.random.Generator(np.random.PCG64(31))
+    x = (rng.standard_normal(100000) * np.exp(rng.uniform(-14, 6, 100000))).astype(np.float32)
+    x = x[np.abs(x) <= 448]
+    ref = torch.from_numpy(x).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(oracle.e4m3_encode(x), ref)
+
+
+def test_blockscale_e4m3out_on_integer_inputs():
+    """Integer codes, unit block scales: the sums are exact integers, known from an
+    integer matmul; c_scale = 1/8 and the result is torch's E4M3 cast of sum/8."""
+    torch = pytest.importorskip("torch")
+    rng = np.random.Generator(np.random.PCG64(32))
+    M, N, K = 6, 20, 256
+    va = rng.integers(-2, 3, size=(M, K))
+    vb = rng.integers(-2, 3, size=(N, K))
+    enc = {v: oracle.e4m3_encode(np.array([v], dtype=np.float32))[0] for v in (-2, -1, 0, 1, 2)}
+    A = np.vectorize(enc.get)(va).astype(np.uint8)
+    B = np.vectorize(enc.get)(vb).astype(np.uint8)
+    sa = np.ones((M, K // 128), np.float32)
+    sb = np.ones(((N + 127) // 128, K // 128), np.float32)
+    codes, y = oracle.blockscale_e4m3out(A, sa, B, sb, 0.125)
+    exact = (va @ vb.T).astype(np.float64) / 8
+    assert np.array_equal(y, exact.astype(np.float32))
+    ref = torch.from_numpy(np.clip(exact, -448, 448).astype(np.float32)).to(torch.float8_e4m3fn).view(torch.uint8)
+    assert np.array_equal(codes, ref.numpy())
