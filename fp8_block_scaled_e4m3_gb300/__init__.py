@@ -30,6 +30,8 @@ _SIGS = {
     "fp8bs_gemm": (_i, [_p, _p, _p, _p, _p, _i, _i, _i, _p]),
     "fp8bs_gemm_tensorscale": (_i, [_p, _p, _p, _i, _i, _i, ctypes.c_float, _p]),
     "fp8bs_gemm_e4m3out": (_i, [_p, _p, _p, _p, _p, ctypes.c_float, _i, _i, _i, _p]),
+    "fp8bs_moe_leaders": (_i, [_p, _i, _i, _i, _p, _p, _p]),
+    "fp8bs_moe_gemm": (_i, [_p, _p, _p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _p]),
     "fp8mx_gemm": (_i, [_p, _p, _p, _p, _p, _i, _i, _i, _p]),
     "fp8mx_gemm_packed": (_i, [_p, _p, _p, _p, _p, _i, _i, _i, _p]),
     "fp8mx_packed_scale_bytes": (_i64, [_i, _i]),
@@ -152,6 +154,51 @@ def gemm_blockscale_e4m3out(A, a_scale, B, b_scale, c_scale, C8=None, stream=Non
                                  _dev_ptr(C8, "C8", (M, N)), float(c_scale), M, N, K, _stream_ptr(stream))
     _check(rc, "fp8bs_gemm_e4m3out")
     return C8
+
+
+MOE_BLOCK_ROWS = 64
+
+
+def moe_leaders(block_expert, num_experts, pair=True, leaders=None, n_leaders=None, stream=None):
+    """Leader descriptor of a sorted block->expert table (int32 [n_blocks], device):
+    returns (leaders int32 [n_blocks], n_leaders int32 [1]), both on the device;
+    leader value = first block | (covers two blocks) << 30. One kernel, no sync."""
+    torch = _torch()
+    n_blocks = int(block_expert.shape[0])
+    if block_expert.dtype != torch.int32:
+        raise TypeError("block_expert must be int32")
+    if leaders is None:
+        leaders = torch.empty((max(n_blocks, 1),), dtype=torch.int32, device=block_expert.device)
+    if n_leaders is None:
+        n_leaders = torch.empty((1,), dtype=torch.int32, device=block_expert.device)
+    rc = _lib.fp8bs_moe_leaders(_dev_ptr(block_expert, "block_expert", (n_blocks,)), n_blocks, int(num_experts),
+                                1 if pair else 0, _dev_ptr(leaders, "leaders", tuple(leaders.shape)),
+                                _dev_ptr(n_leaders, "n_leaders", (1,)), _stream_ptr(stream))
+    _check(rc, "fp8bs_moe_leaders")
+    return leaders, n_leaders
+
+
+def gemm_moe(A, a_scale, B, b_scale, block_expert, leaders, n_leaders, C=None, stream=None):
+    """Grouped MoE blockscale GEMM over sort blocks of 64 rows.
+    A: [64*n_blocks, K] E4M3 (sorted rows); a_scale: fp32 [K/128, a_scale_ld(64*n_blocks)];
+    B: [E, N, K] E4M3; b_scale: fp32 [E, ceil(N/128), K/128]; C: bf16 [64*n_blocks, N]
+    (rows of blocks whose expert is out of range are left as they are)."""
+    torch = _torch()
+    M, K = A.shape
+    E, N, _ = B.shape
+    n_blocks = int(block_expert.shape[0])
+    if M != n_blocks * MOE_BLOCK_ROWS:
+        raise ValueError(f"A has {M} rows, expected {n_blocks} blocks x {MOE_BLOCK_ROWS}")
+    if C is None:
+        C = torch.zeros((M, N), dtype=torch.bfloat16, device=A.device)
+    rc = _lib.fp8bs_moe_gemm(_fp8_ptr(A, "A", (M, K)), _dev_ptr(a_scale, "a_scale", (K // 128, a_scale_ld(M))),
+                             _fp8_ptr(B, "B", (E, N, K)),
+                             _dev_ptr(b_scale, "b_scale", (E, (N + 127) // 128, K // 128)),
+                             _dev_ptr(C, "C", (M, N)), _dev_ptr(block_expert, "block_expert", (n_blocks,)),
+                             _dev_ptr(leaders, "leaders", tuple(leaders.shape)),
+                             _dev_ptr(n_leaders, "n_leaders", (1,)), n_blocks, N, K, E, _stream_ptr(stream))
+    _check(rc, "fp8bs_moe_gemm")
+    return C
 
 
 def gemm_tensorscale(A, B, alpha, C=None, stream=None):

@@ -17,6 +17,9 @@ namespace fp8bs {
 template <int BN, int STAGES>
 cudaError_t launch_blockscale(const CUtensorMap &, const CUtensorMap &, const CUtensorMap &, const CUtensorMap &,
                               const GemmArgs &, int, cudaStream_t);
+template <int BN, int STAGES>
+cudaError_t launch_blockscale_moe(const CUtensorMap &, const CUtensorMap &, const CUtensorMap &, const CUtensorMap &,
+                                  const GemmArgs &, int, cudaStream_t);
 template <int STAGES>
 cudaError_t launch_blockscale_pair(const CUtensorMap &, const CUtensorMap &, const CUtensorMap &, const CUtensorMap &,
                                    const GemmArgs &, int, cudaStream_t);
@@ -448,6 +451,164 @@ int blockscale_gemm(const void *A, const float *a_scale, const void *B, const fl
     return FP8BS_OK;
 }
 
+// MoE leader descriptor (skill card "FlyDSL decode MoE stage-1 blkmap",
+// procedure step 2): for every run of k adjacent sort blocks of one expert,
+// ceil(k/2) leaders, each the first block of a pair (bit 30 set) or a trailing
+// solo block; with pair == 0 every block is its own leader. One CTA scans the
+// table in chunks of 1024 blocks: a max-scan of run starts gives each block's
+// position in its run, an exclusive sum-scan of the leader flags its slot.
+// Blocks whose expert is outside [0, num_experts) are no one's leader.
+constexpr int kScanThreads = 1024;
+
+__device__ __forceinline__ int block_scan_incl(int v, bool is_max, int *s_warp)
+{
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int n = __shfl_up_sync(0xffffffffu, v, o);
+        if (lane >= o)
+            v = is_max ? (n > v ? n : v) : v + n;
+    }
+    if (lane == 31)
+        s_warp[warp] = v;
+    __syncthreads();
+    if (warp == 0) {
+        int w = s_warp[lane];
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int n = __shfl_up_sync(0xffffffffu, w, o);
+            if (lane >= o)
+                w = is_max ? (n > w ? n : w) : w + n;
+        }
+        s_warp[lane] = w;
+    }
+    __syncthreads();
+    if (warp > 0) {
+        const int p = s_warp[warp - 1];
+        v = is_max ? (p > v ? p : v) : v + p;
+    }
+    __syncthreads();   // s_warp is reused by the next scan
+    return v;
+}
+
+__global__ void __launch_bounds__(kScanThreads) moe_leaders_kernel(const int *__restrict__ block_expert, int n_blocks,
+                                                                    int num_experts, int pair,
+                                                                    int *__restrict__ leaders,
+                                                                    int *__restrict__ n_leaders)
+{
+    __shared__ int s_warp[32];
+    __shared__ int s_count, s_start;
+    if (threadIdx.x == 0) {
+        s_count = 0;
+        s_start = 0;
+    }
+    __syncthreads();
+    for (int base = 0; base < n_blocks; base += kScanThreads) {
+        const int b = base + static_cast<int>(threadIdx.x);
+        const bool in = b < n_blocks;
+        const int e = in ? block_expert[b] : -1;
+        const bool starts = in && (b == 0 || block_expert[b - 1] != e);
+        const int carry_start = s_start;
+        const int carry_count = s_count;
+        int run_start = block_scan_incl(starts ? b : -1, true, s_warp);
+        run_start = run_start > carry_start ? run_start : carry_start;
+        const bool valid = in && e >= 0 && e < num_experts;
+        const bool leader = valid && (!pair || ((b - run_start) & 1) == 0);
+        const bool two = leader && pair && b + 1 < n_blocks && block_expert[b + 1] == e;
+        const int incl = block_scan_incl(leader ? 1 : 0, false, s_warp);
+        if (leader)
+            leaders[carry_count + incl - 1] = b | (two ? (1 << 30) : 0);
+        if (threadIdx.x == kScanThreads - 1) {
+            s_count = carry_count + incl;
+            s_start = run_start;
+        }
+        __syncthreads();
+    }
+    if (threadIdx.x == 0)
+        *n_leaders = s_count;
+}
+
+// Grouped blockscale GEMM over the leaders (one-CTA kernel, one CTA per tile).
+int moe_gemm(const void *A, const float *a_scale, const void *B, const float *b_scale, void *C,
+             const int *block_expert, const int *leaders, const int *n_leaders, int n_blocks, int N, int K,
+             int num_experts, void *stream)
+{
+    if (n_blocks < 0 || n_blocks > (1 << 24) || num_experts < 1 || num_experts > (1 << 16))
+        return FP8BS_ERR_SHAPE;
+    const long long M_pad = static_cast<long long>(n_blocks) * kMoeBlockRows;
+    int rc = check_shape(static_cast<int>(M_pad), N, K);
+    if (rc)
+        return rc;
+    if (static_cast<long long>(num_experts) * N >= (1ll << 31))
+        return FP8BS_ERR_SHAPE;
+    if (n_blocks == 0)
+        return FP8BS_OK;
+    if (!A || !a_scale || !B || !b_scale || !C || !block_expert || !leaders || !n_leaders)
+        return FP8BS_ERR_NULL;
+    if (!aligned(A, 16) || !aligned(a_scale, 16) || !aligned(B, 16) || !aligned(b_scale, 4) || !aligned(C, 16) ||
+        !aligned(block_expert, 4) || !aligned(leaders, 4) || !aligned(n_leaders, 4))
+        return FP8BS_ERR_ALIGN;
+    int dev;
+    DeviceState *st;
+    if ((rc = ensure_device(dev, st)))
+        return rc;
+    const int M = static_cast<int>(M_pad);
+    // Tile width: 256, or 128 when even all-paired leaders would leave most SMs idle.
+    Config cfg;
+    cfg.kind = 1;
+    cfg.raster = 0;
+    cfg.sched = 1;
+    cfg.block_n = 256;
+    cfg.stages = 4;
+    if (static_cast<long long>((n_blocks + 1) / 2) * ((N + 255) / 256) * 2 <= st->num_sms) {
+        cfg.block_n = 128;
+        cfg.stages = 6;
+    }
+    if (!override_config(1, 1, cfg) || cfg.sched != 1)
+        return FP8BS_ERR_SHAPE;
+    const int KB = K / 128;
+    const uint64_t ld_sa = static_cast<uint64_t>(fp8bs_a_scale_ld(M));
+    CUtensorMap tmA, tmB, tmSA, tmC;
+    if (!encode_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, A, K, M, K, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, B, K, static_cast<uint64_t>(num_experts) * N, K, 128,
+                   cfg.block_n, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_2d(&tmSA, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, a_scale, ld_sa, KB, ld_sa * 4, 128, 1,
+                   CU_TENSOR_MAP_SWIZZLE_NONE) ||
+        !encode_2d(&tmC, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, C, N, M, static_cast<uint64_t>(N) * 2, kCChunkCols, 32,
+                   CU_TENSOR_MAP_SWIZZLE_64B))
+        return FP8BS_ERR_LAUNCH;
+    GemmArgs args = {};
+    args.M = M;
+    args.N = N;
+    args.K = K;
+    args.raster.m_tiles = (M + kBlockM - 1) / kBlockM;
+    args.raster.n_tiles = (N + cfg.block_n - 1) / cfg.block_n;
+    args.raster.raster = 0;
+    args.raster.group = 1;
+    args.b_scale = b_scale;
+    args.status = st->status_ptr;
+    args.wait_limit_ns = g_wait_limit_ns.load();
+    args.teardown_limit_ns = teardown_limit();
+    args.moe_leaders = leaders;
+    args.moe_n_leaders = n_leaders;
+    args.moe_block_expert = block_expert;
+    args.moe_n_tiles = args.raster.n_tiles;
+    args.moe_n_blocks = n_blocks;
+    args.moe_num_experts = num_experts;
+    // Persistent grid for the worst case (every block a solo leader); CTAs
+    // beyond the device-side tile count find no work.
+    const long long worst = static_cast<long long>(n_blocks) * args.moe_n_tiles;
+    const int grid = worst < st->num_sms ? static_cast<int>(worst) : st->num_sms;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const cudaError_t e = cfg.block_n == 256 ? launch_blockscale_moe<256, 4>(tmA, tmB, tmSA, tmC, args, grid, s)
+                                             : launch_blockscale_moe<128, 6>(tmA, tmB, tmSA, tmC, args, grid, s);
+    if (e != cudaSuccess)
+        return FP8BS_ERR_LAUNCH;
+    t_last_config = config_id(cfg);
+    return FP8BS_OK;
+}
+
 } // namespace host
 } // namespace fp8bs
 
@@ -492,6 +653,34 @@ int fp8mx_gemm_packed(const void *A, const uint8_t *a_sf, const void *B, const u
         return rc;
     t_last_config = config_id(cfg);
     return FP8BS_OK;
+}
+
+int fp8bs_moe_leaders(const int *block_expert, int n_blocks, int num_experts, int pair, int *leaders,
+                      int *n_leaders, void *stream)
+{
+    if (n_blocks < 0 || n_blocks > (1 << 24) || num_experts < 1)
+        return FP8BS_ERR_SHAPE;
+    if (!n_leaders || (n_blocks > 0 && (!block_expert || !leaders)))
+        return FP8BS_ERR_NULL;
+    if (!aligned(n_leaders, 4) || !aligned(block_expert, 4) || !aligned(leaders, 4))
+        return FP8BS_ERR_ALIGN;
+    int dev;
+    DeviceState *st;
+    int rc;
+    if ((rc = ensure_device(dev, st)))
+        return rc;
+    moe_leaders_kernel<<<1, kScanThreads, 0, static_cast<cudaStream_t>(stream)>>>(block_expert, n_blocks,
+                                                                                  num_experts, pair ? 1 : 0,
+                                                                                  leaders, n_leaders);
+    return cudaGetLastError() == cudaSuccess ? FP8BS_OK : FP8BS_ERR_LAUNCH;
+}
+
+int fp8bs_moe_gemm(const void *A, const float *a_scale, const void *B, const float *b_scale, void *C,
+                   const int *block_expert, const int *leaders, const int *n_leaders, int n_blocks, int N, int K,
+                   int num_experts, void *stream)
+{
+    return moe_gemm(A, a_scale, B, b_scale, C, block_expert, leaders, n_leaders, n_blocks, N, K, num_experts,
+                    stream);
 }
 
 int fp8bs_gemm_tensorscale(const void *A, const void *B, void *C, int M, int N, int K, float alpha, void *stream)

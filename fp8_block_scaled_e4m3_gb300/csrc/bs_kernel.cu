@@ -85,7 +85,7 @@ struct BsLayout {
     static_assert(BN == 128 || BN == 256, "tile width");
 };
 
-template <int BN, int STAGES>
+template <int BN, int STAGES, bool MOE>
 __global__ void __launch_bounds__(kBsThreads, 1)
     fp8bs_blockscale_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                             const __grid_constant__ CUtensorMap tmSA, const __grid_constant__ CUtensorMap tmC,
@@ -100,6 +100,9 @@ __global__ void __launch_bounds__(kBsThreads, 1)
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int KB = args.K / kBlockK;
+    // Grouped mode: the leader count is device data (graph-safe), read by every role.
+    const int n_leaders = MOE ? moe_leader_count(args) : 1;
+    const int tiles = MOE ? n_leaders * args.moe_n_tiles : args.raster.num_tiles();
 
     auto full_bar = [&](int s) { return sbase + L::OFF_BAR + 8u * s; };
     auto empty_bar = [&](int s) { return sbase + L::OFF_BAR + 8u * (STAGES + s); };
@@ -153,13 +156,14 @@ __global__ void __launch_bounds__(kBsThreads, 1)
             ptx::prefetch_tmap(&tmB);
             ptx::prefetch_tmap(&tmSA);
             WorkSpan span;
-            span.init(args, KB);
+            span.init(args, KB, tiles);
             int it = 0;
-            int t, kb, mb = 0, nb = 0;
+            int t, kb;
+            TileGeo geo = {};
             span.step(0, t, kb);
             for (; it < span.total; ++it, span.advance(it, t, kb)) {
                 if (it == 0 || kb == 0 || it == span.dp_steps)   // a new tile (a stream-K range may start mid-tile)
-                    args.raster.coords(t, mb, nb);
+                    geo = tile_geo<MOE>(args, t, BN, n_leaders);
                 if ((it & 1) != par)
                     continue;
                 const int s = it % STAGES;
@@ -170,10 +174,10 @@ __global__ void __launch_bounds__(kBsThreads, 1)
                     !wait_bounded(sa_empty_bar(a), aph ^ 1, abort_flag, args))
                     break;
                 ptx::mbar_arrive_expect_tx(full_bar(s), L::A_BYTES + L::B_BYTES);
-                ptx::tma_load_2d(sbase + L::OFF_A + s * L::A_BYTES, &tmA, full_bar(s), kb * kBlockK, mb * kBlockM);
-                ptx::tma_load_2d(sbase + L::OFF_B + s * L::B_BYTES, &tmB, full_bar(s), kb * kBlockK, nb * BN);
+                ptx::tma_load_2d(sbase + L::OFF_A + s * L::A_BYTES, &tmA, full_bar(s), kb * kBlockK, geo.a_row);
+                ptx::tma_load_2d(sbase + L::OFF_B + s * L::B_BYTES, &tmB, full_bar(s), kb * kBlockK, geo.b_row);
                 ptx::mbar_arrive_expect_tx(sa_full_bar(a), L::SA_BYTES);
-                ptx::tma_load_2d(sbase + L::OFF_SA + a * L::SA_BYTES, &tmSA, sa_full_bar(a), mb * kBlockM, kb);
+                ptx::tma_load_2d(sbase + L::OFF_SA + a * L::SA_BYTES, &tmSA, sa_full_bar(a), geo.a_row, kb);
             }
             // Every load issued must have landed before the CTA exits.
             for (int s = par; s < STAGES; s += 2) {
@@ -201,7 +205,7 @@ __global__ void __launch_bounds__(kBsThreads, 1)
             constexpr int SUBN = BN / L::NSUB;
             constexpr uint32_t idesc = ptx::idesc_f8f6f4_e4m3(kBlockM, SUBN);
             WorkSpan span;
-            span.init(args, KB);
+            span.init(args, KB, tiles);
             for (int it = par; it < span.total; it += 2) {
                 const int s = it % STAGES;
                 const uint32_t ph = (it / STAGES) & 1;
@@ -252,7 +256,7 @@ __global__ void __launch_bounds__(kBsThreads, 1)
         const int NB = (args.N + 127) / 128;
         const uint32_t cstage = sbase + L::OFF_C + ew * kCStageBytes;
         WorkSpan span;
-        span.init(args, KB);
+        span.init(args, KB, tiles);
         const int total = span.total;
 
         // b_scale of flattened step g for the 128-column N block of this thread's
@@ -263,11 +267,13 @@ __global__ void __launch_bounds__(kBsThreads, 1)
         auto sb_lane_load = [&](int g) -> float {
             if (g >= total)
                 return 0.f;
-            int t, kb, mb, nb;
+            int t, kb;
             span.step(g, t, kb);
-            args.raster.coords(t, mb, nb);
-            const int nblk = (nb * BN + wg * HALF) >> 7;
-            return nblk < NB ? ptx::ldg_nc_f32(args.b_scale + static_cast<size_t>(nblk) * KB + kb) : 0.f;
+            const TileGeo gg = tile_geo<MOE>(args, t, BN, n_leaders);
+            const int nblk = (gg.nb * BN + wg * HALF) >> 7;
+            // grouped mode: b_scale is [expert][ceil(N/128)][K/128]
+            return nblk < NB ? ptx::ldg_nc_f32(args.b_scale + (static_cast<size_t>(gg.expert) * NB + nblk) * KB + kb)
+                             : 0.f;
         };
         float sb_cur = sb_lane_load(lane);
         float sb_next = sb_lane_load(32 + lane);
@@ -353,10 +359,9 @@ __global__ void __launch_bounds__(kBsThreads, 1)
             }
             if (!ok)
                 break;
-            int t, kb0, mb, nb, kb_last;
+            int t, kb0, kb_last, scratch;
             span.step(seg_start, t, kb0);
-            span.step(seg_end - 1, mb, kb_last);   // mb: scratch
-            args.raster.coords(t, mb, nb);
+            span.step(seg_end - 1, scratch, kb_last);
             // Stream-K hand-off, warp by warp: warp ew of every CTA owns the same
             // 32 rows x HALF columns of a tile, in slot layout [column/4][row].
             const size_t slice = static_cast<size_t>(wg * HALF / 4) * kBlockM + static_cast<size_t>(row);
@@ -383,7 +388,7 @@ __global__ void __launch_bounds__(kBsThreads, 1)
                 // The other CTAs of the tile: up to the one whose range holds the
                 // tile's last unit, the largest c with floor(c * U / G) <= unit.
                 const long long G = gridDim.x;
-                const long long U = static_cast<long long>(args.raster.num_tiles() - span.tile0) * KB;
+                const long long U = static_cast<long long>(tiles - span.tile0) * KB;
                 const long long tile_end = static_cast<long long>(t + 1 - span.tile0) * KB;
                 const int c_last = static_cast<int>((tile_end * G - 1) / U);
                 for (int c2 = static_cast<int>(blockIdx.x) + 1; c2 <= c_last; ++c2) {
@@ -408,9 +413,13 @@ __global__ void __launch_bounds__(kBsThreads, 1)
                 if (!ok)
                     break;
             }
-            const int x0 = nb * BN + wg * HALF;
-            const int y0 = mb * kBlockM + q * 32;
-            if (args.c_e4m3) {
+            const TileGeo geo = tile_geo<MOE>(args, t, BN, n_leaders);
+            const int x0 = geo.nb * BN + wg * HALF;
+            const int y0 = geo.a_row + q * 32;
+            if (MOE && q * 32 >= geo.rows) {
+                // Solo leader: rows 64..127 of the tile are the next sort block's
+                // (another expert's): computed, never stored.
+            } else if (args.c_e4m3) {
 #pragma unroll
                 for (int c = 0; c < HALF / 64; ++c)
                     store_c8_chunk(&tmC, cstage, lane, acc + c * 64, args.c_scale, x0 + c * 64, y0, args.M, args.N);
@@ -434,12 +443,12 @@ __global__ void __launch_bounds__(kBsThreads, 1)
 }
 
 // Launch helpers called by the host API (api.cu).
-template <int BN, int STAGES>
-cudaError_t launch_blockscale(const CUtensorMap &tmA, const CUtensorMap &tmB, const CUtensorMap &tmSA,
-                              const CUtensorMap &tmC, const GemmArgs &args, int grid, cudaStream_t stream)
+template <int BN, int STAGES, bool MOE>
+cudaError_t launch_blockscale_any(const CUtensorMap &tmA, const CUtensorMap &tmB, const CUtensorMap &tmSA,
+                                  const CUtensorMap &tmC, const GemmArgs &args, int grid, cudaStream_t stream)
 {
     using L = BsLayout<BN, STAGES>;
-    auto kern = fp8bs_blockscale_kernel<BN, STAGES>;
+    auto kern = fp8bs_blockscale_kernel<BN, STAGES, MOE>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::DYN_SMEM);
     if (e != cudaSuccess)
         return e;
@@ -451,9 +460,27 @@ cudaError_t launch_blockscale(const CUtensorMap &tmA, const CUtensorMap &tmB, co
     return cudaLaunchKernelEx(&cfg, kern, tmA, tmB, tmSA, tmC, args);
 }
 
+template <int BN, int STAGES>
+cudaError_t launch_blockscale(const CUtensorMap &tmA, const CUtensorMap &tmB, const CUtensorMap &tmSA,
+                              const CUtensorMap &tmC, const GemmArgs &args, int grid, cudaStream_t stream)
+{
+    return launch_blockscale_any<BN, STAGES, false>(tmA, tmB, tmSA, tmC, args, grid, stream);
+}
+
+template <int BN, int STAGES>
+cudaError_t launch_blockscale_moe(const CUtensorMap &tmA, const CUtensorMap &tmB, const CUtensorMap &tmSA,
+                                  const CUtensorMap &tmC, const GemmArgs &args, int grid, cudaStream_t stream)
+{
+    return launch_blockscale_any<BN, STAGES, true>(tmA, tmB, tmSA, tmC, args, grid, stream);
+}
+
 template cudaError_t launch_blockscale<256, 4>(const CUtensorMap &, const CUtensorMap &, const CUtensorMap &,
                                                const CUtensorMap &, const GemmArgs &, int, cudaStream_t);
 template cudaError_t launch_blockscale<128, 6>(const CUtensorMap &, const CUtensorMap &, const CUtensorMap &,
                                                const CUtensorMap &, const GemmArgs &, int, cudaStream_t);
+template cudaError_t launch_blockscale_moe<256, 4>(const CUtensorMap &, const CUtensorMap &, const CUtensorMap &,
+                                                   const CUtensorMap &, const GemmArgs &, int, cudaStream_t);
+template cudaError_t launch_blockscale_moe<128, 6>(const CUtensorMap &, const CUtensorMap &, const CUtensorMap &,
+                                                   const CUtensorMap &, const GemmArgs &, int, cudaStream_t);
 
 } // namespace fp8bs

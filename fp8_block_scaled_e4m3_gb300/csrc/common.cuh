@@ -67,7 +67,65 @@ struct GemmArgs {
     unsigned long long sk_token;      // unique per call; a finisher resets the flag to 0
     int sk;
     int sk_dp;                        // stream-K: whole waves of tiles done one per CTA first
+    // Grouped (MoE) blockscale GEMM: rows of A and C are sort blocks of
+    // kMoeBlockRows rows, each owned by one expert; a tile is a leader (one or
+    // two adjacent sort blocks of the same expert) x one N tile of that
+    // expert's B. Tile t = nb * n_leaders + leader, so the leaders of one
+    // expert, which are adjacent, run side by side on the same B tile.
+    const int *moe_leaders;           // [n_blocks]: first block | (covers two blocks) << 30
+    const int *moe_n_leaders;         // device-side count (written by the descriptor kernel)
+    const int *moe_block_expert;      // [n_blocks]: expert of each sort block
+    int moe_n_tiles;                  // N tiles per leader
+    int moe_n_blocks;                 // sort blocks; device values are clamped to the launch's
+    int moe_num_experts;              // bounds, so a malformed descriptor cannot index out of range
 };
+
+constexpr int kMoeBlockRows = 64;     // MoE sort-block granularity (rows)
+
+// Where tile t sits: first rows of A/C and of B, its N tile, the expert (for
+// the b_scale rows) and how many of its 128 rows are stored.
+struct TileGeo {
+    int a_row, b_row, nb, expert, rows;
+};
+
+__device__ __forceinline__ int moe_leader_count(const GemmArgs &a)
+{
+    return min(max(__ldg(a.moe_n_leaders), 0), a.moe_n_blocks);
+}
+
+template <bool MOE>
+__device__ __forceinline__ TileGeo tile_geo(const GemmArgs &a, int t, int BN, int n_leaders)
+{
+    TileGeo g;
+    if constexpr (MOE) {
+        const int li = t % n_leaders;
+        g.nb = t / n_leaders;
+        const int v = __ldg(a.moe_leaders + li);
+        const int b0 = min(v & 0x3FFFFFFF, a.moe_n_blocks - 1);
+        g.expert = min(max(__ldg(a.moe_block_expert + b0), 0), a.moe_num_experts - 1);
+        g.a_row = b0 * kMoeBlockRows;
+        g.b_row = g.expert * a.N + g.nb * BN;
+        g.rows = (v >> 30) & 1 ? 2 * kMoeBlockRows : kMoeBlockRows;
+    } else {
+        int mb;
+        a.raster.coords(t, mb, g.nb);
+        g.a_row = mb * kBlockM;
+        g.b_row = g.nb * BN;
+        g.expert = 0;
+        g.rows = kBlockM;
+    }
+    return g;
+}
+
+// Tiles of a launch: the raster's, or leaders x N tiles in the grouped mode.
+template <bool MOE>
+__device__ __forceinline__ int launch_tiles(const GemmArgs &a)
+{
+    if constexpr (MOE)
+        return moe_leader_count(a) * a.moe_n_tiles;
+    else
+        return a.raster.num_tiles();
+}
 
 // The work of one CTA as flattened steps g = 0 .. total-1, step g being K block
 // kb of tile t (tile order of TileRaster).
@@ -92,12 +150,13 @@ struct WorkSpan {
         return static_cast<int>((static_cast<long long>(c) * U) / G);
     }
 
-    __device__ __forceinline__ void init(const GemmArgs &a, int KB_)
+    __device__ __forceinline__ void init(const GemmArgs &a, int KB_) { init(a, KB_, a.raster.num_tiles()); }
+
+    __device__ __forceinline__ void init(const GemmArgs &a, int KB_, int tiles)
     {
         KB = KB_;
         const int c = static_cast<int>(blockIdx.x);
         const int G = static_cast<int>(gridDim.x);
-        const int tiles = a.raster.num_tiles();
         if (a.sk) {
             dp_steps = a.sk_dp * KB;
             tile0 = a.sk_dp * G;

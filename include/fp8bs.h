@@ -147,6 +147,47 @@ int fp8mx_gemm_packed(const void *A, const uint8_t *a_sf, const void *B, const u
 int fp8bs_gemm_tensorscale(const void *A, const void *B, void *C, int M, int N, int K, float alpha,
                            void *stream);
 
+/*
+ * Grouped MoE stage-1 (gate+up) blockscale GEMM with paired same-expert sort
+ * blocks (skill card "FlyDSL decode MoE stage-1 blkmap", sections "Mechanism"
+ * and "Procedure" steps 2-5).
+ *
+ * Layout. The routed token rows are sorted by expert and each expert's rows are
+ * padded up to whole sort blocks of FP8BS_MOE_BLOCK_ROWS (64) rows, as the MoE
+ * align/sort step produces them: n_blocks blocks, M = 64 * n_blocks rows.
+ *   block_expert  int32 [n_blocks], device: the expert of each block. Blocks of
+ *                 one expert are adjacent. A value outside [0, num_experts)
+ *                 (e.g. -1 for unused blocks) marks a block that is not
+ *                 computed and whose C rows are left as they are.
+ *   A, a_scale    the sorted rows, as fp8bs_gemm with M = 64 * n_blocks.
+ *   B             E4M3 [num_experts][N][K], 16-byte aligned.
+ *   b_scale       fp32 [num_experts][ceil(N/128)][K/128].
+ *   C             bf16 [M][N]: row r of block b is
+ *                 fp8bs_gemm(A[r], a_scale[r], B[block_expert[b]], b_scale[block_expert[b]]).
+ *
+ * fp8bs_moe_leaders writes the leader descriptor, one kernel, device-side and
+ * graph-safe (no host synchronisation): for every run of k adjacent blocks of
+ * one expert, ceil(k/2) leaders, each the first block of a pair (value b |
+ * 1 << 30) or a trailing solo block (value b); with pair == 0 every block is a
+ * solo leader (the unpaired arm). leaders: int32 [n_blocks] capacity;
+ * n_leaders: one int32, the count. Errors: FP8BS_ERR_SHAPE (n_blocks < 0 or
+ * > 2^24, num_experts < 1), FP8BS_ERR_NULL, FP8BS_ERR_ALIGN.
+ *
+ * fp8bs_moe_gemm computes C from the descriptor (which must come from
+ * fp8bs_moe_leaders for the same block_expert): one 128-row compute tile per
+ * leader and N tile, so a pair streams its expert's B tile once for both
+ * blocks; a solo leader's second 64 rows belong to the next block and are not
+ * stored. One kernel, a persistent grid sized for n_blocks solo leaders that
+ * reads the leader count on the device. Shape rules as fp8bs_gemm for
+ * (64 * n_blocks, N, K), num_experts * N < 2^31; n_blocks = 0 is a no-op.
+ */
+#define FP8BS_MOE_BLOCK_ROWS 64
+int fp8bs_moe_leaders(const int *block_expert, int n_blocks, int num_experts, int pair, int *leaders,
+                      int *n_leaders, void *stream);
+int fp8bs_moe_gemm(const void *A, const float *a_scale, const void *B, const float *b_scale, void *C,
+                   const int *block_expert, const int *leaders, const int *n_leaders, int n_blocks, int N,
+                   int K, int num_experts, void *stream);
+
 /* Size in bytes of the packed scale layout of a [rows][K/32] ue8m0 tensor:
  * ceil(rows/128) * (K/128) * 512. Negative (FP8BS_ERR_SHAPE) for bad shapes. */
 int64_t fp8mx_packed_scale_bytes(int rows, int K);

@@ -163,6 +163,52 @@ def blockscale_e4m3out(A, a_scale, B, b_scale, c_scale, rows=None):
     return e4m3_encode(y), y
 
 
+def moe_leaders(block_expert, num_experts, pair=True) -> np.ndarray:
+    """Leader descriptor of a sorted block -> expert table (skill card "FlyDSL
+    decode MoE stage-1 blkmap", procedure step 2): for every run of k adjacent
+    blocks of one expert, ceil(k/2) leaders, each the first block of a pair
+    (value b | 1 << 30) or a trailing solo block (value b); without pairing,
+    every block leads itself. Blocks whose expert is outside [0, num_experts)
+    lead nothing. Walks the table run by run."""
+    be = [int(v) for v in block_expert]
+    out = []
+    b = 0
+    while b < len(be):
+        r = b
+        while r < len(be) and be[r] == be[b]:
+            r += 1
+        if 0 <= be[b] < num_experts:
+            k = r - b
+            if pair:
+                out.extend((b + i) | ((1 << 30) if i + 1 < k else 0) for i in range(0, k, 2))
+            else:
+                out.extend(range(b, r))
+        b = r
+    return np.array(out, dtype=np.int32)
+
+
+def moe_gemm(A, a_scale, B, b_scale, block_expert, num_experts, block_rows=64):
+    """Grouped blockscale GEMM by its definition: every row of a sort block of
+    expert e is the blockscale GEMM of that row with B[e], b_scale[e] (a_scale
+    logical [M, K/128], B [E, N, K], b_scale [E, ceil(N/128), K/128]). Returns
+    (C bf16 bits [M, N], mask of the rows that are defined: blocks with an
+    expert in range)."""
+    M, K = A.shape
+    N = B.shape[1]
+    be = np.asarray(block_expert)
+    C = np.zeros((M, N), dtype=np.uint16)
+    defined = np.zeros(M, dtype=bool)
+    for e in range(num_experts):
+        blocks = np.nonzero(be == e)[0]
+        if len(blocks) == 0:
+            continue
+        rows = (blocks[:, None] * block_rows + np.arange(block_rows)[None, :]).ravel()
+        C[rows] = blockscale(np.ascontiguousarray(A[rows]), np.ascontiguousarray(a_scale[rows]),
+                             np.ascontiguousarray(B[e]), np.ascontiguousarray(b_scale[e]))
+        defined[rows] = True
+    return C, defined
+
+
 def blockscale_blockpartial(A, a_scale, B, b_scale, rows=None, exact=False):
     M, K = A.shape
     N = B.shape[0]

@@ -585,3 +585,103 @@ def test_e4m3out_feeds_the_next_gemm_with_one_scale():
     sa2 = np.full((M, N1 // 128), np.float32(1.0 / s), dtype=np.float32)
     got = run_blockscale(c8, sa2, z.B, z.b_scale)
     compare(got, oracle.blockscale(codes, sa2, z.B, z.b_scale), "E4M3 C as the next A")
+
+
+# ------------------------------------------------ grouped MoE stage-1 GEMM
+def _moe_dev(x):
+    return (to_dev(x.A), to_dev(workloads.a_scale_to_kmajor(x.a_scale)), to_dev(x.B), to_dev(x.b_scale),
+            to_dev(x.block_expert))
+
+
+@pytest.mark.parametrize("pair", [True, False])
+@pytest.mark.parametrize("case", ["empty", "one", "mixed", "chunks", "long_run"])
+def test_moe_leaders_kernel_matches_oracle(pair, case):
+    import torch
+    import fp8_block_scaled_e4m3_gb300 as f
+    rng = np.random.Generator(np.random.PCG64(7))
+    E = 16
+    if case == "empty":
+        table = np.zeros(0, np.int32)
+    elif case == "one":
+        table = np.array([3], np.int32)
+    elif case == "mixed":
+        table = np.repeat(np.sort(rng.choice(np.arange(-1, E + 2), 40)), rng.integers(1, 6, 40)).astype(np.int32)
+    elif case == "chunks":   # runs that straddle the 1024-block chunks of the scan
+        table = np.repeat(np.arange(E), rng.integers(150, 260, E)).astype(np.int32)
+    else:                    # one run of 2501 blocks, then others
+        table = np.concatenate([np.full(2501, 2), np.full(3, 5), np.full(1030, 7), [-1, -1]]).astype(np.int32)
+    be = torch.from_numpy(table).cuda() if len(table) else torch.zeros(0, dtype=torch.int32, device="cuda")
+    lead, n = f.moe_leaders(be, E, pair=pair)
+    torch.cuda.synchronize()
+    want = oracle.moe_leaders(table, E, pair=pair)
+    assert int(n.item()) == len(want)
+    assert np.array_equal(lead.cpu().numpy()[:len(want)], want)
+
+
+@pytest.mark.parametrize("pair", [True, False])
+@pytest.mark.parametrize("cid", [0, 1256401, 1128601])
+def test_moe_gemm_matches_oracle(override, pair, cid):
+    """Skewed routing (runs of 1..many blocks: pairs and solo tails), an unused
+    block, both tile widths; rows of the unused block keep their sentinel."""
+    import torch
+    import fp8_block_scaled_e4m3_gb300 as f
+    if cid:
+        override(cid)
+    x = workloads.make_moe_inputs(512, 2, 8, 384, 512, seed=11, skew=1.2)
+    x.block_expert[-1] = -1                       # the last block is unused
+    A, sa, B, sb, be = _moe_dev(x)
+    lead, n = f.moe_leaders(be, 8, pair=pair)
+    C = torch.full((x.A.shape[0], 384), float("nan"), dtype=torch.bfloat16, device="cuda")
+    f.gemm_moe(A, sa, B, sb, be, lead, n, C=C)
+    assert f.get_status() == 0
+    got = C.view(torch.int16).cpu().numpy().view(np.uint16)
+    want, defined = oracle.moe_gemm(x.A, x.a_scale, x.B, x.b_scale, x.block_expert, 8)
+    assert not defined.all() and np.all(got[~defined] == got[~defined][0])   # untouched sentinel rows
+    assert np.isnan(oracle.bf16_bits_to_float(got[~defined])).all()
+    compare(got[defined], want[defined], f"moe pair={pair} cid={cid}")
+
+
+def test_moe_gemm_graph_replay_with_new_routing():
+    """Descriptor + GEMM captured once in a CUDA graph; replays after the
+    block -> expert table changes in place give the new routing's result."""
+    import torch
+    import fp8_block_scaled_e4m3_gb300 as f
+    x = workloads.make_moe_inputs(512, 2, 8, 256, 512, seed=12, skew=0.8)
+    A, sa, B, sb, be = _moe_dev(x)
+    lead = torch.empty(x.n_blocks, dtype=torch.int32, device="cuda")
+    n = torch.empty(1, dtype=torch.int32, device="cuda")
+    C = torch.empty((x.A.shape[0], 256), dtype=torch.bfloat16, device="cuda")
+    f.moe_leaders(be, 8, leaders=lead, n_leaders=n)
+    f.gemm_moe(A, sa, B, sb, be, lead, n, C=C)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        f.moe_leaders(be, 8, leaders=lead, n_leaders=n)
+        f.gemm_moe(A, sa, B, sb, be, lead, n, C=C)
+    for table in (7 - x.block_expert, x.block_expert):
+        be.copy_(torch.from_numpy(np.ascontiguousarray(table, dtype=np.int32)).cuda())
+        g.replay()
+        assert f.get_status() == 0
+        got = C.view(torch.int16).cpu().numpy().view(np.uint16)
+        want, _ = oracle.moe_gemm(x.A, x.a_scale, x.B, x.b_scale, table, 8)
+        compare(got, want, "moe graph replay")
+    del g
+
+
+def test_moe_gemm_layer_sized_sampled_blocks():
+    """1024 tokens, top-8 of 32 experts, N = 1536, K = 2048: every row of a
+    sample of sort blocks against the oracle."""
+    import torch
+    import fp8_block_scaled_e4m3_gb300 as f
+    x = workloads.make_moe_inputs(1024, 8, 32, 1536, 2048, seed=13, skew=0.5)
+    A, sa, B, sb, be = _moe_dev(x)
+    lead, n = f.moe_leaders(be, 32)
+    C = f.gemm_moe(A, sa, B, sb, be, lead, n)
+    assert f.get_status() == 0
+    got = C.view(torch.int16).cpu().numpy().view(np.uint16)
+    rng = np.random.Generator(np.random.PCG64(14))
+    for b in rng.choice(x.n_blocks, 6, replace=False):
+        e = int(x.block_expert[b])
+        rows = slice(64 * b, 64 * b + 64)
+        want = oracle.blockscale(x.A[rows], x.a_scale[rows], x.B[e], x.b_scale[e])
+        compare(got[rows], want, f"moe block {b}")

@@ -393,3 +393,72 @@ def test_blockscale_e4m3out_on_integer_inputs():
     assert np.array_equal(y, exact.astype(np.float32))
     ref = torch.from_numpy(np.clip(exact, -448, 448).astype(np.float32)).to(torch.float8_e4m3fn).view(torch.uint8)
     assert np.array_equal(codes, ref.numpy())
+
+
+# ---- grouped MoE stage-1 (skill card "FlyDSL decode MoE stage-1 blkmap")
+
+P30 = 1 << 30
+
+
+def test_moe_leaders_worked_example():
+    """Runs of 3, 1, 2, (unused), 4 blocks: ceil(k/2) leaders per run, pairs
+    first, a trailing odd block solo (procedure step 2); the count is the valid
+    blocks minus the pairs (procedure step 3)."""
+    table = [0, 0, 0, 1, 2, 2, -1, 3, 3, 3, 3]
+    assert oracle.moe_leaders(table, 4, pair=True).tolist() == [0 | P30, 2, 3, 4 | P30, 7 | P30, 9 | P30]
+    assert oracle.moe_leaders(table, 4, pair=False).tolist() == [0, 1, 2, 3, 4, 5, 7, 8, 9, 10]
+    # an expert id past the expert count leads nothing
+    assert oracle.moe_leaders([0, 5, 5, 1], 4, pair=True).tolist() == [0, 3]
+    assert oracle.moe_leaders([], 4).tolist() == []
+
+
+def test_moe_leaders_cover_every_valid_block_once():
+    rng = np.random.Generator(np.random.PCG64(41))
+    for _ in range(50):
+        E = int(rng.integers(1, 9))
+        runs = rng.integers(1, 6, size=int(rng.integers(1, 12)))
+        experts = np.sort(rng.choice(np.arange(-1, E + 1), size=len(runs)))
+        table = np.repeat(experts, runs)
+        lead = oracle.moe_leaders(table, E, pair=True)
+        covered = []
+        for v in lead.tolist():
+            b, two = v & (P30 - 1), bool(v & P30)
+            covered.append(b)
+            if two:
+                assert table[b + 1] == table[b]
+                covered.append(b + 1)
+        valid = [b for b in range(len(table)) if 0 <= table[b] < E]
+        assert sorted(covered) == valid
+        pairs = sum(1 for v in lead.tolist() if v & P30)
+        assert len(lead) == len(valid) - pairs
+
+
+def test_moe_gemm_oracle_reduces_to_the_dense_gemm():
+    """One expert owning every block is the dense blockscale GEMM; E identical
+    experts under any block map give the same rows; unused blocks are undefined."""
+    x = workloads.make_moe_inputs(192, 2, 4, 256, 256, seed=3)
+    M = x.A.shape[0]
+    dense = oracle.blockscale(x.A, x.a_scale, x.B[0], x.b_scale[0])
+    one = np.zeros(x.n_blocks, np.int32)
+    C, d = oracle.moe_gemm(x.A, x.a_scale, x.B, x.b_scale, one, 4)
+    assert d.all() and np.array_equal(C, dense)
+    Bsame = np.repeat(x.B[:1], 4, axis=0)
+    sbsame = np.repeat(x.b_scale[:1], 4, axis=0)
+    C2, d2 = oracle.moe_gemm(x.A, x.a_scale, Bsame, sbsame, x.block_expert, 4)
+    assert d2.all() and np.array_equal(C2, dense)
+    partial = x.block_expert.copy()
+    partial[-1] = -1
+    C3, d3 = oracle.moe_gemm(x.A, x.a_scale, x.B, x.b_scale, partial, 4)
+    assert not d3[M - 64:].any() and d3[:M - 64].all()
+
+
+def test_moe_routing_layout():
+    x = workloads.make_moe_inputs(300, 3, 8, 128, 256, seed=4, skew=1.0)
+    assert x.A.shape[0] == 64 * x.n_blocks and np.all(np.diff(x.block_expert) >= 0)
+    real = x.row_token >= 0
+    assert real.sum() == 300 * 3                      # every (token, slot) routed once
+    for b in range(x.n_blocks):                        # padding only at the end of an expert's rows
+        rows = x.row_token[64 * b:64 * b + 64]
+        if (rows < 0).any():
+            assert np.all(rows[np.argmax(rows < 0):] < 0)
+    assert np.all(x.A[~real] == 0)

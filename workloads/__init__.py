@@ -203,6 +203,68 @@ def make_tensorscale_inputs(M: int, N: int, K: int, seed: int = 0, b_std: float 
     return TensorscaleInputs(M, N, K, seed, A, B, np.float32(sa * sb))
 
 
+@dataclass
+class MoeInputs:
+    tokens: int
+    top_k: int
+    num_experts: int
+    N: int
+    K: int
+    seed: int
+    A: np.ndarray             # uint8 [64 * n_blocks, K]: routed rows sorted by expert, padded per expert
+    a_scale: np.ndarray       # fp32 [64 * n_blocks, K/128] (padding rows: zeros with scale 1)
+    B: np.ndarray             # uint8 [E, N, K]
+    b_scale: np.ndarray       # fp32 [E, N/128, K/128]
+    block_expert: np.ndarray  # int32 [n_blocks]
+    row_token: np.ndarray     # int32 [64 * n_blocks]: source token of each row, -1 for padding
+
+    @property
+    def n_blocks(self) -> int:
+        return int(self.block_expert.shape[0])
+
+
+MOE_BLOCK_ROWS = 64
+
+
+def make_moe_inputs(tokens: int, top_k: int, num_experts: int, N: int, K: int, seed: int = 0,
+                    skew: float = 0.0, b_std: float = 0.02) -> MoeInputs:
+    """Synthetic MoE stage-1 routing and operands. Each token picks top_k
+    distinct experts with probability proportional to (e + 1)^-skew (0 =
+    uniform); rows are grouped by expert in token order and each expert's count
+    is padded up to whole sort blocks of 64 rows, the layout the MoE align/sort
+    step produces. Token activations N(0,1) are quantised per (token, 128-wide K
+    block) and gathered; the expert weights N(0, b_std) are quantised per 128x128
+    block (N a multiple of 128, so no block spans two experts)."""
+    assert N % BLOCK_K == 0 and K % BLOCK_K == 0 and top_k <= num_experts
+    rng = np.random.Generator(np.random.PCG64(seed))
+    p = (np.arange(num_experts) + 1.0) ** (-skew)
+    p /= p.sum()
+    choice = np.stack([rng.choice(num_experts, size=top_k, replace=False, p=p) for _ in range(tokens)])
+    x = rng.standard_normal((tokens, K), dtype=np.float32)
+    codes, scales = quantise_blockscale_a(x)
+    del x
+    w = rng.standard_normal((num_experts * N, K), dtype=np.float32) * np.float32(b_std)
+    B, sb = quantise_blockscale_b(w)
+    del w
+    row_token, block_expert = [], []
+    for e in range(num_experts):
+        toks = np.nonzero((choice == e).any(axis=1))[0]
+        nb = -(-len(toks) // MOE_BLOCK_ROWS)
+        pad = nb * MOE_BLOCK_ROWS - len(toks)
+        row_token.extend(toks.tolist() + [-1] * pad)
+        block_expert.extend([e] * nb)
+    row_token = np.array(row_token, dtype=np.int32)
+    real = row_token >= 0
+    A = np.zeros((len(row_token), K), dtype=np.uint8)
+    a_scale = np.ones((len(row_token), K // BLOCK_K), dtype=np.float32)
+    A[real] = codes[row_token[real]]
+    a_scale[real] = scales[row_token[real]]
+    return MoeInputs(tokens, top_k, num_experts, N, K, seed, A, a_scale,
+                     np.ascontiguousarray(B.reshape(num_experts, N, K)),
+                     np.ascontiguousarray(sb.reshape(num_experts, N // BLOCK_K, K // BLOCK_K)),
+                     np.array(block_expert, dtype=np.int32), row_token)
+
+
 def make_mxfp8_inputs(M: int, N: int, K: int, seed: int = 0) -> MxInputs:
     rng = np.random.Generator(np.random.PCG64(seed))
     a = rng.standard_normal((M, K), dtype=np.float32)
