@@ -477,11 +477,220 @@ def measure_e2e(args, torch, f, kind, M, N, K, host, gemm):
             "pipeline": "uploads, GEMMs and downloads of consecutive steps on three streams"}
 
 
+# ------------------------------------------------------------ grouped MoE stage-1
+def moe_stats(block_expert, num_experts):
+    be = np.asarray(block_expert)
+    runs = np.diff(np.flatnonzero(np.r_[True, be[1:] != be[:-1], True])) if len(be) else np.zeros(0, int)
+    pairs = int(np.sum(runs // 2))
+    return {"n_blocks": int(len(be)), "experts_used": int(len(runs)), "pair_count": pairs,
+            "pair_count_fraction": pairs / max(1, len(be)), "paired_block_fraction": 2 * pairs / max(1, len(be))}
+
+
+def moe_work(w, x):
+    """Useful FLOPs (routed rows only), and algorithmic bytes: the sorted rows and
+    their scales read once, each used expert's weights and scales read once, C written once."""
+    rows = x.A.shape[0]
+    N, K = w["N"], w["K"]
+    used = len(np.unique(x.block_expert))
+    flops = 2.0 * w["tokens"] * w["top_k"] * N * K
+    nbytes = (rows * K + 4 * rows * (K // 128) + used * (N * K + 4 * (N // 128) * (K // 128)) + 2 * rows * N)
+    return flops, nbytes
+
+
+def moe_cpu_sample(x, target_s):
+    import oracle
+    t0 = time.perf_counter()
+    done = 0
+    b = 0
+    while b < x.n_blocks and (done == 0 or time.perf_counter() - t0 < target_s):
+        e = int(x.block_expert[b])
+        rows = slice(64 * b, 64 * b + 64)
+        oracle.blockscale(x.A[rows], x.a_scale[rows], x.B[e], x.b_scale[e])
+        done += 1
+        b += 1
+    dt = time.perf_counter() - t0
+    flops = 2.0 * 64 * done * x.N * x.K
+    return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": oracle.max_threads(), "kind": "oracle",
+            "sample": f"{done} of {x.n_blocks} sort blocks (64 rows each, padded rows included) in {dt:.2f} s, "
+                      f"fp64 dequantise + naive triple loop"}
+
+
+def run_moe(args):
+    import torch
+    world, rank, local = dist_setup(args)
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU")
+    torch.cuda.set_device(local)
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+        pg = dist
+    import fp8_block_scaled_e4m3_gb300 as f
+
+    w = workloads.WORKLOADS[args.workload]
+    E, N, K = w["experts"], w["N"], w["K"]
+    x = workloads.make_moe_inputs(w["tokens"], w["top_k"], E, N, K, seed=args.seed, skew=w["skew"])
+    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+    host = [x.A, workloads.a_scale_to_kmajor(x.a_scale), x.block_expert]
+    A, sa, be = [dev(h) for h in host]
+    B, sb = dev(x.B), dev(x.b_scale)
+    lead = torch.empty(x.n_blocks, dtype=torch.int32, device="cuda")
+    nl = torch.empty(1, dtype=torch.int32, device="cuda")
+    C = torch.empty((x.A.shape[0], N), dtype=torch.bfloat16, device="cuda")
+    flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.int32, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def segment(pair=True, a=A, s_a=sa, table=be, out=C):
+        f.moe_leaders(table, E, pair=pair, leaders=lead, n_leaders=nl)
+        f.gemm_moe(a, s_a, B, sb, table, lead, nl, C=out)
+
+    def timed(fn, n):
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+        for i in range(n):
+            flush.fill_(1)
+            ev[i][0].record(stream)
+            fn()
+            ev[i][1].record(stream)
+        torch.cuda.synchronize()
+        assert f.get_status() == 0
+        return [a.elapsed_time(b) for a, b in ev]
+
+    segment()
+    assert f.get_status() == 0
+    cfg_id = f.last_config_id()
+    sampler = ClockSampler(torch.cuda.current_device()) if rank == 0 else None
+    if sampler:
+        sampler.start()
+    t_w = time.perf_counter()
+    n_w = 0
+    while n_w < max(args.warmup, 3) or time.perf_counter() - t_w < args.warmup_seconds:
+        flush.fill_(1)
+        segment()
+        n_w += 1
+        if n_w % 50 == 0:
+            torch.cuda.synchronize()
+    if pg:
+        pg.barrier()
+    torch.cuda.synchronize()
+    wall0 = time.perf_counter()
+    per_ms = timed(segment, args.steps)
+    if pg:
+        pg.barrier()
+    wall = time.perf_counter() - wall0
+    clocks = sampler.stop() if sampler else None
+    ms = max_over_ranks(statistics.mean(per_ms), pg, torch, "cuda")
+    n_ab = max(3, min(args.steps, 100))
+    gemm_ms = statistics.mean(timed(lambda: f.gemm_moe(A, sa, B, sb, be, lead, nl, C=C), n_ab))
+    n_leaders_paired = int(nl.item())
+    unpaired_ms = statistics.mean(timed(lambda: segment(pair=False), n_ab))
+    n_leaders_unpaired = int(nl.item())
+    paired_ms = statistics.mean(timed(segment, n_ab))
+    desc_ms = statistics.mean(timed(lambda: f.moe_leaders(be, E, leaders=lead, n_leaders=nl), n_ab))
+
+    flops, nbytes = moe_work(w, x)
+    value = aggregate_tflops(world, flops, ms)
+    peaks = load_peaks()
+    t_hbm = nbytes / (peaks["hbm_gbs"] * 1e9)
+    t_tensor = 2.0 * x.A.shape[0] * N * K / (peaks["fp8_tflops"] * 1e12)   # padded rows go through the MMAs
+    if t_hbm >= t_tensor:
+        achieved = nbytes / (gemm_ms * 1e-3) / 1e9
+        roofline = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                    "frac": achieved / peaks["hbm_gbs"], "traffic": None}
+    else:
+        achieved = 2.0 * x.A.shape[0] * N * K / (gemm_ms * 1e-3) / 1e12
+        roofline = {"bound": "tensor", "achieved": achieved, "peak": peaks["fp8_tflops"], "unit": "TFLOP/s",
+                    "frac": achieved / peaks["fp8_tflops"], "traffic": None}
+    roofline.update({"kernel": "fp8bs_blockscale_kernel (grouped)", "kernel_ms": gemm_ms,
+                     "algorithmic_bytes": nbytes, "hbm_time_us": t_hbm * 1e6, "tensor_time_us": t_tensor * 1e6,
+                     "peak_source": f"{peaks['source']} (MEASURED_PEAKS hbm_gbs / 2 x bf16_tflops)"})
+
+    e2e = None
+    if not args.no_e2e:
+        # per step: the routed rows, their scales and the routing table up, C down (weights resident)
+        pin = [torch.from_numpy(np.ascontiguousarray(h)).pin_memory() for h in host]
+        outp = torch.empty(C.shape, dtype=C.dtype).pin_memory()
+        dA, dsa, dbe = [torch.empty_like(p, device="cuda") for p in pin]
+
+        def e2e_step():
+            for dst, src in zip((dA, dsa, dbe), pin):
+                dst.copy_(src, non_blocking=True)
+            segment(a=dA, s_a=dsa, table=dbe)
+            outp.copy_(C, non_blocking=True)
+
+        for _ in range(3):
+            e2e_step()
+        torch.cuda.synchronize()
+        n_e = max(3, min(args.steps, 50))
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(n_e):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        e_ms = e0.elapsed_time(e1) / n_e
+        e2e = {"value": aggregate_tflops(world, flops, e_ms), "unit": "TFLOP/s",
+               "h2d_bytes_per_step": int(sum(p.numel() * p.element_size() for p in pin)),
+               "d2h_bytes_per_step": int(outp.numel() * outp.element_size()), "ms_per_step": e_ms,
+               "pipeline": "serial: upload, segment, download per step on one stream"}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = moe_cpu_sample(x, args.cpu_seconds)
+
+    st = moe_stats(x.block_expert, E)
+    line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "e4m3 x e4m3 -> f32 accumulate -> bf16", "data": "synthetic",
+            "config": {"workload": args.workload, "tokens": w["tokens"], "top_k": w["top_k"], "experts": E,
+                       "N": N, "K": K, "skew": w["skew"], "seed": args.seed, "rows": int(x.A.shape[0]),
+                       "step": "leader descriptor + grouped GEMM (paired)",
+                       "flops": "2 * tokens * top_k * N * K (routed rows only)",
+                       "l2": "flushed before every step by a 256 MiB write (outside the timed events)",
+                       "kernel_config": f.decode_config(cfg_id), "config_id": cfg_id,
+                       "parallelism": f"{world} independent replicas (weak scaling)",
+                       "wall_s_timed_loop": wall, "warmup_steps_run": n_w, "ms_min": min(per_ms)},
+            "roofline": roofline,
+            "pairing": dict(st, n_leaders_paired=n_leaders_paired, n_leaders_unpaired=n_leaders_unpaired,
+                            paired_segment_ms=paired_ms, unpaired_segment_ms=unpaired_ms,
+                            descriptor_ms=desc_ms, speedup=unpaired_ms / paired_ms),
+            "gpu_launches": args.steps * 2, "clocks": clocks, "e2e": e2e, "cpu_baseline": cpu}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if pg:
+        pg.destroy_process_group()
+    return 0
+
+
+def run_moe_reference(args):
+    world, rank, _ = dist_setup(args)
+    if rank != 0:
+        return 0
+    w = workloads.WORKLOADS[args.workload]
+    x = workloads.make_moe_inputs(w["tokens"], w["top_k"], w["experts"], w["N"], w["K"], seed=args.seed,
+                                  skew=w["skew"])
+    per, cb = [], None
+    for i in range(args.warmup + args.steps):
+        cb = moe_cpu_sample(x, args.cpu_seconds / max(1, args.steps + args.warmup))
+        if i >= args.warmup:
+            per.append(cb["value"])
+    val = statistics.mean(per)
+    flops, _ = moe_work(w, x)
+    line = {"impl": "reference", "metric": METRIC, "value": val, "unit": "TFLOP/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": flops / (val * 1e12) * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": args.workload, "seed": args.seed}, "cpu_baseline": dict(cb, value=val),
+            "e2e": {"value": val, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main():
     args = parse()
+    moe = workloads.WORKLOADS[args.workload]["kind"] == "moe"
     if args.impl == "reference":
-        return run_reference(args)
-    return run_ours(args)
+        return run_moe_reference(args) if moe else run_reference(args)
+    return run_moe(args) if moe else run_ours(args)
 
 
 if __name__ == "__main__":

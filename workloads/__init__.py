@@ -295,6 +295,13 @@ WORKLOADS = {
 for _m in (1024, 2048, 4096, 16384):
     WORKLOADS[f"mx_{_m}x5120x2048"] = dict(kind="mx", M=_m, N=5120, K=2048, seeds=(0,))
     WORKLOADS[f"mx_{_m}x8192x1280"] = dict(kind="mx", M=_m, N=8192, K=1280, seeds=(0,))
+# Grouped MoE stage-1 (gate+up) at decode-like token counts: synthetic routing
+# (skill card "FlyDSL decode MoE stage-1 blkmap": sort blocks of 64 rows; the
+# card's measured model is not reproduced, these are generic sizes).
+WORKLOADS["moe_s1_T256_top8_E32_N1536_K2048"] = dict(kind="moe", tokens=256, top_k=8, experts=32, N=1536,
+                                                      K=2048, skew=0.0, seeds=(0,))
+WORKLOADS["moe_s1_T1024_top8_E32_N1536_K2048_skew1"] = dict(kind="moe", tokens=1024, top_k=8, experts=32,
+                                                             N=1536, K=2048, skew=1.0, seeds=(0,))
 
 
 def make_inputs(kind: str, M: int, N: int, K: int, seed: int = 0):
