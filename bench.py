@@ -601,6 +601,7 @@ def run_moe(args):
         achieved = 2.0 * x.A.shape[0] * N * K / (gemm_ms * 1e-3) / 1e12
         roofline = {"bound": "tensor", "achieved": achieved, "peak": peaks["fp8_tflops"], "unit": "TFLOP/s",
                     "frac": achieved / peaks["fp8_tflops"], "traffic": None}
+    roofline["traffic"] = profiled_traffic("bs", args.workload)
     roofline.update({"kernel": "fp8bs_blockscale_kernel (grouped)", "kernel_ms": gemm_ms,
                      "algorithmic_bytes": nbytes, "hbm_time_us": t_hbm * 1e6, "tensor_time_us": t_tensor * 1e6,
                      "peak_source": f"{peaks['source']} (MEASURED_PEAKS hbm_gbs / 2 x bf16_tflops)"})
