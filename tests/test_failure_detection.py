@@ -25,6 +25,62 @@ def _gpu():
         pytest.skip("no CUDA device")
 
 
+def _call(kind, x):
+    """A callable that launches the path under test once on the inputs x and
+    returns its output tensor."""
+    import torch
+    import fp8_block_scaled_e4m3_gb300 as f
+    if kind in ("bs", "bs_sk", "e4m3"):
+        d = (to_dev(x.A), to_dev(workloads.a_scale_to_kmajor(x.a_scale)), to_dev(x.B), to_dev(x.b_scale))
+        if kind == "e4m3":
+            return lambda: f.gemm_blockscale_e4m3out(*d, 8.0)
+        return lambda: f.gemm_blockscale(*d)
+    if kind in ("mx", "mx_sk"):
+        return lambda: f.gemm_mxfp8(to_dev(x.A), to_dev(x.a_e8m0), to_dev(x.B), to_dev(x.b_e8m0))
+    if kind == "twin":
+        return lambda: f.gemm_tensorscale(to_dev(x.A), to_dev(x.B), 1e-3)
+    A, sa = to_dev(x.A), to_dev(workloads.a_scale_to_kmajor(x.a_scale))
+    B, sb, be = to_dev(x.B), to_dev(x.b_scale), to_dev(x.block_expert)
+
+    def moe():
+        lead, n = f.moe_leaders(be, x.num_experts)
+        return f.gemm_moe(A, sa, B, sb, be, lead, n)
+    return moe
+
+
+OVERRIDE = {"bs_sk": 1256402, "mx_sk": 2256402}
+
+
+@pytest.mark.parametrize("kind", ["bs", "bs_sk", "e4m3", "mx", "mx_sk", "twin", "moe"])
+def test_every_path_reports_a_timeout_and_recovers(kind):
+    """Stream-K included: a CTA that gives up never publishes its partial, and
+    the finishers waiting for it run out of time as well instead of hanging."""
+    import torch
+    import fp8_block_scaled_e4m3_gb300 as f
+    if kind == "moe":
+        x = workloads.make_moe_inputs(512, 2, 8, 256, 1024, seed=5, skew=1.0)
+    else:
+        x = workloads.make_inputs("mx" if kind.startswith("mx") else "bs", 256, 1024, 4096, seed=4)
+    f.set_config_override(OVERRIDE.get(kind, 0))
+    try:
+        run = _call(kind, x)
+        f.set_wait_limit_ns(200)
+        try:
+            run()
+            assert f.get_status() == TIMEOUT
+        finally:
+            f.set_wait_limit_ns(0)
+        assert f.get_status() == 0
+        first = run()
+        assert f.get_status() == 0
+        second = run()            # a clean call after the recovered one: same bits (fresh stream-K tokens)
+        assert f.get_status() == 0
+        torch.cuda.synchronize()
+        assert torch.equal(first.view(torch.uint8), second.view(torch.uint8))
+    finally:
+        f.set_config_override(0)
+
+
 @pytest.mark.parametrize("kind", ["bs", "mx"])
 def test_wait_timeout_reported_and_context_survives(kind):
     import torch
