@@ -31,6 +31,7 @@ _SIGS = {
     "fp8bs_gemm_tensorscale": (_i, [_p, _p, _p, _i, _i, _i, ctypes.c_float, _p]),
     "fp8bs_gemm_e4m3out": (_i, [_p, _p, _p, _p, _p, ctypes.c_float, _i, _i, _i, _p]),
     "fp8bs_moe_leaders": (_i, [_p, _i, _i, _i, _p, _p, _p]),
+    "fp8mx_gemm_e4m3out": (_i, [_p, _p, _p, _p, _p, ctypes.c_float, _i, _i, _i, _p]),
     "fp8bs_moe_gemm": (_i, [_p, _p, _p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _p]),
     "fp8mx_gemm": (_i, [_p, _p, _p, _p, _p, _i, _i, _i, _p]),
     "fp8mx_gemm_packed": (_i, [_p, _p, _p, _p, _p, _i, _i, _i, _p]),
@@ -153,6 +154,22 @@ def gemm_blockscale_e4m3out(A, a_scale, B, b_scale, c_scale, C8=None, stream=Non
                                  _dev_ptr(b_scale, "b_scale", ((N + 127) // 128, K // 128)),
                                  _dev_ptr(C8, "C8", (M, N)), float(c_scale), M, N, K, _stream_ptr(stream))
     _check(rc, "fp8bs_gemm_e4m3out")
+    return C8
+
+
+def gemm_mxfp8_e4m3out(A, a_e8m0, B, b_e8m0, c_scale, C8=None, stream=None):
+    """C8[M,N] E4M3 codes (uint8) = e4m3(c_scale * the MXFP8 GEMM's fp32 sum); N % 16 == 0."""
+    torch = _torch()
+    M, K = A.shape
+    N = B.shape[0]
+    if C8 is None:
+        C8 = torch.empty((M, N), dtype=torch.uint8, device=A.device)
+    if C8.dtype not in (torch.uint8, torch.float8_e4m3fn):
+        raise TypeError("C8 must be uint8 or float8_e4m3fn")
+    rc = _lib.fp8mx_gemm_e4m3out(_fp8_ptr(A, "A", (M, K)), _dev_ptr(a_e8m0, "a_e8m0", (M, K // 32)),
+                                 _fp8_ptr(B, "B", (N, K)), _dev_ptr(b_e8m0, "b_e8m0", (N, K // 32)),
+                                 _dev_ptr(C8, "C8", (M, N)), float(c_scale), M, N, K, _stream_ptr(stream))
+    _check(rc, "fp8mx_gemm_e4m3out")
     return C8
 
 

@@ -329,15 +329,20 @@ __global__ void pack_a_scale_kernel(const float *__restrict__ src, float *__rest
 // (cfg.kind 2) or of the tensor-scale twin (cfg.kind 4, no scale atoms, one
 // alpha): a persistent grid of min(tiles, SMs) CTAs, or the stream-K grid.
 int launch_mx(const Config &cfg, const void *A, const uint8_t *a_sf, const void *B, const uint8_t *b_sf, void *C,
-              int M, int N, int K, float alpha, int *status_ptr, int num_sms, cudaMemPool_t pool, cudaStream_t s)
+              int M, int N, int K, float alpha, int *status_ptr, int num_sms, cudaMemPool_t pool, cudaStream_t s,
+              bool c_e4m3 = false, float c_scale = 1.f)
 {
     CUtensorMap tmA, tmB, tmC;
     if (!encode_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, A, K, M, K, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
         !encode_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, B, K, N, K, 128, cfg.block_n, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !encode_2d(&tmC, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, C, N, M, static_cast<uint64_t>(N) * 2, kCChunkCols, 32,
-                   CU_TENSOR_MAP_SWIZZLE_64B))
+        !(c_e4m3 ? encode_2d(&tmC, CU_TENSOR_MAP_DATA_TYPE_UINT8, C, N, M, static_cast<uint64_t>(N), 64, 32,
+                             CU_TENSOR_MAP_SWIZZLE_64B)
+                 : encode_2d(&tmC, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, C, N, M, static_cast<uint64_t>(N) * 2,
+                             kCChunkCols, 32, CU_TENSOR_MAP_SWIZZLE_64B)))
         return FP8BS_ERR_LAUNCH;
     GemmArgs args = {};
+    args.c_e4m3 = c_e4m3 ? 1 : 0;
+    args.c_scale = c_scale;
     args.M = M;
     args.N = N;
     args.K = K;
@@ -633,12 +638,14 @@ int fp8bs_gemm_e4m3out(const void *A, const float *a_scale, const void *B, const
     return blockscale_gemm(A, a_scale, B, b_scale, C8, true, c_scale, M, N, K, stream);
 }
 
-int fp8mx_gemm_packed(const void *A, const uint8_t *a_sf, const void *B, const uint8_t *b_sf, void *C, int M,
-                      int N, int K, void *stream)
+static int mx_gemm_packed_any(const void *A, const uint8_t *a_sf, const void *B, const uint8_t *b_sf, void *C,
+                              bool c_e4m3, float c_scale, int M, int N, int K, void *stream)
 {
     int rc = check_shape(M, N, K);
     if (rc)
         return rc;
+    if (c_e4m3 && (N % 16) != 0)
+        return FP8BS_ERR_SHAPE;
     if (M == 0)
         return FP8BS_OK;
     if (!A || !a_sf || !B || !b_sf || !C)
@@ -653,10 +660,16 @@ int fp8mx_gemm_packed(const void *A, const uint8_t *a_sf, const void *B, const u
     if (!override_config(2, 2, cfg))
         return FP8BS_ERR_SHAPE;
     if ((rc = launch_mx(cfg, A, a_sf, B, b_sf, C, M, N, K, 1.f, st->status_ptr, st->num_sms, st->pool,
-                        static_cast<cudaStream_t>(stream))))
+                        static_cast<cudaStream_t>(stream), c_e4m3, c_scale)))
         return rc;
     t_last_config = config_id(cfg);
     return FP8BS_OK;
+}
+
+int fp8mx_gemm_packed(const void *A, const uint8_t *a_sf, const void *B, const uint8_t *b_sf, void *C, int M,
+                      int N, int K, void *stream)
+{
+    return mx_gemm_packed_any(A, a_sf, B, b_sf, C, false, 1.f, M, N, K, stream);
 }
 
 int fp8bs_moe_leaders(const int *block_expert, int n_blocks, int num_experts, int pair, int *leaders,
@@ -737,12 +750,14 @@ int fp8mx_pack_scales(const uint8_t *e8m0, uint8_t *packed, int rows, int K, voi
     return launch_pack_scales(e8m0, packed, rows, e8m0, packed, 0, K, st->num_sms, static_cast<cudaStream_t>(stream));
 }
 
-int fp8mx_gemm(const void *A, const uint8_t *a_e8m0, const void *B, const uint8_t *b_e8m0, void *C, int M, int N,
-               int K, void *stream)
+static int mx_gemm_any(const void *A, const uint8_t *a_e8m0, const void *B, const uint8_t *b_e8m0, void *C,
+                       bool c_e4m3, float c_scale, int M, int N, int K, void *stream)
 {
     int rc = check_shape(M, N, K);
     if (rc)
         return rc;
+    if (c_e4m3 && (N % 16) != 0)
+        return FP8BS_ERR_SHAPE;
     if (M == 0)
         return FP8BS_OK;
     if (!A || !a_e8m0 || !B || !b_e8m0 || !C)
@@ -763,10 +778,22 @@ int fp8mx_gemm(const void *A, const uint8_t *a_e8m0, const void *B, const uint8_
     uint8_t *b_sf = a_sf + a_bytes;
     rc = launch_pack_scales(a_e8m0, a_sf, M, b_e8m0, b_sf, N, K, st->num_sms, s);
     if (rc == FP8BS_OK)
-        rc = fp8mx_gemm_packed(A, a_sf, B, b_sf, C, M, N, K, stream);
+        rc = mx_gemm_packed_any(A, a_sf, B, b_sf, C, c_e4m3, c_scale, M, N, K, stream);
     if (cudaFreeAsync(ws, s) != cudaSuccess && rc == FP8BS_OK)
         rc = FP8BS_ERR_CUDA;
     return rc;
+}
+
+int fp8mx_gemm(const void *A, const uint8_t *a_e8m0, const void *B, const uint8_t *b_e8m0, void *C, int M, int N,
+               int K, void *stream)
+{
+    return mx_gemm_any(A, a_e8m0, B, b_e8m0, C, false, 1.f, M, N, K, stream);
+}
+
+int fp8mx_gemm_e4m3out(const void *A, const uint8_t *a_e8m0, const void *B, const uint8_t *b_e8m0, void *C8,
+                       float c_scale, int M, int N, int K, void *stream)
+{
+    return mx_gemm_any(A, a_e8m0, B, b_e8m0, C8, true, c_scale, M, N, K, stream);
 }
 
 int64_t fp8bs_a_scale_ld(int M) { return (static_cast<int64_t>(M) + 3) / 4 * 4; }

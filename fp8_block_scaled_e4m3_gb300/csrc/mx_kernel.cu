@@ -319,9 +319,16 @@ __device__ __forceinline__ void mx_gemm_body(const CUtensorMap &tmA, const CUten
             }
             const int x0 = nb * BN + wg * HALF;
             const int y0 = mb * kBlockM + q * 32;
+            if (MX && args.c_e4m3) {
 #pragma unroll
-            for (int c = 0; c < HALF / kCChunkCols; ++c)
-                store_c_chunk(&tmC, cstage, lane, v + c * kCChunkCols, x0 + c * kCChunkCols, y0, args.M, args.N);
+                for (int c = 0; c < HALF / 64; ++c)
+                    store_c8_chunk(&tmC, cstage, lane, v + c * 64, args.c_scale, x0 + c * 64, y0, args.M, args.N);
+            } else {
+#pragma unroll
+                for (int c = 0; c < HALF / kCChunkCols; ++c)
+                    store_c_chunk(&tmC, cstage, lane, v + c * kCChunkCols, x0 + c * kCChunkCols, y0, args.M,
+                                  args.N);
+            }
         }
         if (lane == 0)
             ptx::bulk_wait_all();

@@ -118,6 +118,14 @@ int fp8mx_gemm(const void *A, const uint8_t *a_e8m0, const void *B, const uint8_
                int M, int N, int K, void *stream);
 
 /*
+ * fp8mx_gemm with an E4M3 C: C8[m,n] = e4m3(c_scale * the fp32 sum), rounded
+ * and saturated as fp8bs_gemm_e4m3out; N % 16 == 0. Other arguments, launches
+ * and errors as fp8mx_gemm.
+ */
+int fp8mx_gemm_e4m3out(const void *A, const uint8_t *a_e8m0, const void *B, const uint8_t *b_e8m0, void *C8,
+                       float c_scale, int M, int N, int K, void *stream);
+
+/*
  * MXFP8 GEMM on scale factors already in the packed layout (one kernel; no
  * allocation except the stream-K workspace, chosen as for fp8bs_gemm when it
  * saves at least 13 K steps of 128, same size, pool and graph caveat). The PR above keeps its scale shuffles as separate weight-prep

@@ -163,6 +163,13 @@ def blockscale_e4m3out(A, a_scale, B, b_scale, c_scale, rows=None):
     return e4m3_encode(y), y
 
 
+def mxfp8_e4m3out(A, a_e8m0, B, b_e8m0, c_scale, rows=None):
+    """The MXFP8 GEMM with an E4M3 C, as blockscale_e4m3out: (codes, y)."""
+    _, exact = mxfp8(A, a_e8m0, B, b_e8m0, rows=rows, exact=True)
+    y = (exact.astype(np.float32) * np.float32(c_scale)).astype(np.float32)
+    return e4m3_encode(y), y
+
+
 def moe_leaders(block_expert, num_experts, pair=True) -> np.ndarray:
     """Leader descriptor of a sorted block -> expert table (skill card "FlyDSL
     decode MoE stage-1 blkmap", procedure step 2): for every run of k adjacent

@@ -80,6 +80,10 @@ def test_e4m3out_entry_checks_before_launch(lib):
     assert f(None, None, None, None, None, one, 0, 32, 128, None) == 0
     assert f(None, P, P, P, P, one, 4, 32, 128, None) == -1
     assert f(P, P, P, P, ctypes.c_void_p((1 << 20) + 8), one, 4, 32, 128, None) == -2
+    g = L.fp8mx_gemm_e4m3out
+    assert g(P, P, P, P, P, one, 4, 24, 128, None) == -3        # N % 16
+    assert g(None, None, None, None, None, one, 0, 32, 128, None) == 0
+    assert g(None, P, P, P, P, one, 4, 32, 128, None) == -1
 
 
 def test_alignment_rejected_before_launch(lib):

@@ -685,3 +685,20 @@ def test_moe_gemm_layer_sized_sampled_blocks():
         rows = slice(64 * b, 64 * b + 64)
         want = oracle.blockscale(x.A[rows], x.a_scale[rows], x.B[e], x.b_scale[e])
         compare(got[rows], want, f"moe block {b}")
+
+
+@pytest.mark.parametrize("cfg", [2256411, 2128611, 2256412])
+@pytest.mark.parametrize("M,N,K", [(300, 528, 1280), (129, 144, 256), (1, 16, 128)])
+def test_mxfp8_e4m3out_every_config(override, cfg, M, N, K):
+    import fp8_block_scaled_e4m3_gb300 as f
+    raster = 1 if M >= N else 0
+    cid = cfg - (cfg // 10 % 10) * 10 + raster * 10
+    override(cid)
+    x = workloads.make_mxfp8_inputs(M, N, K, seed=M + 5 * N)
+    ref = oracle.bf16_bits_to_float(oracle.mxfp8(x.A, x.a_e8m0, x.B, x.b_e8m0)).astype(np.float64)
+    s = float(2.0 ** np.round(np.log2(16.0 / (np.sqrt(np.mean(ref ** 2)) or 1.0))))
+    got = f.gemm_mxfp8_e4m3out(to_dev(x.A), to_dev(x.a_e8m0), to_dev(x.B), to_dev(x.b_e8m0), s).cpu().numpy()
+    assert f.get_status() == 0
+    assert f.last_config_id() == cid
+    codes, y = oracle.mxfp8_e4m3out(x.A, x.a_e8m0, x.B, x.b_e8m0, s)
+    compare_e4m3(got, codes, y, s, f"mx e4m3out {cid} {M}x{N}x{K}")

@@ -462,3 +462,23 @@ def test_moe_routing_layout():
         if (rows < 0).any():
             assert np.all(rows[np.argmax(rows < 0):] < 0)
     assert np.all(x.A[~real] == 0)
+
+
+def test_mxfp8_e4m3out_on_integer_inputs():
+    """Integer codes with unit ue8m0 scales (byte 127): exact integer sums; c_scale
+    = 1/4 and the codes are torch's E4M3 cast of sum/4."""
+    torch = pytest.importorskip("torch")
+    rng = np.random.Generator(np.random.PCG64(33))
+    M, N, K = 5, 24, 128
+    va = rng.integers(-2, 3, size=(M, K))
+    vb = rng.integers(-2, 3, size=(N, K))
+    enc = {v: oracle.e4m3_encode(np.array([v], dtype=np.float32))[0] for v in (-2, -1, 0, 1, 2)}
+    A = np.vectorize(enc.get)(va).astype(np.uint8)
+    B = np.vectorize(enc.get)(vb).astype(np.uint8)
+    ea = np.full((M, K // 32), 127, np.uint8)
+    eb = np.full((N, K // 32), 127, np.uint8)
+    codes, y = oracle.mxfp8_e4m3out(A, ea, B, eb, 0.25)
+    exact = (va @ vb.T).astype(np.float64) / 4
+    assert np.array_equal(y, exact.astype(np.float32))
+    ref = torch.from_numpy(exact.astype(np.float32)).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(codes, ref)
