@@ -166,10 +166,13 @@ bool decode_config_id(int id, Config &c)
 }
 
 // Stream-K grid: every CTA gets at least max(8, KB/4) K blocks, so a tile is
-// cut between at most about five CTAs and its finisher adds few partials.
-long long sk_grid(long long units, long long KB, int num_sms)
+// cut between at most about five CTAs and its finisher adds few partials. With
+// a single row of tiles (M <= 128, decode) the hand-off moves only the live
+// rows, so the floor is max(4, KB/8): more CTAs stream the weights.
+long long sk_grid(long long units, long long KB, int num_sms, bool one_row = false)
 {
-    const long long min_units = KB / 4 > 8 ? KB / 4 : 8;
+    const long long floor_units = one_row ? 4 : 8;
+    const long long min_units = KB / (one_row ? 8 : 4) > floor_units ? KB / (one_row ? 8 : 4) : floor_units;
     long long g = units / min_units;
     if (g > num_sms)
         g = num_sms;
@@ -200,13 +203,13 @@ int setup_stream_k(int tiles, int KB, int num_sms, cudaMemPool_t pool, cudaStrea
     const long long units = static_cast<long long>(tiles) * KB;
     if (units >= (1ll << 31) || !pool)
         return FP8BS_ERR_SHAPE;
-    grid = static_cast<int>(sk_grid(units, KB, num_sms));
+    grid = static_cast<int>(sk_grid(units, KB, num_sms, args.M <= 128));
     const int full_waves = tiles / grid;
     args.sk_dp = full_waves >= 2 ? full_waves - 1 : 0;
     // Every CTA must hold at least one unit of the stream-K range: a finisher
     // waits for each CTA after it up to the one holding its tile's last unit.
     // (True by construction: the range has at least a wave of tiles, or grid <=
-    // units / 8.)
+    // units / 4.)
     if (static_cast<long long>(tiles - args.sk_dp * grid) * KB < grid)
         return FP8BS_ERR_SHAPE;
     const size_t slot = static_cast<size_t>(kBlockM) * 256 * sizeof(float);
@@ -245,7 +248,7 @@ Config choose_config(int kind, int M, int N, int K, int num_sms)
     const long long units = tiles256 * KB;
     const long long min_gain = kind == 2 ? kSkMinGainMx : kSkMinGainBs;
     if (tiles256 > 0 && units < (1ll << 31) && num_sms > 0) {
-        const long long g = sk_grid(units, KB, num_sms);
+        const long long g = sk_grid(units, KB, num_sms, M <= 128);
         const long long per_tile = (tiles256 + num_sms - 1) / num_sms * KB;   // one CTA per tile
         const long long per_unit = (units + g - 1) / g;                       // stream-K
         if (per_tile - per_unit >= min_gain) {

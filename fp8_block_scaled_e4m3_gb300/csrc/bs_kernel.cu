@@ -365,8 +365,15 @@ __global__ void __launch_bounds__(kBsThreads, 1)
             // Stream-K hand-off, warp by warp: warp ew of every CTA owns the same
             // 32 rows x HALF columns of a tile, in slot layout [column/4][row].
             const size_t slice = static_cast<size_t>(wg * HALF / 4) * kBlockM + static_cast<size_t>(row);
+            const TileGeo geo = tile_geo<MOE>(args, t, BN, n_leaders);
+            // A warp whose 32 rows all lie past M stores nothing, so it neither
+            // publishes nor adds partials (its counterparts in the other CTAs of
+            // the tile decide the same way): small-M tiles move only live rows.
+            const bool rows_live = geo.a_row + q * 32 < args.M;
             // (Stream-K runs with the 256-wide tile only; the host never sets it for the others.)
             if (kSk && kb0 > 0) {
+                if (!rows_live)
+                    continue;
                 // Head of a tile begun by an earlier CTA: publish the scaled partial.
                 float *dst = args.sk_partial + static_cast<size_t>(blockIdx.x) * (BN * kBlockM) + 4 * slice;
 #pragma unroll
@@ -382,7 +389,7 @@ __global__ void __launch_bounds__(kBsThreads, 1)
                                             args.sk_token);
                 continue;
             }
-            if (kSk && kb_last != KB - 1) {
+            if (kSk && kb_last != KB - 1 && rows_live) {
                 // This CTA holds K block 0 of a cut tile: add the partials of the
                 // CTAs that hold the rest of it, then store the tile.
                 // The other CTAs of the tile: up to the one whose range holds the
@@ -413,7 +420,6 @@ __global__ void __launch_bounds__(kBsThreads, 1)
                 if (!ok)
                     break;
             }
-            const TileGeo geo = tile_geo<MOE>(args, t, BN, n_leaders);
             const int x0 = geo.nb * BN + wg * HALF;
             const int y0 = geo.a_row + q * 32;
             if (MOE && q * 32 >= geo.rows) {

@@ -267,7 +267,11 @@ __device__ __forceinline__ void mx_gemm_body(const CUtensorMap &tmA, const CUten
             // ew of every CTA owns the same 32 rows x HALF columns of a tile, in
             // slot layout [column/4][row] of float4.
             const size_t slice = static_cast<size_t>(wg * HALF / 4) * kBlockM + static_cast<size_t>(row);
+            // Warps whose rows all lie past M skip the hand-off (as in the blockscale kernel).
+            const bool rows_live = mb * kBlockM + q * 32 < args.M;
             if (kSk && ks0 > 0) {
+                if (!rows_live)
+                    continue;
                 // Head of a tile begun by an earlier CTA: publish the partial.
                 float *dst = args.sk_partial + static_cast<size_t>(blockIdx.x) * (BN * kBlockM) + 4 * slice;
 #pragma unroll
@@ -283,7 +287,7 @@ __device__ __forceinline__ void mx_gemm_body(const CUtensorMap &tmA, const CUten
                                             args.sk_token);
                 continue;
             }
-            if (kSk && ks_last != KS - 1) {
+            if (kSk && ks_last != KS - 1 && rows_live) {
                 // This CTA holds K step 0 of a cut tile: add the partials of the
                 // CTAs up to the one whose range holds the tile's last unit.
                 const long long G = gridDim.x;
