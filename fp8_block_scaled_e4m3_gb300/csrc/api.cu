@@ -247,7 +247,12 @@ Config choose_config(int kind, int M, int N, int K, int num_sms)
     const long long KB = K / 128;
     const long long units = tiles256 * KB;
     const long long min_gain = kind == 2 ? kSkMinGainMx : kSkMinGainBs;
-    if (tiles256 > 0 && units < (1ll << 31) && num_sms > 0) {
+    // One row of tiles with more than two live 32-row groups: the hand-off
+    // carries most of each partial, and the 128-wide tile measured faster
+    // (blockscale 128x2048x7168: 26.7 vs 29.1 us; 32x1536x7168: stream-K 25.8
+    // vs 26.6 us, 16x2048x7168: 24.9 vs 26.5 us).
+    const bool heavy_decode = M <= 128 && M > 64;
+    if (tiles256 > 0 && units < (1ll << 31) && num_sms > 0 && !heavy_decode) {
         const long long g = sk_grid(units, KB, num_sms, M <= 128);
         const long long per_tile = (tiles256 + num_sms - 1) / num_sms * KB;   // one CTA per tile
         const long long per_unit = (units + g - 1) / g;                       // stream-K

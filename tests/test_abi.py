@@ -170,6 +170,9 @@ def test_schedule_selection(lib):
     assert sched(16384, 1536, 7168, sms=128) == "tile"  # 768 tiles = 6 full waves
     assert sched(4096, 2048, 128) == "tile"           # one K block: nothing to share
     assert sched(256, 512, 512) == "tile"             # 8 tiles x 4: 4 -> 1, not worth a hand-off
+    assert sched(16, 2048, 7168) == "stream_k"        # decode: 8 tiles x 56, pieces of >= 7
+    assert sched(128, 2048, 7168) == "tile"           # one row of tiles, four live row groups
+    assert lib.decode_config(lib.select_config("bs", 128, 2048, 7168, 152))["block_n"] == 128
     mx = lambda M, N, K, sms=152: lib.decode_config(lib.select_config("mx", M, N, K, sms))["schedule"]
     assert mx(1024, 5120, 2048) == "stream_k"         # 160 tiles x 16: 32 -> 17
     assert mx(2048, 5120, 2048) == "stream_k"         # 320 tiles x 16: 48 -> 34
