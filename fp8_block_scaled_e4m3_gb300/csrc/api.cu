@@ -154,7 +154,9 @@ bool decode_config_id(int id, Config &c)
     c.stages = (id / 100) % 10;
     c.raster = (id / 10) % 10;
     c.sched = id % 10;
-    if (c.sched < 1 || c.sched > 2 || c.raster > 1 || (c.sched == 2 && (c.kind == 3 || c.block_n != 256)))
+    // stream-K: the 256-wide tile of kinds 1, 2 and 4, and the MXFP8 kernel's 128-wide tile
+    if (c.sched < 1 || c.sched > 2 || c.raster > 1 ||
+        (c.sched == 2 && (c.kind == 3 || (c.block_n != 256 && !(c.kind == 2 && c.block_n == 128)))))
         return false;
     if (c.kind == 1)
         return (c.block_n == 256 && c.stages == 4) || (c.block_n == 128 && c.stages == 6);
@@ -368,7 +370,7 @@ int launch_mx(const Config &cfg, const void *A, const uint8_t *a_sf, const void 
     int grid = tiles < num_sms ? tiles : num_sms;
     void *ws = nullptr;
     if (cfg.sched == 2) {
-        if (cfg.block_n != 256)
+        if (cfg.block_n != 256 && cfg.kind != 2)
             return FP8BS_ERR_SHAPE;
         const int rc = setup_stream_k(tiles, K / 128, num_sms, pool, s, args, grid, ws);
         if (rc)

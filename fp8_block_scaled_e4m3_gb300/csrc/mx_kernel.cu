@@ -228,7 +228,7 @@ __device__ __forceinline__ void mx_gemm_body(const CUtensorMap &tmA, const CUten
         ptx::setmaxnreg_inc<kMxRegsHigh>();
         // ------------------------------------------------------ epilogue
         constexpr int HALF = BN / 2;
-        constexpr bool kSk = BN == 256;         // tile width with the stream-K hand-off
+        constexpr bool kSk = true;              // both tile widths carry the stream-K hand-off
         const int ew = warp - 4;                // 0..7
         const int wg = ew >> 2;
         const int q = warp & 3;

@@ -148,7 +148,7 @@ def test_config_selection(lib):
     L = lib.lib()
     assert L.fp8bs_set_config_override(1999911) == -3      # no such kernel
     assert L.fp8bs_set_config_override(1160511) == -3      # the 160-wide tile was removed
-    assert L.fp8bs_set_config_override(2128612) == -3      # stream-K runs with the 256-wide tile only
+    assert L.fp8bs_set_config_override(2128612) == 0       # the MXFP8 kernel's 128-wide tile has stream-K too
     assert L.fp8bs_set_config_override(4128612) == -3
     assert L.fp8bs_set_config_override(3128812) == -3      # no stream-K for the CTA pair
     assert L.fp8bs_set_config_override(1256413) == -3      # no such schedule

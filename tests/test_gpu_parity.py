@@ -180,7 +180,7 @@ def test_pack_a_scale_bit_exact():
 # every built kernel configuration, forced through the override
 # one-CTA 128x256, 128x128 (one CTA per tile), 128x256 stream-K, CTA-pair 256x128
 BS_CONFIGS = [1256411, 1128611, 1256412, 3128811]
-MX_CONFIGS = [2256411, 2128611, 2256412]
+MX_CONFIGS = [2256411, 2128611, 2256412, 2128612]
 
 
 @pytest.fixture
@@ -436,13 +436,15 @@ def test_mxfp8_cuda_graph_replay(override, cid):
         del g
 
 
+@pytest.mark.parametrize("width", [256, 128])
 @pytest.mark.parametrize("M,N,K", [(256, 512, 7168), (130, 264, 3840), (1100, 776, 2048), (32, 5120, 2048),
-                                   (1, 520, 1280)])
-def test_mxfp8_stream_k_tiles_cut_between_many_ctas(override, M, N, K):
-    """MXFP8 under stream-K: few tiles (decode-like M included), each accumulated
-    in pieces by several CTAs; ragged tails inside cut tiles."""
+                                   (1, 520, 1280), (70, 1024, 4096)])
+def test_mxfp8_stream_k_tiles_cut_between_many_ctas(override, width, M, N, K):
+    """MXFP8 under stream-K, both tile widths: few tiles (decode-like M
+    included, where only the live row groups hand off), each accumulated in
+    pieces by several CTAs; ragged tails inside cut tiles."""
     import fp8_block_scaled_e4m3_gb300 as f
-    cid = 2256402 + (10 if M >= N else 0)
+    cid = (2256402 if width == 256 else 2128602) + (10 if M >= N else 0)
     override(cid)
     x = workloads.make_mxfp8_inputs(M, N, K, seed=M + N + 5)
     got = run_mxfp8(x.A, x.a_e8m0, x.B, x.b_e8m0)
@@ -687,7 +689,7 @@ def test_moe_gemm_layer_sized_sampled_blocks():
         compare(got[rows], want, f"moe block {b}")
 
 
-@pytest.mark.parametrize("cfg", [2256411, 2128611, 2256412])
+@pytest.mark.parametrize("cfg", [2256411, 2128611, 2256412, 2128612])
 @pytest.mark.parametrize("M,N,K", [(300, 528, 1280), (129, 144, 256), (1, 16, 128)])
 def test_mxfp8_e4m3out_every_config(override, cfg, M, N, K):
     import fp8_block_scaled_e4m3_gb300 as f
