@@ -57,6 +57,9 @@ def parse():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-twin", action="store_true", help="skip the promote-free twin timing (blockscale)")
+    p.add_argument("--ksweep", action="store_true",
+                   help="blockscale: time the kernel and its twin over K at the workload's M, N; print the "
+                        "fixed + slope fit (skill card 'Bottleneck diagnosis' step 6) instead of the bench line")
     p.add_argument("--warmup-seconds", type=float, default=1.0,
                    help="minimum warm-up duration (clock sampling); 0 for profiler runs")
     return p.parse_args()
@@ -320,6 +323,17 @@ def run_ours(args):
         kernel_ms = statistics.mean(a.elapsed_time(b) for a, b in kev)
         assert f.get_status() == 0
     assert f.get_status() == 0
+    # hot-L2 figure beside the cold one: the same step back to back, no flush
+    for _ in range(3):
+        step()
+    hev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(50)]
+    for a, b in hev:
+        a.record(stream)
+        step()
+        b.record(stream)
+    torch.cuda.synchronize()
+    assert f.get_status() == 0
+    hot_ms = statistics.mean(a.elapsed_time(b) for a, b in hev)
 
     flops = 2.0 * M * N * K
     value = aggregate_tflops(world, flops, ms)
@@ -360,7 +374,7 @@ def run_ours(args):
                        "kernel_config": f.decode_config(cfg_id), "config_id": cfg_id,
                        "parallelism": f"{world} independent replicas (weak scaling)",
                        "wall_s_timed_loop": wall, "warmup_steps_run": n_w, "ms_min": min(per_ms),
-                       "ms_median": statistics.median(per_ms)},
+                       "ms_median": statistics.median(per_ms), "hot_l2_ms_per_step": hot_ms},
             "roofline": roofline, "ceiling_twin": twin, "e4m3_out": e4m3,
             "gpu_launches": args.steps * (f.lib().fp8bs_launches_per_call() if kind == "bs"
                                           else f.lib().fp8mx_launches_per_call()),
@@ -686,8 +700,52 @@ def run_moe_reference(args):
     return 0
 
 
+def run_ksweep(args):
+    """t(K) = fixed + slope * K/128 for the blockscale kernel and its promote-free
+    twin at the workload's M and N (L2 flushed, CUDA events, least squares)."""
+    import torch
+    import fp8_block_scaled_e4m3_gb300 as f
+    kind, M, N, K0 = workload_shape(args.workload)
+    assert kind == "bs", "--ksweep is for blockscale workloads"
+    flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.int32, device="cuda")
+    stream = torch.cuda.current_stream()
+    n = max(10, min(args.steps, 100))
+    ks = [k for k in (1024, 2048, 3072, 4096, 5120, 6144, 7168) if k <= max(K0, 1024)]
+    rows = []
+    for K in ks:
+        x, _, d = make_device_inputs("bs", M, N, K, args.seed, torch)
+        out = {"K": K, "KB": K // 128}
+        for name, fn in (("blockscale", lambda: f.gemm_blockscale(*d)),
+                         ("twin", lambda: f.gemm_tensorscale(d[0], d[2], 1e-6))):
+            for _ in range(3):
+                fn()
+            ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+            for a, b in ev:
+                flush.fill_(1)
+                a.record(stream)
+                fn()
+                b.record(stream)
+            torch.cuda.synchronize()
+            assert f.get_status() == 0
+            out[name + "_us"] = statistics.mean(a.elapsed_time(b) for a, b in ev) * 1e3
+            out[name + "_config"] = f.last_config_id()
+        rows.append(out)
+    fit = {}
+    kb = np.array([r["KB"] for r in rows], dtype=np.float64)
+    for name in ("blockscale", "twin"):
+        t = np.array([r[name + "_us"] for r in rows])
+        slope, fixed = np.polyfit(kb, t, 1)
+        fit[name] = {"fixed_us": fixed, "slope_us_per_kblock": slope}
+    print(json.dumps({"ksweep": args.workload, "M": M, "N": N, "l2": "flushed", "points": rows, "fit": fit,
+                      "note": "slope per K block of the whole GEMM; per CTA divide by the tiles each CTA holds"}),
+          flush=True)
+    return 0
+
+
 def main():
     args = parse()
+    if args.ksweep:
+        return run_ksweep(args)
     moe = workloads.WORKLOADS[args.workload]["kind"] == "moe"
     if args.impl == "reference":
         return run_moe_reference(args) if moe else run_reference(args)

@@ -31,6 +31,7 @@ _SIGS = {
     "fp8bs_gemm_tensorscale": (_i, [_p, _p, _p, _i, _i, _i, ctypes.c_float, _p]),
     "fp8bs_gemm_e4m3out": (_i, [_p, _p, _p, _p, _p, ctypes.c_float, _i, _i, _i, _p]),
     "fp8bs_moe_leaders": (_i, [_p, _i, _i, _i, _p, _p, _p]),
+    "fp8bs_shutdown": (_i, []),
     "fp8mx_gemm_e4m3out": (_i, [_p, _p, _p, _p, _p, ctypes.c_float, _i, _i, _i, _p]),
     "fp8bs_moe_gemm": (_i, [_p, _p, _p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _p]),
     "fp8mx_gemm": (_i, [_p, _p, _p, _p, _p, _i, _i, _i, _p]),
@@ -334,6 +335,11 @@ def set_config_override(config_id: int) -> None:
 
 def set_wait_limit_ns(ns: int) -> None:
     _lib.fp8bs_set_wait_limit_ns(int(ns))
+
+
+def shutdown() -> None:
+    """Release the library's per-device workspace pools (see fp8bs_shutdown)."""
+    _check(_lib.fp8bs_shutdown(), "fp8bs_shutdown")
 
 
 def version() -> str:

@@ -906,6 +906,27 @@ int fp8bs_set_config_override(int config_id)
     return FP8BS_OK;
 }
 
+int fp8bs_shutdown(void)
+{
+    std::lock_guard<std::mutex> lock(g_mutex);
+    int cur = -1;
+    const bool have_cur = cudaGetDevice(&cur) == cudaSuccess;
+    int rc = FP8BS_OK;
+    for (int d = 0; d < kMaxDevices; ++d) {
+        DeviceState &st = g_dev[d];
+        if (!st.ready)
+            continue;
+        if (cudaSetDevice(d) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess)
+            rc = FP8BS_ERR_CUDA;
+        if (st.pool && cudaMemPoolDestroy(st.pool) != cudaSuccess)
+            rc = FP8BS_ERR_CUDA;
+        st = DeviceState();
+    }
+    if (have_cur)
+        cudaSetDevice(cur);
+    return rc;
+}
+
 int fp8bs_device_info(int *num_sms, int *pair_clusters)
 {
     int dev;

@@ -273,6 +273,15 @@ const char *fp8bs_status_string(int status);
  * over two SMs), 4 = tensor-scale twin (fp8bs_gemm_tensorscale); schedule 1 =
  * one CTA per tile, 2 = stream-K (kinds 1, 2 and 4 with block_n 256 only). */
 int fp8bs_last_config_id(void);
+/* Release what the library holds per device: waits for each device it set
+ * up (cudaDeviceSynchronize), destroys its stream-ordered workspace pool and
+ * forgets the set-up, which the next call repeats. No call of this library may
+ * be in flight on another thread, and CUDA graphs captured earlier must not be
+ * replayed afterwards (their stream-K or scale workspaces came from that pool).
+ * The fixed scratch of fp8mx_gemm_noalloc and the status words are static and
+ * stay. Returns FP8BS_OK, or FP8BS_ERR_CUDA if a step failed (the rest is still
+ * released). A no-op when nothing was set up. */
+int fp8bs_shutdown(void);
 /* Configuration id fp8bs_gemm / fp8mx_gemm would choose for a shape on a
  * device with `num_sms` SMs (host-only, no CUDA calls). */
 int fp8bs_select_config(int M, int N, int K, int num_sms);

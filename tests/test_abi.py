@@ -183,6 +183,11 @@ def test_schedule_selection(lib):
     assert mx(256, 512, 512) == "tile"
 
 
+def test_shutdown_without_setup_is_a_noop(lib):
+    assert lib.lib().fp8bs_shutdown() == 0
+    lib.shutdown()
+
+
 def test_status_strings(lib):
     L = lib.lib()
     for code in range(-7, 1):

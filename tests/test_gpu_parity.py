@@ -704,3 +704,17 @@ def test_mxfp8_e4m3out_every_config(override, cfg, M, N, K):
     assert f.last_config_id() == cid
     codes, y = oracle.mxfp8_e4m3out(x.A, x.a_e8m0, x.B, x.b_e8m0, s)
     compare_e4m3(got, codes, y, s, f"mx e4m3out {cid} {M}x{N}x{K}")
+
+
+def test_shutdown_then_calls_set_up_again():
+    """fp8bs_shutdown releases the pools; the next calls (pooled stream-K and
+    scale workspaces included) set the device up again and are correct."""
+    import fp8_block_scaled_e4m3_gb300 as f
+    x = workloads.make_blockscale_inputs(256, 512, 7168, seed=61)   # stream-K shape (pooled workspace)
+    y = workloads.make_mxfp8_inputs(200, 264, 1280, seed=62)        # scale pack (pooled workspace)
+    want_x = oracle.blockscale(x.A, x.a_scale, x.B, x.b_scale)
+    want_y = oracle.mxfp8(y.A, y.a_e8m0, y.B, y.b_e8m0)
+    for _ in range(2):
+        compare(run_blockscale(x.A, x.a_scale, x.B, x.b_scale), want_x, "bs around shutdown")
+        compare(run_mxfp8(y.A, y.a_e8m0, y.B, y.b_e8m0), want_y, "mx around shutdown")
+        f.shutdown()
