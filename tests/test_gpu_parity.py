@@ -718,3 +718,51 @@ def test_shutdown_then_calls_set_up_again():
         compare(run_blockscale(x.A, x.a_scale, x.B, x.b_scale), want_x, "bs around shutdown")
         compare(run_mxfp8(y.A, y.a_e8m0, y.B, y.b_e8m0), want_y, "mx around shutdown")
         f.shutdown()
+
+
+# ------------------------------------------------ seeded random shapes, every entry point
+def _random_shapes(seed, n):
+    rng = np.random.Generator(np.random.PCG64(seed))
+    out = []
+    for _ in range(n):
+        M = int(rng.choice([1, 7, 64, 127, 128, 129, 200, 255, 256, 383, 520, 777]))
+        N = int(rng.choice([16, 48, 128, 144, 256, 272, 400, 512, 528, 784]))
+        K = 128 * int(rng.integers(1, 25))
+        out.append((M, N, K))
+    return out
+
+
+@pytest.mark.parametrize("M,N,K", _random_shapes(2026, 12))
+def test_random_shapes_every_entry_point(override, M, N, K):
+    """Seeded random shapes (tails in M and N, K from 128 to 3072) through every
+    entry point and every configuration that accepts the shape."""
+    import torch
+    import fp8_block_scaled_e4m3_gb300 as f
+    raster = 1 if M >= N else 0
+    x = workloads.make_blockscale_inputs(M, N, K, seed=M * 31 + N * 7 + K)
+    want = oracle.blockscale(x.A, x.a_scale, x.B, x.b_scale)
+    for cfg in (0, 1256401, 1128601, 1256402, 3128801):
+        if cfg:
+            override(cfg + raster * 10)
+        compare(run_blockscale(x.A, x.a_scale, x.B, x.b_scale), want, f"bs cfg {cfg} {M}x{N}x{K}")
+    override(0)
+    y = workloads.make_mxfp8_inputs(M, N, K, seed=M * 13 + N + K)
+    want_mx = oracle.mxfp8(y.A, y.a_e8m0, y.B, y.b_e8m0)
+    for cfg in (0, 2256401, 2128601, 2256402, 2128602):
+        if cfg:
+            override(cfg + raster * 10)
+        compare(run_mxfp8(y.A, y.a_e8m0, y.B, y.b_e8m0), want_mx, f"mx cfg {cfg} {M}x{N}x{K}")
+    override(0)
+    t = workloads.make_tensorscale_inputs(M, N, K, seed=M + N * 3 + K)
+    for cfg in (0, 4256401, 4128601, 4256402):
+        if cfg:
+            override(cfg + raster * 10)
+        got = f.gemm_tensorscale(to_dev(t.A), to_dev(t.B), float(t.alpha))
+        assert f.get_status() == 0
+        compare(got.view(torch.int16).cpu().numpy().view(np.uint16), oracle.tensorscale(t.A, t.B, float(t.alpha)),
+                f"twin cfg {cfg} {M}x{N}x{K}")
+    override(0)
+    if N % 16 == 0:
+        s = _c_scale(x)
+        codes, yv = oracle.blockscale_e4m3out(x.A, x.a_scale, x.B, x.b_scale, s)
+        compare_e4m3(_run_e4m3out(x, s), codes, yv, s, f"bs e4m3 {M}x{N}x{K}")
