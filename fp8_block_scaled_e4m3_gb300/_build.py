@@ -55,13 +55,13 @@ def parse_ptxas(log_path: str) -> dict:
 
 
 def check_resources(log_path: str) -> None:
-    """The blockscale, MXFP8 and tensor-scale kernels re-split their registers with
-    setmaxnreg (4 warps low, 8 high) out of a launch allotment of 384 threads x
-    168; that split is only valid when the kernel is compiled to exactly 168
-    registers. No kernel may spill."""
+    """The blockscale kernel and the stream-K MXFP8 and tensor-scale kernels
+    re-split their registers with setmaxnreg (4 warps low, 8 high) out of a
+    launch allotment of 384 threads x 168; that split is only valid when the
+    kernel is compiled to exactly 168 registers. No kernel may spill."""
     info = parse_ptxas(log_path)
     for sym, r in info.items():
-        split = any(k in sym for k in ("fp8bs_blockscale_kernel", "fp8bs_mxfp8_kernel", "fp8bs_tensorscale_kernel"))
+        split = any(k in sym for k in ("fp8bs_blockscale_kernel", "fp8bs_mxfp8_sk_kernel", "fp8bs_tensorscale_sk_kernel"))
         if split and r.get("registers") != 168:
             raise RuntimeError(f"{sym}: {r.get('registers')} registers, the setmaxnreg split needs 168")
         if r.get("spill_stores", 0) or r.get("spill_loads", 0):

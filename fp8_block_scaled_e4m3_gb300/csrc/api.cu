@@ -26,11 +26,8 @@ cudaError_t launch_blockscale_pair(const CUtensorMap &, const CUtensorMap &, con
 template <int STAGES>
 cudaError_t max_pair_clusters(int *);
 template <int BN, int STAGES>
-cudaError_t launch_mxfp8(const CUtensorMap &, const CUtensorMap &, const CUtensorMap &, const GemmArgs &, int,
-                         cudaStream_t);
-template <int BN, int STAGES>
-cudaError_t launch_tensorscale(const CUtensorMap &, const CUtensorMap &, const CUtensorMap &, const GemmArgs &, int,
-                               cudaStream_t);
+cudaError_t launch_mx_family(int kind, bool sk, const CUtensorMap &, const CUtensorMap &, const CUtensorMap &,
+                             const GemmArgs &, int, cudaStream_t);
 
 namespace host {
 
@@ -338,10 +335,12 @@ __global__ void pack_a_scale_kernel(const float *__restrict__ src, float *__rest
 // Tensor maps, arguments and launch of the MXFP8 kernel on packed scales
 // (cfg.kind 2) or of the tensor-scale twin (cfg.kind 4, no scale atoms, one
 // alpha): a persistent grid of min(tiles, SMs) CTAs, or the stream-K grid.
-int launch_mx(const Config &cfg, const void *A, const uint8_t *a_sf, const void *B, const uint8_t *b_sf, void *C,
-              int M, int N, int K, float alpha, int *status_ptr, int num_sms, cudaMemPool_t pool, cudaStream_t s,
+int launch_mx(Config &cfg, const void *A, const uint8_t *a_sf, const void *B, const uint8_t *b_sf, void *C, int M,
+              int N, int K, float alpha, int *status_ptr, int num_sms, cudaMemPool_t pool, cudaStream_t s,
               bool c_e4m3 = false, float c_scale = 1.f)
 {
+    if (c_e4m3)
+        cfg.sched = 1;   // the E4M3-output MXFP8 kernel runs one CTA per tile (cfg reports what ran)
     CUtensorMap tmA, tmB, tmC;
     if (!encode_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, A, K, M, K, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
         !encode_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, B, K, N, K, 128, cfg.block_n, CU_TENSOR_MAP_SWIZZLE_128B) ||
@@ -376,16 +375,12 @@ int launch_mx(const Config &cfg, const void *A, const uint8_t *a_sf, const void 
         if (rc)
             return rc;
     }
-    cudaError_t e;
-    if (cfg.kind == 4)
-        e = cfg.block_n == 256 ? launch_tensorscale<256, 4>(tmA, tmB, tmC, args, grid, s)
-                               : launch_tensorscale<128, 6>(tmA, tmB, tmC, args, grid, s);
-    else
-        e = cfg.block_n == 256 ? launch_mxfp8<256, 4>(tmA, tmB, tmC, args, grid, s)
-                               : launch_mxfp8<128, 6>(tmA, tmB, tmC, args, grid, s);
-    if (ws && cudaFreeAsync(ws, s) != cudaSuccess && e == cudaSuccess)
-        e = cudaErrorUnknown;
-    return e == cudaSuccess ? FP8BS_OK : FP8BS_ERR_LAUNCH;
+    const int family = cfg.kind == 4 ? 2 : (c_e4m3 ? 1 : 0);
+    const bool sk = cfg.sched == 2;
+    const cudaError_t e = cfg.block_n == 256 ? launch_mx_family<256, 4>(family, sk, tmA, tmB, tmC, args, grid, s)
+                                             : launch_mx_family<128, 6>(family, sk, tmA, tmB, tmC, args, grid, s);
+    const bool freed = !ws || cudaFreeAsync(ws, s) == cudaSuccess;
+    return e == cudaSuccess && freed ? FP8BS_OK : FP8BS_ERR_LAUNCH;
 }
 
 // The blockscale GEMM with a bf16 (c_e4m3 == false) or an E4M3 C.

@@ -38,14 +38,25 @@
 
 namespace fp8bs {
 
-constexpr int kMxThreads = (4 + kEpiWarps) * 32;
-// Register split (setmaxnreg) out of the launch allotment of 384 threads x 168:
-// the control warpgroup drops to kMxRegsLow, the two epilogue warpgroups rise
-// to kMxRegsHigh (128 * 64 + 256 * 216 <= 384 * 168). The epilogue holds a
-// thread's 128 accumulator columns in registers through the stream-K hand-off.
+// Kernel variants (one instance each, so that the common path carries no code
+// it does not run: with the stream-K hand-off and the E4M3 store compiled into
+// one kernel, 16384x5120x2048 measured 136.9 us against 125.3 us without
+// either, and the stream-K register split below cost another 3.6%):
+//   kMxPlain  one CTA per tile, bf16 C: 10 warps (producer, issuer, 8 epilogue)
+//   kMxSplitK stream-K, bf16 C: 12 warps with a register split (the epilogue
+//             holds a thread's accumulator columns through the hand-off)
+//   kMxE4m3   one CTA per tile, E4M3 C (MXFP8 only): 10 warps
+constexpr int kMxPlain = 0;
+constexpr int kMxSplitK = 1;
+constexpr int kMxE4m3 = 2;
+template <int V> constexpr int kMxCtrlWarps = V == kMxSplitK ? 4 : 2;
+template <int V> constexpr int kMxThreads = (kMxCtrlWarps<V> + kEpiWarps) * 32;
+// Register split of the stream-K variant (setmaxnreg) out of the launch
+// allotment of 384 threads x 168: the control warpgroup drops to kMxRegsLow,
+// the two epilogue warpgroups rise to kMxRegsHigh.
 constexpr int kMxRegsLow = 64;
 constexpr int kMxRegsHigh = 216;
-static_assert(128 * kMxRegsLow + 256 * kMxRegsHigh <= kMxThreads * 168, "register split");
+static_assert(128 * kMxRegsLow + 256 * kMxRegsHigh <= kMxThreads<kMxSplitK> * 168, "register split");
 
 template <int BN, int STAGES, bool MX = true>
 struct MxLayout {
@@ -77,7 +88,7 @@ struct MxLayout {
 // Body of both kernels below. MX: block-scaled MMAs with the ue8m0 scale atoms
 // staged per K step; !MX: plain fp8 MMAs and one per-tensor scale (args.alpha)
 // applied in the epilogue, i.e. the same MMA work with no per-block scaling.
-template <int BN, int STAGES, bool MX>
+template <int BN, int STAGES, bool MX, int V>
 __device__ __forceinline__ void mx_gemm_body(const CUtensorMap &tmA, const CUtensorMap &tmB, const CUtensorMap &tmC,
                                              const GemmArgs &args)
 {
@@ -120,8 +131,10 @@ __device__ __forceinline__ void mx_gemm_body(const CUtensorMap &tmA, const CUten
     ptx::tc_fence_after();
     const uint32_t tmem_base = *tmem_holder;
 
-    if (warp < 4) {
-    ptx::setmaxnreg_dec<kMxRegsLow>();
+    constexpr int CTRL = kMxCtrlWarps<V>;
+    if (warp < CTRL) {
+    if constexpr (V == kMxSplitK)
+        ptx::setmaxnreg_dec<kMxRegsLow>();
     if (warp == 0) {
         // ------------------------------------------------------------ producer
         if (lane == 0) {
@@ -225,11 +238,12 @@ __device__ __forceinline__ void mx_gemm_body(const CUtensorMap &tmA, const CUten
         }
     }
     } else {
-        ptx::setmaxnreg_inc<kMxRegsHigh>();
+        if constexpr (V == kMxSplitK)
+            ptx::setmaxnreg_inc<kMxRegsHigh>();
         // ------------------------------------------------------ epilogue
         constexpr int HALF = BN / 2;
-        constexpr bool kSk = true;              // both tile widths carry the stream-K hand-off
-        const int ew = warp - 4;                // 0..7
+        constexpr bool kSk = V == kMxSplitK;    // the stream-K hand-off
+        const int ew = warp - CTRL;             // 0..7
         const int wg = ew >> 2;
         const int q = warp & 3;
         const int row = q * 32 + lane;          // row of the tile
@@ -323,7 +337,7 @@ __device__ __forceinline__ void mx_gemm_body(const CUtensorMap &tmA, const CUten
             }
             const int x0 = nb * BN + wg * HALF;
             const int y0 = mb * kBlockM + q * 32;
-            if (MX && args.c_e4m3) {
+            if constexpr (MX && V == kMxE4m3) {
 #pragma unroll
                 for (int c = 0; c < HALF / 64; ++c)
                     store_c8_chunk(&tmC, cstage, lane, v + c * 64, args.c_scale, x0 + c * 64, y0, args.M, args.N);
@@ -346,64 +360,81 @@ __device__ __forceinline__ void mx_gemm_body(const CUtensorMap &tmA, const CUten
     }
 }
 
-template <int BN, int STAGES>
-__global__ void __launch_bounds__(kMxThreads, 1)
+// The MXFP8 GEMM, one CTA per tile: bf16 C (V = kMxPlain) or E4M3 C (kMxE4m3).
+template <int BN, int STAGES, int V>
+__global__ void __launch_bounds__(kMxThreads<V>, 1)
     fp8bs_mxfp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                        const __grid_constant__ CUtensorMap tmC, const GemmArgs args)
 {
-    mx_gemm_body<BN, STAGES, true>(tmA, tmB, tmC, args);
+    mx_gemm_body<BN, STAGES, true, V>(tmA, tmB, tmC, args);
+}
+
+// The MXFP8 GEMM under stream-K.
+template <int BN, int STAGES>
+__global__ void __launch_bounds__(kMxThreads<kMxSplitK>, 1)
+    fp8bs_mxfp8_sk_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                          const __grid_constant__ CUtensorMap tmC, const GemmArgs args)
+{
+    mx_gemm_body<BN, STAGES, true, kMxSplitK>(tmA, tmB, tmC, args);
 }
 
 // Promote-free ceiling twin of the blockscale GEMM (skill card "FlyDSL fp8
 // blockscale GEMM", section "Bottleneck diagnosis": the same kernel with one
 // per-tensor scale, i.e. identical MMA work): C = bf16(alpha * A.B^T).
 template <int BN, int STAGES>
-__global__ void __launch_bounds__(kMxThreads, 1)
+__global__ void __launch_bounds__(kMxThreads<kMxPlain>, 1)
     fp8bs_tensorscale_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                              const __grid_constant__ CUtensorMap tmC, const GemmArgs args)
 {
-    mx_gemm_body<BN, STAGES, false>(tmA, tmB, tmC, args);
+    mx_gemm_body<BN, STAGES, false, kMxPlain>(tmA, tmB, tmC, args);
 }
 
-template <int BN, int STAGES, bool MX>
-cudaError_t launch_mx_or_tensorscale(const CUtensorMap &tmA, const CUtensorMap &tmB, const CUtensorMap &tmC,
-                                     const GemmArgs &args, int grid, cudaStream_t stream)
+template <int BN, int STAGES>
+__global__ void __launch_bounds__(kMxThreads<kMxSplitK>, 1)
+    fp8bs_tensorscale_sk_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                                const __grid_constant__ CUtensorMap tmC, const GemmArgs args)
 {
-    using L = MxLayout<BN, STAGES, MX>;
-    auto kern = MX ? fp8bs_mxfp8_kernel<BN, STAGES> : fp8bs_tensorscale_kernel<BN, STAGES>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::DYN_SMEM);
+    mx_gemm_body<BN, STAGES, false, kMxSplitK>(tmA, tmB, tmC, args);
+}
+
+template <int BN, int STAGES, bool MX, int V, typename Kern>
+cudaError_t launch_mx_kernel(Kern kern, const CUtensorMap &tmA, const CUtensorMap &tmB, const CUtensorMap &tmC,
+                             const GemmArgs &args, int grid, cudaStream_t stream)
+{
+    constexpr int DYN_SMEM = MxLayout<BN, STAGES, MX>::DYN_SMEM;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, DYN_SMEM);
     if (e != cudaSuccess)
         return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
-    cfg.blockDim = dim3(kMxThreads);
-    cfg.dynamicSmemBytes = L::DYN_SMEM;
+    cfg.blockDim = dim3(kMxThreads<V>);
+    cfg.dynamicSmemBytes = DYN_SMEM;
     cfg.stream = stream;
     return cudaLaunchKernelEx(&cfg, kern, tmA, tmB, tmC, args);
 }
 
+// kind: 0 MXFP8 bf16 C, 1 MXFP8 E4M3 C, 2 tensor-scale twin; sk: stream-K.
 template <int BN, int STAGES>
-cudaError_t launch_mxfp8(const CUtensorMap &tmA, const CUtensorMap &tmB, const CUtensorMap &tmC,
-                         const GemmArgs &args, int grid, cudaStream_t stream)
+cudaError_t launch_mx_family(int kind, bool sk, const CUtensorMap &tmA, const CUtensorMap &tmB,
+                             const CUtensorMap &tmC, const GemmArgs &args, int grid, cudaStream_t stream)
 {
-    return launch_mx_or_tensorscale<BN, STAGES, true>(tmA, tmB, tmC, args, grid, stream);
+    if (kind == 2)
+        return sk ? launch_mx_kernel<BN, STAGES, false, kMxSplitK>(fp8bs_tensorscale_sk_kernel<BN, STAGES>, tmA, tmB, tmC,
+                                                             args, grid, stream)
+                  : launch_mx_kernel<BN, STAGES, false, kMxPlain>(fp8bs_tensorscale_kernel<BN, STAGES>, tmA, tmB, tmC, args,
+                                                            grid, stream);
+    if (kind == 1)
+        return launch_mx_kernel<BN, STAGES, true, kMxE4m3>(fp8bs_mxfp8_kernel<BN, STAGES, kMxE4m3>, tmA, tmB, tmC, args,
+                                                      grid, stream);
+    return sk ? launch_mx_kernel<BN, STAGES, true, kMxSplitK>(fp8bs_mxfp8_sk_kernel<BN, STAGES>, tmA, tmB, tmC, args, grid,
+                                                         stream)
+              : launch_mx_kernel<BN, STAGES, true, kMxPlain>(fp8bs_mxfp8_kernel<BN, STAGES, kMxPlain>, tmA, tmB, tmC, args,
+                                                        grid, stream);
 }
 
-template <int BN, int STAGES>
-cudaError_t launch_tensorscale(const CUtensorMap &tmA, const CUtensorMap &tmB, const CUtensorMap &tmC,
-                               const GemmArgs &args, int grid, cudaStream_t stream)
-{
-    return launch_mx_or_tensorscale<BN, STAGES, false>(tmA, tmB, tmC, args, grid, stream);
-}
-
-template cudaError_t launch_mxfp8<256, 4>(const CUtensorMap &, const CUtensorMap &, const CUtensorMap &,
-                                          const GemmArgs &, int, cudaStream_t);
-template cudaError_t launch_mxfp8<128, 6>(const CUtensorMap &, const CUtensorMap &, const CUtensorMap &,
-                                          const GemmArgs &, int, cudaStream_t);
-
-template cudaError_t launch_tensorscale<256, 4>(const CUtensorMap &, const CUtensorMap &, const CUtensorMap &,
-                                                const GemmArgs &, int, cudaStream_t);
-template cudaError_t launch_tensorscale<128, 6>(const CUtensorMap &, const CUtensorMap &, const CUtensorMap &,
-                                                const GemmArgs &, int, cudaStream_t);
+template cudaError_t launch_mx_family<256, 4>(int, bool, const CUtensorMap &, const CUtensorMap &,
+                                              const CUtensorMap &, const GemmArgs &, int, cudaStream_t);
+template cudaError_t launch_mx_family<128, 6>(int, bool, const CUtensorMap &, const CUtensorMap &,
+                                              const CUtensorMap &, const GemmArgs &, int, cudaStream_t);
 
 } // namespace fp8bs
