@@ -120,7 +120,9 @@ int fp8mx_gemm(const void *A, const uint8_t *a_e8m0, const void *B, const uint8_
 /*
  * fp8mx_gemm with an E4M3 C: C8[m,n] = e4m3(c_scale * the fp32 sum), rounded
  * and saturated as fp8bs_gemm_e4m3out; N % 16 == 0. Other arguments, launches
- * and errors as fp8mx_gemm.
+ * and errors as fp8mx_gemm, except that it always runs one CTA per tile (a
+ * stream-K configuration, chosen or forced, runs as its one-per-tile twin and
+ * is reported so).
  */
 int fp8mx_gemm_e4m3out(const void *A, const uint8_t *a_e8m0, const void *B, const uint8_t *b_e8m0, void *C8,
                        float c_scale, int M, int N, int K, void *stream);
