@@ -141,18 +141,8 @@ __device__ __forceinline__ void mx_gemm_body(const CUtensorMap &tmA, const CUten
             ptx::prefetch_tmap(&tmA);
             ptx::prefetch_tmap(&tmB);
             const int n_blocks = (args.N + 127) / 128;   // packed atoms per K step of B
-            WorkSpan span;
-            span.init(args, KS);
-            int it = 0;
-            int t, ks, mb = 0, nb = 0;
-            span.step(0, t, ks);
-            for (; it < span.total; ++it, span.advance(it, t, ks)) {
-                if (it == 0 || ks == 0 || it == span.dp_steps)   // a new tile (a stream-K range may start mid-tile)
-                    args.raster.coords(t, mb, nb);
-                const int s = it % STAGES;
-                const uint32_t ph = (it / STAGES) & 1;
-                if (!wait_bounded(empty_bar(s), ph ^ 1, abort_flag, args))
-                    break;
+            // Stage s <- K step ks of tile (mb, nb).
+            auto load_step = [&](int s, int ks, int mb, int nb) {
                 ptx::mbar_arrive_expect_tx(full_bar(s), L::A_BYTES + L::B_BYTES + L::SF_BYTES);
                 ptx::tma_load_2d(sbase + L::OFF_A + s * L::A_BYTES, &tmA, full_bar(s), ks * kBlockK, mb * kBlockM);
                 ptx::tma_load_2d(sbase + L::OFF_B + s * L::B_BYTES, &tmB, full_bar(s), ks * kBlockK, nb * BN);
@@ -170,6 +160,36 @@ __device__ __forceinline__ void mx_gemm_body(const CUtensorMap &tmA, const CUten
                                        args.b_sf + (static_cast<size_t>(bblk) * KS + ks) * 512, 512, full_bar(s));
                     }
                 }
+            };
+            int it = 0;
+            if constexpr (V != kMxSplitK) {
+                // one CTA per tile: tiles blockIdx.x, + gridDim.x, ...
+                bool ok = true;
+                for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+                    int mb, nb;
+                    args.raster.coords(t, mb, nb);
+                    for (int ks = 0; ks < KS; ++ks, ++it) {
+                        const int s = it % STAGES;
+                        if (!wait_bounded(empty_bar(s), ((it / STAGES) & 1) ^ 1, abort_flag, args)) {
+                            ok = false;
+                            break;
+                        }
+                        load_step(s, ks, mb, nb);
+                    }
+                }
+            } else {
+                WorkSpan span;
+                span.init(args, KS);
+                int t, ks, mb = 0, nb = 0;
+                span.step(0, t, ks);
+                for (; it < span.total; ++it, span.advance(it, t, ks)) {
+                    if (it == 0 || ks == 0 || it == span.dp_steps)   // a new tile (a range may start mid-tile)
+                        args.raster.coords(t, mb, nb);
+                    const int s = it % STAGES;
+                    if (!wait_bounded(empty_bar(s), ((it / STAGES) & 1) ^ 1, abort_flag, args))
+                        break;
+                    load_step(s, ks, mb, nb);
+                }
             }
             for (int s = 0; s < STAGES; ++s) {
                 const int uses = it > s ? (it - s + STAGES - 1) / STAGES : 0;
@@ -182,36 +202,17 @@ __device__ __forceinline__ void mx_gemm_body(const CUtensorMap &tmA, const CUten
         // One accumulation per segment: the K steps of one tile in this CTA's
         // range (a whole tile, or a piece of a tile cut by stream-K).
         if (lane == 0) {
-            WorkSpan span;
-            span.init(args, KS);
-            bool ok = true;
-            for (int it = 0, sg = 0; it < span.total && ok; ++sg) {
-                int t, ks0;
-                span.step(it, t, ks0);
-                const int seg_end = it + ((KS - ks0) < (span.total - it) ? (KS - ks0) : (span.total - it));
-                if (!wait_bounded(acc_empty_bar, (sg & 1) ^ 1, abort_flag, args))
-                    break;
-                ptx::tc_fence_after();
-                const int seg_start = it;
-                for (; it < seg_end; ++it) {
-                    const int s = it % STAGES;
-                    const uint32_t ph = (it / STAGES) & 1;
-                    if (!wait_bounded(full_bar(s), ph, abort_flag, args)) {
-                        ok = false;
-                        break;
-                    }
-                    ptx::tc_fence_after();
-                    if constexpr (!MX) {
-                        constexpr uint32_t idesc = ptx::idesc_f8f6f4_e4m3(kBlockM, BN);
-                        const uint64_t adesc = ptx::desc_kmajor_sw128(sbase + L::OFF_A + s * L::A_BYTES);
-                        const uint64_t bdesc = ptx::desc_kmajor_sw128(sbase + L::OFF_B + s * L::B_BYTES);
+            // The MMAs of the K step in stage s; `first` starts the accumulation.
+            auto issue_step = [&](int s, bool first) {
+                if constexpr (!MX) {
+                    constexpr uint32_t idesc = ptx::idesc_f8f6f4_e4m3(kBlockM, BN);
+                    const uint64_t adesc = ptx::desc_kmajor_sw128(sbase + L::OFF_A + s * L::A_BYTES);
+                    const uint64_t bdesc = ptx::desc_kmajor_sw128(sbase + L::OFF_B + s * L::B_BYTES);
 #pragma unroll
-                        for (int kk = 0; kk < kBlockK / kMmaK; ++kk)
-                            ptx::mma_f8f6f4(tmem_base, adesc + 2 * kk, bdesc + 2 * kk, idesc,
-                                            (it != seg_start || kk != 0) ? 1u : 0u);
-                        ptx::tc_commit(empty_bar(s));
-                        continue;
-                    }
+                    for (int kk = 0; kk < kBlockK / kMmaK; ++kk)
+                        ptx::mma_f8f6f4(tmem_base, adesc + 2 * kk, bdesc + 2 * kk, idesc,
+                                        (!first || kk != 0) ? 1u : 0u);
+                } else {
                     const uint32_t sf_smem = sbase + L::OFF_SF + s * L::SF_BYTES;
                     const uint32_t sfa_t = tmem_base + static_cast<uint32_t>(L::SF_COL0 + s * L::SF_COLS_PER_STAGE);
                     const uint32_t sfb_t = sfa_t + 4;
@@ -226,12 +227,54 @@ __device__ __forceinline__ void mx_gemm_body(const CUtensorMap &tmA, const CUten
                     for (int kk = 0; kk < kBlockK / kMmaK; ++kk)
                         ptx::mma_mxf8f6f4(tmem_base, adesc + 2 * kk, bdesc + 2 * kk,
                                           ptx::idesc_mxf8f6f4_e4m3(kBlockM, BN, kk, kk), sfa_t, sfb_t,
-                                          (it != seg_start || kk != 0) ? 1u : 0u);
-                    ptx::tc_commit(empty_bar(s));
+                                          (!first || kk != 0) ? 1u : 0u);
                 }
-                if (!ok)
-                    break;
-                ptx::tc_commit(acc_full_bar);
+                ptx::tc_commit(empty_bar(s));
+            };
+            bool ok = true;
+            if constexpr (V != kMxSplitK) {
+                int it = 0, titer = 0;
+                for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x, ++titer) {
+                    if (!wait_bounded(acc_empty_bar, (titer & 1) ^ 1, abort_flag, args))
+                        break;
+                    ptx::tc_fence_after();
+                    for (int ks = 0; ks < KS; ++ks, ++it) {
+                        const int s = it % STAGES;
+                        if (!wait_bounded(full_bar(s), (it / STAGES) & 1, abort_flag, args)) {
+                            ok = false;
+                            break;
+                        }
+                        ptx::tc_fence_after();
+                        issue_step(s, ks == 0);
+                    }
+                    if (!ok)
+                        break;
+                    ptx::tc_commit(acc_full_bar);
+                }
+            } else {
+                WorkSpan span;
+                span.init(args, KS);
+                for (int it = 0, sg = 0; it < span.total && ok; ++sg) {
+                    int t, ks0;
+                    span.step(it, t, ks0);
+                    const int seg_end = it + ((KS - ks0) < (span.total - it) ? (KS - ks0) : (span.total - it));
+                    if (!wait_bounded(acc_empty_bar, (sg & 1) ^ 1, abort_flag, args))
+                        break;
+                    ptx::tc_fence_after();
+                    const int seg_start = it;
+                    for (; it < seg_end; ++it) {
+                        const int s = it % STAGES;
+                        if (!wait_bounded(full_bar(s), (it / STAGES) & 1, abort_flag, args)) {
+                            ok = false;
+                            break;
+                        }
+                        ptx::tc_fence_after();
+                        issue_step(s, it == seg_start);
+                    }
+                    if (!ok)
+                        break;
+                    ptx::tc_commit(acc_full_bar);
+                }
             }
             ptx::tc_commit(mma_done_bar);
             wait_teardown(mma_done_bar, 0, args);
