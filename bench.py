@@ -1,11 +1,15 @@
 #!/usr/bin/env python
 """Benchmark: FP8 block-scaled GEMM (and MXFP8 GEMM) throughput on GB300.
 
-One "step" = one GEMM over one batch of synthetic inputs resident in HBM.
+One "step" = one GEMM over one batch of synthetic inputs resident in HBM
+(for the grouped MoE workloads: the leader descriptor plus the grouped GEMM).
 Prints ONE JSON line (rank 0). Default workload: the blockscale GEMM
-M=4096 N=2048 K=7168 (narrow-N, deep-K) at seed 0.
+M=4096 N=2048 K=7168 (narrow-N, deep-K) at seed 0. Blockscale lines also time
+the promote-free twin and the E4M3-output variant on the same operands; MoE
+lines time the unpaired arm beside the paired one.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+  python bench.py --ksweep [--workload bs_...]    # fixed + slope per K block, kernel vs twin
 
 Timing: W untimed steps, then K timed steps between a barrier +
 cuda.synchronize() on both sides. Before every step a 256 MiB buffer is

@@ -1,5 +1,10 @@
 """FP8 block-scaled GEMM and MXFP8 GEMM on GB300 (sm_103a).
 
+Entry points: gemm_blockscale, gemm_blockscale_e4m3out (E4M3 C), gemm_mxfp8,
+gemm_mxfp8_packed, gemm_mxfp8_e4m3out, gemm_tensorscale (the promote-free
+twin), moe_leaders + gemm_moe (grouped MoE stage-1 over 64-row sort blocks),
+plus the layout helpers, status and configuration introspection.
+
 Thin ctypes binding over libfp8bs.so (include/fp8bs.h). Every step of the
 computation runs in the library's CUDA kernels; this module only checks
 tensors, marshals pointers and the current CUDA stream, and raises on a
