@@ -766,3 +766,39 @@ def test_random_shapes_every_entry_point(override, M, N, K):
         s = _c_scale(x)
         codes, yv = oracle.blockscale_e4m3out(x.A, x.a_scale, x.B, x.b_scale, s)
         compare_e4m3(_run_e4m3out(x, s), codes, yv, s, f"bs e4m3 {M}x{N}x{K}")
+
+
+# ------------------------------------------------ size limits
+def test_maximum_k_every_entry_point():
+    """K at its limit (2^20, 8192 K blocks of one tile): blockscale (stream-K cuts
+    the single tile between many CTAs), MXFP8, the twin and the E4M3 output."""
+    import torch
+    import fp8_block_scaled_e4m3_gb300 as f
+    M, N, K = 2, 16, 1 << 20
+    x = workloads.make_blockscale_inputs(M, N, K, seed=71)
+    compare(run_blockscale(x.A, x.a_scale, x.B, x.b_scale), oracle.blockscale(x.A, x.a_scale, x.B, x.b_scale),
+            "bs K=2^20")
+    codes, yv = oracle.blockscale_e4m3out(x.A, x.a_scale, x.B, x.b_scale, 4.0)
+    compare_e4m3(_run_e4m3out(x, 4.0), codes, yv, 4.0, "bs e4m3 K=2^20")
+    y = workloads.make_mxfp8_inputs(M, N, K, seed=72)
+    compare(run_mxfp8(y.A, y.a_e8m0, y.B, y.b_e8m0), oracle.mxfp8(y.A, y.a_e8m0, y.B, y.b_e8m0), "mx K=2^20")
+    t = workloads.make_tensorscale_inputs(M, N, K, seed=73)
+    got = f.gemm_tensorscale(to_dev(t.A), to_dev(t.B), float(t.alpha))
+    assert f.get_status() == 0
+    compare(got.view(torch.int16).cpu().numpy().view(np.uint16), oracle.tensorscale(t.A, t.B, float(t.alpha)),
+            "twin K=2^20")
+
+
+def test_tall_m_sampled_rows():
+    """M = 2^17 rows (a_scale row stride, tile and row indices far from small
+    values): sampled rows of blockscale and MXFP8 against the oracle."""
+    M, N, K = 1 << 17, 16, 128
+    rng = np.random.Generator(np.random.PCG64(74))
+    rows = np.sort(rng.choice(M, 64, replace=False))
+    rows[-1] = M - 1
+    x = workloads.make_blockscale_inputs(M, N, K, seed=75)
+    got = run_blockscale(x.A, x.a_scale, x.B, x.b_scale)
+    compare(got[rows], oracle.blockscale(x.A[rows], x.a_scale[rows], x.B, x.b_scale), "bs M=2^17")
+    y = workloads.make_mxfp8_inputs(M, N, K, seed=76)
+    got = run_mxfp8(y.A, y.a_e8m0, y.B, y.b_e8m0)
+    compare(got[rows], oracle.mxfp8(y.A[rows], y.a_e8m0[rows], y.B, y.b_e8m0), "mx M=2^17")
