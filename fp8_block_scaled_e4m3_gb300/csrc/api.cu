@@ -25,6 +25,11 @@ cudaError_t launch_blockscale_pair(const CUtensorMap &, const CUtensorMap &, con
                                    const GemmArgs &, int, cudaStream_t);
 template <int STAGES>
 cudaError_t max_pair_clusters(int *);
+template <int STAGES>
+cudaError_t launch_mxfp8_pair(const CUtensorMap &, const CUtensorMap &, const CUtensorMap &, const CUtensorMap &,
+                              const CUtensorMap &, const GemmArgs &, int, cudaStream_t);
+template <int STAGES>
+cudaError_t max_mx_pair_clusters(int *);
 template <int BN, int STAGES>
 cudaError_t launch_mx_family(int kind, bool sk, const CUtensorMap &, const CUtensorMap &, const CUtensorMap &,
                              const GemmArgs &, int, cudaStream_t);
@@ -36,6 +41,7 @@ __device__ int g_status_word;   // per-device status written by the kernels
 constexpr int kMaxDevices = 64;
 constexpr unsigned long long kDefaultWaitLimitNs = 2000000000ull;
 constexpr int kPairStages = 8;
+constexpr int kMxPairStages = 6;
 
 struct DeviceState {
     bool ready = false;
@@ -44,6 +50,7 @@ struct DeviceState {
     int *status_ptr = nullptr;      // device address of g_status_word
     cudaMemPool_t pool = nullptr;   // stream-ordered pool for fp8mx_gemm's packed scales
     int pair_clusters = 0;          // co-resident CTA pairs of the pair kernel
+    int mx_pair_clusters = 0;       // co-resident CTA pairs of the MXFP8 pair kernel
 };
 
 std::mutex g_mutex;
@@ -90,6 +97,8 @@ int ensure_device(int &dev, DeviceState *&st)
         return st->status = FP8BS_ERR_CUDA;
     if (max_pair_clusters<kPairStages>(&st->pair_clusters) != cudaSuccess || st->pair_clusters < 1)
         return st->status = FP8BS_ERR_CUDA;
+    if (max_mx_pair_clusters<kMxPairStages>(&st->mx_pair_clusters) != cudaSuccess || st->mx_pair_clusters < 1)
+        return st->status = FP8BS_ERR_CUDA;
     if (!g_encode) {
         cudaDriverEntryPointQueryResult q;
         void *fn = nullptr;
@@ -132,7 +141,8 @@ int check_shape(int M, int N, int K)
 
 // Kernel configuration. kind 1: one-CTA blockscale kernel, 2: MXFP8 kernel,
 // 3: CTA-pair blockscale kernel (256 x 128 tiles over two SMs), 4: tensor-scale
-// twin (the MXFP8 kernel's pipeline with plain fp8 MMAs).
+// twin (the MXFP8 kernel's pipeline with plain fp8 MMAs), 5: CTA-pair MXFP8
+// kernel (256 x 256 tiles over two SMs).
 // sched 1: one CTA per tile; 2: stream-K (256-wide tile of kinds 1, 2 and 4).
 struct Config {
     int kind, block_n, stages, raster, sched;
@@ -161,6 +171,8 @@ bool decode_config_id(int id, Config &c)
         return (c.block_n == 256 && c.stages == 4) || (c.block_n == 128 && c.stages == 6);
     if (c.kind == 3)
         return c.block_n == 128 && c.stages == kPairStages;
+    if (c.kind == 5)
+        return c.block_n == 256 && c.stages == kMxPairStages && c.sched == 1;
     return false;
 }
 
@@ -341,6 +353,40 @@ int launch_mx(Config &cfg, const void *A, const uint8_t *a_sf, const void *B, co
 {
     if (c_e4m3)
         cfg.sched = 1;   // the E4M3-output MXFP8 kernel runs one CTA per tile (cfg reports what ran)
+    if (cfg.kind == 5) {
+        if (c_e4m3)
+            return FP8BS_ERR_SHAPE;   // the pair kernel stores bf16 only
+        const int KS = K / 128;
+        const uint64_t atoms_a = static_cast<uint64_t>((M + 127) / 128) * KS;
+        const uint64_t atoms_b = static_cast<uint64_t>((N + 127) / 128) * KS;
+        CUtensorMap tmA, tmB, tmSFA, tmSFB, tmC;
+        // a scale atom is 512 contiguous bytes: 4 rows of 128 in these tensors
+        if (!encode_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, A, K, M, K, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
+            !encode_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, B, K, N, K, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
+            !encode_2d(&tmSFA, CU_TENSOR_MAP_DATA_TYPE_UINT8, a_sf, 128, atoms_a * 4, 128, 128, 4,
+                       CU_TENSOR_MAP_SWIZZLE_NONE) ||
+            !encode_2d(&tmSFB, CU_TENSOR_MAP_DATA_TYPE_UINT8, b_sf, 128, atoms_b * 4, 128, 128, 4,
+                       CU_TENSOR_MAP_SWIZZLE_NONE) ||
+            !encode_2d(&tmC, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, C, N, M, static_cast<uint64_t>(N) * 2, kCChunkCols, 32,
+                       CU_TENSOR_MAP_SWIZZLE_64B))
+            return FP8BS_ERR_LAUNCH;
+        GemmArgs args = {};
+        args.M = M;
+        args.N = N;
+        args.K = K;
+        args.raster.m_tiles = (M + 2 * kBlockM - 1) / (2 * kBlockM);
+        args.raster.n_tiles = (N + 255) / 256;
+        args.raster.raster = cfg.raster;
+        args.raster.group = 1;
+        args.status = status_ptr;
+        args.wait_limit_ns = g_wait_limit_ns.load();
+        args.teardown_limit_ns = teardown_limit();
+        int dev = 0;
+        cudaGetDevice(&dev);
+        const cudaError_t e =
+            launch_mxfp8_pair<kMxPairStages>(tmA, tmB, tmSFA, tmSFB, tmC, args, g_dev[dev].mx_pair_clusters, s);
+        return e == cudaSuccess ? FP8BS_OK : FP8BS_ERR_LAUNCH;
+    }
     CUtensorMap tmA, tmB, tmC;
     if (!encode_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, A, K, M, K, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
         !encode_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, B, K, N, K, 128, cfg.block_n, CU_TENSOR_MAP_SWIZZLE_128B) ||
@@ -662,7 +708,7 @@ static int mx_gemm_packed_any(const void *A, const uint8_t *a_sf, const void *B,
     if ((rc = ensure_device(dev, st)))
         return rc;
     Config cfg = choose_config(2, M, N, K, st->num_sms);
-    if (!override_config(2, 2, cfg))
+    if (!override_config(2, 5, cfg))
         return FP8BS_ERR_SHAPE;
     if ((rc = launch_mx(cfg, A, a_sf, B, b_sf, C, M, N, K, 1.f, st->status_ptr, st->num_sms, st->pool,
                         static_cast<cudaStream_t>(stream), c_e4m3, c_scale)))
