@@ -276,6 +276,16 @@ Config choose_config(int kind, int M, int N, int K, int num_sms)
     if (tiles256 * 2 <= num_sms) {
         c.block_n = 128;
         c.stages = 6;
+        return c;
+    }
+    // MXFP8 with M >= 4096, one CTA per tile: the CTA-pair kernel (256 x 256
+    // tiles, half of B per CTA, six stages). Measured against the one-CTA
+    // kernel (us): 16384x5120x2048 121.5 -> 119.6, 16384x8192x1280 130.2 ->
+    // 126.3, 4096x8192x1280 42.8 -> 41.3, 4096x5120x2048 43.3 -> 42.8; at
+    // M <= 2048 it is no better.
+    if (kind == 2 && M >= 4096) {
+        c.kind = 5;
+        c.stages = 6;
     }
     return c;
 }
@@ -353,9 +363,11 @@ int launch_mx(Config &cfg, const void *A, const uint8_t *a_sf, const void *B, co
 {
     if (c_e4m3)
         cfg.sched = 1;   // the E4M3-output MXFP8 kernel runs one CTA per tile (cfg reports what ran)
+    if (cfg.kind == 5 && c_e4m3) {
+        cfg.kind = 2;     // the pair kernel stores bf16 only: E4M3 C goes through the one-CTA kernel
+        cfg.stages = 4;
+    }
     if (cfg.kind == 5) {
-        if (c_e4m3)
-            return FP8BS_ERR_SHAPE;   // the pair kernel stores bf16 only
         const int KS = K / 128;
         const uint64_t atoms_a = static_cast<uint64_t>((M + 127) / 128) * KS;
         const uint64_t atoms_b = static_cast<uint64_t>((N + 127) / 128) * KS;

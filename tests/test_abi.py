@@ -140,7 +140,11 @@ def test_config_selection(lib):
     # mxfp8: wide tiles, the narrow tile when the wide grid would starve the SMs
     assert lib.decode_config(lib.select_config("mx", 16384, 5120, 2048, 152))["block_n"] == 256
     assert lib.decode_config(lib.select_config("mx", 256, 512, 512, 152))["block_n"] == 128
-    assert lib.decode_config(lib.select_config("mx", 16384, 5120, 2048, 152))["kind"] == "mxfp8"
+    assert lib.decode_config(lib.select_config("mx", 16384, 5120, 2048, 152))["kind"] == "mxfp8_pair"
+    assert lib.decode_config(lib.select_config("mx", 2048, 8192, 1280, 152))["kind"] == "mxfp8"
+    assert lib.select_config("mx", 16384, 8192, 1280, 152) == 5256611
+    assert lib.lib().fp8bs_set_config_override(5256612) == -3   # no stream-K for the MXFP8 pair
+    assert lib.lib().fp8bs_set_config_override(5128611) == -3
     # raster streams the larger operand
     assert lib.decode_config(lib.select_config("bs", 4096, 65536, 1536, 152))["raster"] == 0
     assert lib.decode_config(lib.select_config("bs", 16384, 1536, 7168, 152))["raster"] == 1

@@ -35,7 +35,7 @@ def _call(kind, x):
         if kind == "e4m3":
             return lambda: f.gemm_blockscale_e4m3out(*d, 8.0)
         return lambda: f.gemm_blockscale(*d)
-    if kind in ("mx", "mx_sk"):
+    if kind in ("mx", "mx_sk", "mx_pair"):
         return lambda: f.gemm_mxfp8(to_dev(x.A), to_dev(x.a_e8m0), to_dev(x.B), to_dev(x.b_e8m0))
     if kind == "twin":
         return lambda: f.gemm_tensorscale(to_dev(x.A), to_dev(x.B), 1e-3)
@@ -48,10 +48,10 @@ def _call(kind, x):
     return moe
 
 
-OVERRIDE = {"bs_sk": 1256402, "mx_sk": 2256402}
+OVERRIDE = {"bs_sk": 1256402, "mx_sk": 2256402, "mx_pair": 5256601}
 
 
-@pytest.mark.parametrize("kind", ["bs", "bs_sk", "e4m3", "mx", "mx_sk", "twin", "moe"])
+@pytest.mark.parametrize("kind", ["bs", "bs_sk", "e4m3", "mx", "mx_sk", "mx_pair", "twin", "moe"])
 def test_every_path_reports_a_timeout_and_recovers(kind):
     """Stream-K included: a CTA that gives up never publishes its partial, and
     the finishers waiting for it run out of time as well instead of hanging."""

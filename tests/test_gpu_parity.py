@@ -180,7 +180,7 @@ def test_pack_a_scale_bit_exact():
 # every built kernel configuration, forced through the override
 # one-CTA 128x256, 128x128 (one CTA per tile), 128x256 stream-K, CTA-pair 256x128
 BS_CONFIGS = [1256411, 1128611, 1256412, 3128811]
-MX_CONFIGS = [2256411, 2128611, 2256412, 2128612]
+MX_CONFIGS = [2256411, 2128611, 2256412, 2128612, 5256611]
 
 
 @pytest.fixture
@@ -748,7 +748,7 @@ def test_random_shapes_every_entry_point(override, M, N, K):
     override(0)
     y = workloads.make_mxfp8_inputs(M, N, K, seed=M * 13 + N + K)
     want_mx = oracle.mxfp8(y.A, y.a_e8m0, y.B, y.b_e8m0)
-    for cfg in (0, 2256401, 2128601, 2256402, 2128602):
+    for cfg in (0, 2256401, 2128601, 2256402, 2128602, 5256601):
         if cfg:
             override(cfg + raster * 10)
         compare(run_mxfp8(y.A, y.a_e8m0, y.B, y.b_e8m0), want_mx, f"mx cfg {cfg} {M}x{N}x{K}")
@@ -802,3 +802,47 @@ def test_tall_m_sampled_rows():
     y = workloads.make_mxfp8_inputs(M, N, K, seed=76)
     got = run_mxfp8(y.A, y.a_e8m0, y.B, y.b_e8m0)
     compare(got[rows], oracle.mxfp8(y.A[rows], y.a_e8m0[rows], y.B, y.b_e8m0), "mx M=2^17")
+
+
+@pytest.mark.parametrize("M,N,K", [(4096, 1280, 1280), (4100, 776, 384), (257, 264, 3840), (1, 16, 128)])
+def test_mxfp8_pair_kernel(override, M, N, K):
+    """The CTA-pair MXFP8 kernel (256 x 256 tiles over two SMs): M and N tails,
+    an odd number of 128-row B blocks, a single row; and the E4M3 output, which
+    runs through the one-CTA kernel when the pair is forced."""
+    import fp8_block_scaled_e4m3_gb300 as f
+    cid = 5256601 + (10 if M >= N else 0)
+    override(cid)
+    y = workloads.make_mxfp8_inputs(M, N, K, seed=M + 3 * N + K)
+    got = run_mxfp8(y.A, y.a_e8m0, y.B, y.b_e8m0)
+    assert f.last_config_id() == cid
+    compare(got, oracle.mxfp8(y.A, y.a_e8m0, y.B, y.b_e8m0), f"mx pair {M}x{N}x{K}")
+    if N % 16 == 0:
+        s = 16.0
+        c8 = f.gemm_mxfp8_e4m3out(to_dev(y.A), to_dev(y.a_e8m0), to_dev(y.B), to_dev(y.b_e8m0), s).cpu().numpy()
+        assert f.get_status() == 0
+        assert f.decode_config(f.last_config_id())["kind"] == "mxfp8"
+        codes, yv = oracle.mxfp8_e4m3out(y.A, y.a_e8m0, y.B, y.b_e8m0, s)
+        compare_e4m3(c8, codes, yv, s, f"mx pair e4m3 fallback {M}x{N}x{K}")
+
+
+def test_mxfp8_pair_graph_replay_and_repeat(override):
+    import torch
+    import fp8_block_scaled_e4m3_gb300 as f
+    override(5256611)
+    M, N, K = 1024, 512, 1280
+    x0, x1 = (workloads.make_mxfp8_inputs(M, N, K, seed=s) for s in (81, 82))
+    d = [to_dev(x0.A), to_dev(x0.a_e8m0), to_dev(x0.B), to_dev(x0.b_e8m0)]
+    C = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    f.gemm_mxfp8(*d, C=C)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        f.gemm_mxfp8(*d, C=C)
+    for x in (x1, x0, x1):
+        for dst, src in zip(d, (x.A, x.a_e8m0, x.B, x.b_e8m0)):
+            dst.copy_(to_dev(src))
+        g.replay()
+        assert f.get_status() == 0
+        compare(C.view(torch.int16).cpu().numpy().view(np.uint16), oracle.mxfp8(x.A, x.a_e8m0, x.B, x.b_e8m0),
+                "mx pair graph replay")
+    del g
