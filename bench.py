@@ -49,6 +49,18 @@ PAGE_US = {"mx_16384x5120x2048": 157.0, "mx_16384x8192x1280": 175.8, "mx_1024x51
 KERNEL_NAMES = {"bs": "fp8bs_blockscale_kernel", "mx": "fp8bs_mxfp8_kernel"}
 
 
+def kernel_name(decoded):
+    """The kernel a configuration runs (decoded configuration id)."""
+    kind, sched = decoded["kind"], decoded["schedule"]
+    if kind == "mxfp8_pair":
+        return "fp8bs_mxfp8_pair_kernel"
+    if kind == "mxfp8":
+        return "fp8bs_mxfp8_sk_kernel" if sched == "stream_k" else "fp8bs_mxfp8_kernel"
+    if kind == "blockscale_pair":
+        return "fp8bs_blockscale_pair_kernel"
+    return "fp8bs_blockscale_kernel"
+
+
 def parse():
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
@@ -102,9 +114,9 @@ def source_hash():
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(kind, workload):
+def profiled_traffic(kernel, workload):
     """DRAM bytes per launch from a committed ncu summary, if it was taken on this exact kernel source."""
-    path = os.path.join(ROOT, "profiles", f"{KERNEL_NAMES[kind]}_{workload}.txt")
+    path = os.path.join(ROOT, "profiles", f"{kernel}_{workload}.txt")
     if not os.path.exists(path):
         return None
     vals = {}
@@ -343,14 +355,15 @@ def run_ours(args):
     value = aggregate_tflops(world, flops, ms)
     peaks = load_peaks()
     kernel_tflops = flops / (kernel_ms * 1e-3) / 1e12
-    traffic = profiled_traffic(kind, args.workload)
+    kname = kernel_name(f.decode_config(cfg_id))
+    traffic = profiled_traffic(kname, args.workload)
     roofline = {"bound": "tensor", "achieved": kernel_tflops, "peak": peaks["fp8_tflops"], "unit": "TFLOP/s",
                 "frac": kernel_tflops / peaks["fp8_tflops"], "traffic": traffic,
                 "peak_source": f"{peaks['source']}: 2 x MEASURED_PEAKS bf16_tflops (fp8/bf16 nominal ratio 2)"
                 if peaks["source"] == "measured" else "fallback 2 x 1900 TFLOP/s bf16",
                 "algorithmic_bytes": algorithmic_bytes(kind, M, N, K),
                 "hbm_time_frac": (algorithmic_bytes(kind, M, N, K) / (peaks["hbm_gbs"] * 1e9)) / (kernel_ms * 1e-3),
-                "kernel": KERNEL_NAMES[kind], "kernel_ms": kernel_ms}
+                "kernel": kname, "kernel_ms": kernel_ms}
 
     twin = None
     if kind == "bs" and not args.no_twin:
@@ -619,7 +632,7 @@ def run_moe(args):
         achieved = 2.0 * x.A.shape[0] * N * K / (gemm_ms * 1e-3) / 1e12
         roofline = {"bound": "tensor", "achieved": achieved, "peak": peaks["fp8_tflops"], "unit": "TFLOP/s",
                     "frac": achieved / peaks["fp8_tflops"], "traffic": None}
-    roofline["traffic"] = profiled_traffic("bs", args.workload)
+    roofline["traffic"] = profiled_traffic("fp8bs_blockscale_kernel", args.workload)
     roofline.update({"kernel": "fp8bs_blockscale_kernel (grouped)", "kernel_ms": gemm_ms,
                      "algorithmic_bytes": nbytes, "hbm_time_us": t_hbm * 1e6, "tensor_time_us": t_tensor * 1e6,
                      "peak_source": f"{peaks['source']} (MEASURED_PEAKS hbm_gbs / 2 x bf16_tflops)"})
