@@ -11,7 +11,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libfp8bs.so")
-SOURCES = ["api.cu", "bs_kernel.cu", "bs2_kernel.cu", "mx_kernel.cu", "mx2_kernel.cu"]
+SOURCES = ["api.cu", "bs_kernel.cu", "bs2_kernel.cu", "mx_kernel.cu", "mx2_kernel.cu", "mxd_kernel.cu"]
 HEADERS = ["ptx.cuh", "common.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
@@ -34,7 +34,7 @@ def _stale() -> bool:
 
 
 def parse_ptxas(log_path: str) -> dict:
-    """{kernel symbol: {"registers": int, "spill_stores": int, "spill_loads": int}} from ptxas -v output."""
+    """{kernel symbol: {"registers": int, "stack": int, "spill_stores": int, "spill_loads": int}} from ptxas -v."""
     import re
     out, cur = {}, None
     with open(log_path) as f:
@@ -44,6 +44,9 @@ def parse_ptxas(log_path: str) -> dict:
                 cur = m.group(1)
                 out[cur] = {}
                 continue
+            m = re.search(r"(\d+) bytes stack frame", line)
+            if m and cur:
+                out[cur]["stack"] = int(m.group(1))
             m = re.search(r"(\d+) bytes spill stores, (\d+) bytes spill loads", line)
             if m and cur:
                 out[cur]["spill_stores"] = int(m.group(1))
@@ -58,14 +61,15 @@ def check_resources(log_path: str) -> None:
     """The blockscale kernel and the stream-K MXFP8 and tensor-scale kernels
     re-split their registers with setmaxnreg (4 warps low, 8 high) out of a
     launch allotment of 384 threads x 168; that split is only valid when the
-    kernel is compiled to exactly 168 registers. No kernel may spill."""
+    kernel is compiled to exactly 168 registers. No kernel may spill or keep
+    an array in local memory (a stack frame)."""
     info = parse_ptxas(log_path)
     for sym, r in info.items():
         split = any(k in sym for k in ("fp8bs_blockscale_kernel", "fp8bs_mxfp8_sk_kernel", "fp8bs_tensorscale_sk_kernel"))
         if split and r.get("registers") != 168:
             raise RuntimeError(f"{sym}: {r.get('registers')} registers, the setmaxnreg split needs 168")
-        if r.get("spill_stores", 0) or r.get("spill_loads", 0):
-            raise RuntimeError(f"{sym}: register spills {r}")
+        if r.get("spill_stores", 0) or r.get("spill_loads", 0) or r.get("stack", 0):
+            raise RuntimeError(f"{sym}: register spills or stack frame {r}")
 
 
 def build(force: bool = False, verbose: bool = False) -> str:

@@ -33,6 +33,10 @@ cudaError_t max_mx_pair_clusters(int *);
 template <int BN, int STAGES>
 cudaError_t launch_mx_family(int kind, bool sk, const CUtensorMap &, const CUtensorMap &, const CUtensorMap &,
                              const GemmArgs &, int, cudaStream_t);
+template <int MAXS>
+cudaError_t launch_mxfp8_decode(const CUtensorMap &, const CUtensorMap &, const GemmArgs &, cudaStream_t);
+template <int MAXS>
+cudaError_t max_mxfp8_decode_clusters(int, int *);
 
 namespace host {
 
@@ -51,6 +55,7 @@ struct DeviceState {
     cudaMemPool_t pool = nullptr;   // stream-ordered pool for fp8mx_gemm's packed scales
     int pair_clusters = 0;          // co-resident CTA pairs of the pair kernel
     int mx_pair_clusters = 0;       // co-resident CTA pairs of the MXFP8 pair kernel
+    int mxd_clusters[9] = {};       // co-resident clusters of the MXFP8 decode kernel by size (2..8), -1 unknown
 };
 
 std::mutex g_mutex;
@@ -173,7 +178,30 @@ bool decode_config_id(int id, Config &c)
         return c.block_n == 128 && c.stages == kPairStages;
     if (c.kind == 5)
         return c.block_n == 256 && c.stages == kMxPairStages && c.sched == 1;
+    if (c.kind == 6)
+        return c.block_n == 128 && c.stages == kMxdMaxSteps && c.sched == 1 && c.raster == 0;   // no tile raster
     return false;
+}
+
+// K slices per 128-column tile of the MXFP8 decode kernel (its cluster size):
+// enough that a slice (at most kMxdMaxSteps K steps) fits in shared memory
+// whole, and otherwise as many as one wave of CTAs on num_sms SMs allows, at
+// most the portable cluster size 8. 0 when the kernel does not apply (more than
+// one row of tiles, or a K that needs more than 8 slices).
+int mxd_slices(int M, int N, int K, int num_sms)
+{
+    const int tiles = (N + 127) / 128;
+    const int KS = K / 128;
+    if (M > 128 || KS < 1)
+        return 0;
+    const int s_min = (KS + kMxdMaxSteps - 1) / kMxdMaxSteps;
+    if (s_min > 8)
+        return 0;
+    const int s_fill = num_sms / tiles;
+    int S = s_fill > s_min ? s_fill : s_min;
+    if (S > KS)
+        S = KS;
+    return S > 8 ? 8 : S;
 }
 
 // Stream-K grid: every CTA gets at least max(8, KB/4) K blocks, so a tile is
@@ -290,13 +318,13 @@ Config choose_config(int kind, int M, int N, int K, int num_sms)
     return c;
 }
 
-bool override_config(int kind_a, int kind_b, Config &cfg)
+bool override_config(int kind_a, int kind_b, Config &cfg, int kind_c = -1)
 {
     const int ovr = g_config_override.load();
     if (!ovr)
         return true;
     Config o;
-    if (!decode_config_id(ovr, o) || (o.kind != kind_a && o.kind != kind_b))
+    if (!decode_config_id(ovr, o) || (o.kind != kind_a && o.kind != kind_b && o.kind != kind_c))
         return false;
     cfg = o;
     return true;
@@ -366,6 +394,43 @@ int launch_mx(Config &cfg, const void *A, const uint8_t *a_sf, const void *B, co
     if (cfg.kind == 5 && c_e4m3) {
         cfg.kind = 2;     // the pair kernel stores bf16 only: E4M3 C goes through the one-CTA kernel
         cfg.stages = 4;
+    }
+    int slices = cfg.kind == 6 ? mxd_slices(M, N, K, num_sms) : 0;
+    if (slices > 1) {
+        // Clusters of that size must fit on the device (queried once per size).
+        int dev = 0;
+        cudaGetDevice(&dev);
+        int &fit = g_dev[dev].mxd_clusters[slices];
+        if (fit == 0 && (max_mxfp8_decode_clusters<kMxdMaxSteps>(slices, &fit) != cudaSuccess || fit < 1))
+            fit = -1;
+        if (fit < 0)
+            slices = 0;
+    }
+    if (cfg.kind == 6 && (c_e4m3 || slices < 1)) {
+        // The decode kernel stores bf16 only and takes one row of tiles and a
+        // K of at most 8 slices: the one-CTA 128-wide kernel instead.
+        cfg.kind = 2;
+        cfg.block_n = 128;
+        cfg.stages = 6;
+        cfg.sched = 1;
+    }
+    if (cfg.kind == 6) {
+        CUtensorMap tmA, tmB;
+        if (!encode_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, A, K, M, K, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
+            !encode_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, B, K, N, K, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B))
+            return FP8BS_ERR_LAUNCH;
+        GemmArgs args = {};
+        args.M = M;
+        args.N = N;
+        args.K = K;
+        args.a_sf = a_sf;
+        args.b_sf = b_sf;
+        args.c_out = C;
+        args.kslices = slices;
+        args.status = status_ptr;
+        args.wait_limit_ns = g_wait_limit_ns.load();
+        args.teardown_limit_ns = teardown_limit();
+        return launch_mxfp8_decode<kMxdMaxSteps>(tmA, tmB, args, s) == cudaSuccess ? FP8BS_OK : FP8BS_ERR_LAUNCH;
     }
     if (cfg.kind == 5) {
         const int KS = K / 128;
@@ -720,7 +785,7 @@ static int mx_gemm_packed_any(const void *A, const uint8_t *a_sf, const void *B,
     if ((rc = ensure_device(dev, st)))
         return rc;
     Config cfg = choose_config(2, M, N, K, st->num_sms);
-    if (!override_config(2, 5, cfg))
+    if (!override_config(2, 5, cfg, 6))
         return FP8BS_ERR_SHAPE;
     if ((rc = launch_mx(cfg, A, a_sf, B, b_sf, C, M, N, K, 1.f, st->status_ptr, st->num_sms, st->pool,
                         static_cast<cudaStream_t>(stream), c_e4m3, c_scale)))

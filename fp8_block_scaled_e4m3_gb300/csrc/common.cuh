@@ -67,6 +67,10 @@ struct GemmArgs {
     unsigned long long sk_token;      // unique per call; a finisher resets the flag to 0
     int sk;
     int sk_dp;                        // stream-K: whole waves of tiles done one per CTA first
+    // MXFP8 decode kernel: K slices per tile (its partials use sk_partial, its
+    // per-tile arrival counters sk_flags) and the C it writes with plain stores.
+    int kslices;
+    void *c_out;
     // Grouped (MoE) blockscale GEMM: rows of A and C are sort blocks of
     // kMoeBlockRows rows, each owned by one expert; a tile is a leader (one or
     // two adjacent sort blocks of the same expert) x one N tile of that
@@ -81,6 +85,7 @@ struct GemmArgs {
 };
 
 constexpr int kMoeBlockRows = 64;     // MoE sort-block granularity (rows)
+constexpr int kMxdMaxSteps = 6;       // MXFP8 decode kernel: most K steps a CTA holds in shared memory
 
 // Where tile t sits: first rows of A/C and of B, its N tile, the expert (for
 // the b_scale rows) and how many of its 128 rows are stored.

@@ -97,6 +97,25 @@ __device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bu
 __device__ __forceinline__ void bulk_wait_read_le1() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
+// Named barrier `ID` over `N` threads (a multiple of 32) that also returns
+// the AND of `pred` over those threads.
+template <int ID, int N>
+__device__ __forceinline__ bool bar_red_and(bool pred)
+{
+    uint32_t r;
+    asm volatile(
+        "{\n"
+        ".reg .pred p, q;\n"
+        "setp.ne.u32 p, %1, 0;\n"
+        "bar.red.and.pred q, %2, %3, p;\n"
+        "selp.u32 %0, 1, 0, q;\n"
+        "}\n"
+        : "=r"(r)
+        : "r"(static_cast<uint32_t>(pred)), "n"(ID), "n"(N)
+        : "memory");
+    return r != 0;
+}
+
 // Make this thread's generic-proxy shared-memory writes visible to the async proxy.
 __device__ __forceinline__ void fence_proxy_async_smem()
 {
@@ -269,6 +288,24 @@ __device__ __forceinline__ uint32_t mapa_shared(uint32_t a, uint32_t rank)
     uint32_t r;
     asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(rank));
     return r;
+}
+
+// Loads from shared::cluster addresses (another CTA's shared memory, from mapa_shared).
+__device__ __forceinline__ float4 ld_cluster_v4_f32(uint32_t addr)
+{
+    float4 v;
+    asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "r"(addr)
+                 : "memory");
+    return v;
+}
+
+__device__ __forceinline__ uint32_t ld_cluster_u32(uint32_t addr)
+{
+    uint32_t v;
+    asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+    return v;
 }
 
 // All threads of every CTA of the cluster.

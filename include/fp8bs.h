@@ -272,8 +272,15 @@ const char *fp8bs_status_string(int status);
  * host thread launched (0 if none): kind*1000000 + block_n*1000 + stages*100 +
  * raster*10 + schedule; kind 1 = one-CTA blockscale kernel (128 x block_n
  * tiles), 2 = mxfp8 kernel, 3 = CTA-pair blockscale kernel (256 x block_n tiles
- * over two SMs), 4 = tensor-scale twin (fp8bs_gemm_tensorscale); schedule 1 =
- * one CTA per tile, 2 = stream-K (kinds 1, 2 and 4 with block_n 256 only). */
+ * over two SMs), 4 = tensor-scale twin (fp8bs_gemm_tensorscale), 5 = CTA-pair
+ * mxfp8 kernel (256 x 256 tiles over two SMs), 6 = mxfp8 decode kernel
+ * (6128601 only; selectable by fp8bs_set_config_override, never chosen by the
+ * shape rule: M <= 128, the K steps of each 128-column tile cut into up to 8
+ * slices that run as one thread-block cluster and add their fp32 partials in
+ * distributed shared memory, in slice order, so the result is the same on
+ * every call; a shape it does not take (M > 128, K > 6144, an E4M3 C) runs the
+ * one-CTA 128-wide kernel and reports 2128601); schedule 1 = one CTA per tile,
+ * 2 = stream-K (kinds 1, 2 and 4 with block_n 256, and kind 2 with block_n 128). */
 int fp8bs_last_config_id(void);
 /* Release what the library holds per device: waits for each device it set
  * up (cudaDeviceSynchronize), destroys its stream-ordered workspace pool and

@@ -157,7 +157,14 @@ def test_config_selection(lib):
     assert L.fp8bs_set_config_override(3128812) == -3      # no stream-K for the CTA pair
     assert L.fp8bs_set_config_override(1256413) == -3      # no such schedule
     assert L.fp8bs_set_config_override(1128612) == -3      # stream-K runs with the 256-wide tile only
+    # the MXFP8 decode kernel (K slices in clusters): selectable, one id only, never chosen by the rule
+    assert L.fp8bs_set_config_override(6128601) == 0
+    assert lib.decode_config(6128601)["kind"] == "mxfp8_decode"
+    for bad in (6256601, 6128401, 6128602, 6128611):
+        assert L.fp8bs_set_config_override(bad) == -3
     assert L.fp8bs_set_config_override(0) == 0
+    for M, N, K in [(1, 5120, 2048), (32, 8192, 1280), (128, 5120, 2048)]:
+        assert lib.decode_config(lib.select_config("mx", M, N, K, 152))["kind"] == "mxfp8"
 
 
 def test_schedule_selection(lib):

@@ -35,7 +35,7 @@ def _call(kind, x):
         if kind == "e4m3":
             return lambda: f.gemm_blockscale_e4m3out(*d, 8.0)
         return lambda: f.gemm_blockscale(*d)
-    if kind in ("mx", "mx_sk", "mx_pair"):
+    if kind in ("mx", "mx_sk", "mx_pair", "mx_decode"):
         return lambda: f.gemm_mxfp8(to_dev(x.A), to_dev(x.a_e8m0), to_dev(x.B), to_dev(x.b_e8m0))
     if kind == "twin":
         return lambda: f.gemm_tensorscale(to_dev(x.A), to_dev(x.B), 1e-3)
@@ -48,17 +48,21 @@ def _call(kind, x):
     return moe
 
 
-OVERRIDE = {"bs_sk": 1256402, "mx_sk": 2256402, "mx_pair": 5256601}
+OVERRIDE = {"bs_sk": 1256402, "mx_sk": 2256402, "mx_pair": 5256601, "mx_decode": 6128601}
 
 
-@pytest.mark.parametrize("kind", ["bs", "bs_sk", "e4m3", "mx", "mx_sk", "mx_pair", "twin", "moe"])
+@pytest.mark.parametrize("kind", ["bs", "bs_sk", "e4m3", "mx", "mx_sk", "mx_pair", "mx_decode", "twin", "moe"])
 def test_every_path_reports_a_timeout_and_recovers(kind):
     """Stream-K included: a CTA that gives up never publishes its partial, and
-    the finishers waiting for it run out of time as well instead of hanging."""
+    the finishers waiting for it run out of time as well instead of hanging.
+    In the decode kernel's clusters every CTA still reaches both cluster
+    barriers, and a partial marked invalid is never stored."""
     import torch
     import fp8_block_scaled_e4m3_gb300 as f
     if kind == "moe":
         x = workloads.make_moe_inputs(512, 2, 8, 256, 1024, seed=5, skew=1.0)
+    elif kind == "mx_decode":   # one row of tiles, 8 K slices per cluster
+        x = workloads.make_inputs("mx", 32, 1024, 2048, seed=4)
     else:
         x = workloads.make_inputs("mx" if kind.startswith("mx") else "bs", 256, 1024, 4096, seed=4)
     f.set_config_override(OVERRIDE.get(kind, 0))

@@ -846,3 +846,76 @@ def test_mxfp8_pair_graph_replay_and_repeat(override):
         compare(C.view(torch.int16).cpu().numpy().view(np.uint16), oracle.mxfp8(x.A, x.a_e8m0, x.B, x.b_e8m0),
                 "mx pair graph replay")
     del g
+
+
+# ------------------------------------------------ MXFP8 decode kernel (selectable)
+# (M, N, K, slices on 152 SMs): one slice (K = 128; or 512 tiles, several
+# waves); 2..8 slices in a cluster; ragged N; M of one to four 32-row groups.
+DECODE_CASES = [(1, 5120, 2048, 3), (32, 5120, 2048, 3), (33, 8192, 1280, 2), (128, 1536, 2048, 8),
+                (5, 1000, 896, 7), (3, 136, 128, 1), (9, 1024, 6144, 8), (100, 2048, 768, 6),
+                (20, 3840, 2048, 5), (64, 65536, 256, 1)]
+
+
+@pytest.mark.parametrize("M,N,K,slices", DECODE_CASES)
+def test_mxfp8_decode_kernel(override, M, N, K, slices):
+    """The decode kernel (K slices of one 128-column tile in a thread-block
+    cluster, partials added in distributed shared memory): oracle parity and
+    the same bits on a repeat call, at every slice count it takes."""
+    import torch
+    import fp8_block_scaled_e4m3_gb300 as f
+    override(6128601)
+    y = workloads.make_mxfp8_inputs(M, N, K, seed=M + N + K)
+    d = (to_dev(y.A), to_dev(y.a_e8m0), to_dev(y.B), to_dev(y.b_e8m0))
+    c1 = f.gemm_mxfp8(*d)
+    assert f.get_status() == 0
+    assert f.last_config_id() == 6128601
+    c2 = f.gemm_mxfp8(*d)
+    assert f.get_status() == 0
+    torch.cuda.synchronize()
+    assert torch.equal(c1.view(torch.int16), c2.view(torch.int16))
+    compare(c1.view(torch.int16).cpu().numpy().view(np.uint16), oracle.mxfp8(y.A, y.a_e8m0, y.B, y.b_e8m0),
+            f"mx decode {M}x{N}x{K} ({slices} slices)")
+
+
+def test_mxfp8_decode_kernel_falls_back(override):
+    """Shapes and outputs the decode kernel does not take run the one-CTA
+    128-wide kernel: more than one row of tiles, a K needing more than 8
+    slices, an E4M3 C."""
+    import fp8_block_scaled_e4m3_gb300 as f
+    override(6128601)
+    for M, N, K in [(129, 256, 512), (17, 512, 7168)]:
+        y = workloads.make_mxfp8_inputs(M, N, K, seed=7)
+        compare(run_mxfp8(y.A, y.a_e8m0, y.B, y.b_e8m0), oracle.mxfp8(y.A, y.a_e8m0, y.B, y.b_e8m0),
+                f"mx decode fallback {M}x{N}x{K}")
+        assert f.last_config_id() == 2128601
+    y = workloads.make_mxfp8_inputs(16, 1024, 2048, seed=8)
+    c8 = f.gemm_mxfp8_e4m3out(to_dev(y.A), to_dev(y.a_e8m0), to_dev(y.B), to_dev(y.b_e8m0), 16.0).cpu().numpy()
+    assert f.get_status() == 0
+    assert f.last_config_id() == 2128601
+    codes, yv = oracle.mxfp8_e4m3out(y.A, y.a_e8m0, y.B, y.b_e8m0, 16.0)
+    compare_e4m3(c8, codes, yv, 16.0, "mx decode e4m3 fallback")
+
+
+def test_mxfp8_decode_kernel_graph_replay(override):
+    """Captured once, replayed on new contents: the cluster hand-off holds no
+    state between launches."""
+    import torch
+    import fp8_block_scaled_e4m3_gb300 as f
+    override(6128601)
+    M, N, K = 16, 2048, 2048
+    x0, x1 = (workloads.make_mxfp8_inputs(M, N, K, seed=s) for s in (91, 92))
+    d = [to_dev(x0.A), to_dev(x0.a_e8m0), to_dev(x0.B), to_dev(x0.b_e8m0)]
+    C = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    f.gemm_mxfp8(*d, C=C)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        f.gemm_mxfp8(*d, C=C)
+    for x in (x1, x0, x1):
+        for dst, src in zip(d, (x.A, x.a_e8m0, x.B, x.b_e8m0)):
+            dst.copy_(to_dev(src))
+        g.replay()
+        assert f.get_status() == 0
+        compare(C.view(torch.int16).cpu().numpy().view(np.uint16), oracle.mxfp8(x.A, x.a_e8m0, x.B, x.b_e8m0),
+                "mx decode graph replay")
+    del g
