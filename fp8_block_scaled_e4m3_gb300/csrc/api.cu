@@ -55,7 +55,6 @@ struct DeviceState {
     cudaMemPool_t pool = nullptr;   // stream-ordered pool for fp8mx_gemm's packed scales
     int pair_clusters = 0;          // co-resident CTA pairs of the pair kernel
     int mx_pair_clusters = 0;       // co-resident CTA pairs of the MXFP8 pair kernel
-    int mxd_clusters[9] = {};       // co-resident clusters of the MXFP8 decode kernel by size (2..8), -1 unknown
 };
 
 std::mutex g_mutex;
@@ -63,6 +62,10 @@ DeviceState g_dev[kMaxDevices];
 std::atomic<unsigned long long> g_wait_limit_ns{kDefaultWaitLimitNs};
 std::atomic<int> g_config_override{0};
 std::atomic<unsigned long long> g_sk_token{0};   // stream-K hand-off tokens, unique per call
+// Whether clusters of n CTAs (2..8) of the MXFP8 decode kernel fit on a device:
+// 0 not yet asked, 1 yes, -1 no. A property of the device and the kernel, so it
+// survives fp8bs_shutdown; both entry paths (with and without the pool) use it.
+std::atomic<int> g_mxd_fit[kMaxDevices][9];
 thread_local int t_last_config = 0;
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
@@ -400,9 +403,12 @@ int launch_mx(Config &cfg, const void *A, const uint8_t *a_sf, const void *B, co
         // Clusters of that size must fit on the device (queried once per size).
         int dev = 0;
         cudaGetDevice(&dev);
-        int &fit = g_dev[dev].mxd_clusters[slices];
-        if (fit == 0 && (max_mxfp8_decode_clusters<kMxdMaxSteps>(slices, &fit) != cudaSuccess || fit < 1))
-            fit = -1;
+        int fit = dev >= 0 && dev < kMaxDevices ? g_mxd_fit[dev][slices].load() : -1;
+        if (fit == 0) {
+            int n = 0;
+            fit = max_mxfp8_decode_clusters<kMxdMaxSteps>(slices, &n) == cudaSuccess && n >= 1 ? 1 : -1;
+            g_mxd_fit[dev][slices].store(fit);
+        }
         if (fit < 0)
             slices = 0;
     }
