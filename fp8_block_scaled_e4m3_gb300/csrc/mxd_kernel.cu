@@ -113,6 +113,7 @@ __global__ void __launch_bounds__(kMxdThreads, 1)
     const uint32_t part_smem = sbase + L::OFF_A;
     float v[128];                 // epilogue: this thread's row of the accumulator
     bool epi_live = false;        // epilogue thread of a warp with a row below M, holding v
+    bool epi_ok = false;          // epilogue thread: no epilogue warp of this CTA gave up
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
@@ -203,9 +204,12 @@ __global__ void __launch_bounds__(kMxdThreads, 1)
                 }
             }
             // The partial of this CTA is whole only if no epilogue warp gave up.
-            const bool all_ok = ptx::bar_red_and<2, kMxdEpiWarps * 32>(ok);
+            // Every epilogue thread gets the answer from the barrier; the flag
+            // in shared memory is for slice 0 of the cluster, which reads it
+            // after the cluster barrier.
+            epi_ok = ptx::bar_red_and<2, kMxdEpiWarps * 32>(ok);
             if (threadIdx.x == 64)
-                *valid_flag = all_ok ? 1 : 0;
+                *valid_flag = epi_ok ? 1 : 0;
         }
     }
 
@@ -233,14 +237,14 @@ __global__ void __launch_bounds__(kMxdThreads, 1)
     };
 
     if (S == 1) {
-        if (epi_live && *valid_flag)
+        if (epi_live && epi_ok)
             store_row(v, 0, std::integral_constant<int, 16>{});
     } else {
         // Every CTA of the cluster, every thread, on every path (all waits
         // above are bounded): the partials and their valid flags are visible.
         ptx::cluster_sync();
         if (slice == 0 && epi_live) {
-            bool all_valid = *valid_flag != 0;
+            bool all_valid = epi_ok;
             for (int r = 1; r < S; ++r)
                 all_valid = all_valid && ptx::ld_cluster_u32(ptx::mapa_shared(sbase + L::OFF_MISC + 8, r)) != 0;
             if (all_valid) {

@@ -224,7 +224,8 @@ int fp8mx_pack_scales(const uint8_t *e8m0, uint8_t *packed, int rows, int K, voi
  * from a memory pool; this entry point uses a fixed device array of
  * fp8mx_noalloc_scratch_bytes() bytes (8 MiB) built into the library instead,
  * which every GPU that loads the library holds until the process exits. It
- * always runs one CTA per tile (stream-K would need a workspace).
+ * always runs one CTA per tile (stream-K would need a workspace); the MXFP8
+ * decode kernel (config 6128601, by override), which needs none, runs too.
  *
  * Limit: fp8mx_packed_scale_bytes(M, K) + fp8mx_packed_scale_bytes(N, K) must
  * not exceed that size, else FP8BS_ERR_SCRATCH_TOO_SMALL (checked on the host,

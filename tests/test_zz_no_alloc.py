@@ -62,3 +62,27 @@ def test_noalloc_matches_fp8mx_gemm_on_two_calls_in_a_row():
         ref = C_ref.view(torch.int16).cpu().numpy().view(np.uint16)
         got = C_new.view(torch.int16).cpu().numpy().view(np.uint16)
         compare(got, ref, f"noalloc vs fp8mx_gemm {M}x{N}x{K}")
+
+
+@pytest.mark.gpu
+def test_noalloc_runs_the_decode_kernel_when_forced():
+    """The MXFP8 decode kernel reduces its K slices in distributed shared
+    memory, so it needs no workspace and runs under the allocation-free entry."""
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import oracle
+    f, L = _lib()
+    M, N, K = 8, 1024, 2048
+    x = workloads.make_mxfp8_inputs(M, N, K, seed=13)
+    A, ea, B, eb = to_dev(x.A), to_dev(x.a_e8m0), to_dev(x.B), to_dev(x.b_e8m0)
+    C = torch.full((M, N), float("nan"), dtype=torch.bfloat16, device="cuda")
+    f.set_config_override(6128601)
+    try:
+        assert _call(L, L.fp8mx_gemm_noalloc, A, ea, B, eb, C, M, N, K) == 0
+        assert f.get_status() == 0
+        assert f.last_config_id() == 6128601
+    finally:
+        f.set_config_override(0)
+    compare(C.view(torch.int16).cpu().numpy().view(np.uint16), oracle.mxfp8(x.A, x.a_e8m0, x.B, x.b_e8m0),
+            "noalloc decode kernel")
