@@ -73,6 +73,13 @@ def parse():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-twin", action="store_true", help="skip the promote-free twin timing (blockscale)")
+    p.add_argument("--no-mx-gates", action="store_true",
+                   help="default line: skip timing the two gated MXFP8 workloads (M = 16384) beside it")
+    p.add_argument("--ref-seconds", type=float, default=240.0,
+                   help="reference arm: CPU time budget of the whole run (warm-up + timed steps)")
+    p.add_argument("--cpu-all", action="store_true",
+                   help="time the oracle on every workload (full C, all host cores) and on one core for the "
+                        "smallest blockscale and MXFP8 workloads; one JSON line, no GPU")
     p.add_argument("--ksweep", action="store_true",
                    help="blockscale: time the kernel and its twin over K at the workload's M, N; print the "
                         "fixed + slope fit (skill card 'Bottleneck diagnosis' step 6) instead of the bench line")
@@ -114,8 +121,9 @@ def source_hash():
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(kernel, workload):
-    """DRAM bytes per launch from a committed ncu summary, if it was taken on this exact kernel source."""
+def profiled_values(kernel, workload):
+    """Key/value lines of the committed ncu summary of this kernel on this workload,
+    or None when there is none or it was taken on other kernel sources."""
     path = os.path.join(ROOT, "profiles", f"{kernel}_{workload}.txt")
     if not os.path.exists(path):
         return None
@@ -127,10 +135,25 @@ def profiled_traffic(kernel, workload):
                 vals[k.strip()] = v.strip()
     if vals.get("source_hash") != source_hash():
         return None
+    return vals
+
+
+def _profiled_float(kernel, workload, key):
+    vals = profiled_values(kernel, workload)
     try:
-        return float(vals["dram_bytes_per_launch"])
+        return float(vals[key]) if vals else None
     except (KeyError, ValueError):
         return None
+
+
+def profiled_traffic(kernel, workload):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on this exact kernel source."""
+    return _profiled_float(kernel, workload, "dram_bytes_per_launch")
+
+
+def profiled_tensor_active(kernel, workload):
+    """ncu sm__pipe_tensor_cycles_active (% of peak sustained, elapsed) from the same summary."""
+    return _profiled_float(kernel, workload, "sm__pipe_tensor_cycles_active.pct_of_peak_sustained_elapsed")
 
 
 class ClockSampler:
@@ -237,27 +260,90 @@ def cpu_oracle_sample(kind, x, target_s):
                       f"fp64 dequantise + naive triple loop, OpenMP over rows"}
 
 
+def _oracle_fn(kind, x):
+    import oracle
+    if kind == "bs":
+        return lambda r0, r1: oracle.blockscale(x.A, x.a_scale, x.B, x.b_scale, rows=(r0, r1))
+    return lambda r0, r1: oracle.mxfp8(x.A, x.a_e8m0, x.B, x.b_e8m0, rows=(r0, r1))
+
+
 def run_reference(args):
+    """The oracle as it stands, timed on the host cores. Every step computes the
+    same rows of C: all of C when the whole run (warm-up + timed steps) fits the
+    --ref-seconds budget at the measured rate, else the first rows that do (the
+    line says how many). ms_per_step is the measured wall time of one step; the
+    value is the measured rate over those steps (nothing is extrapolated)."""
+    import oracle
     world, rank, _ = dist_setup(args)
     if rank != 0:
         return 0
     kind, M, N, K = workload_shape(args.workload)
     x = workloads.make_inputs(kind, M, N, K, args.seed)
-    per = []
-    cb = None
-    for i in range(args.warmup + args.steps):
-        cb = cpu_oracle_sample(kind, x, args.cpu_seconds / max(1, args.steps + args.warmup))
+    fn = _oracle_fn(kind, x)
+    threads = oracle.max_threads()
+    probe = min(M, max(threads, 8))
+    t0 = time.perf_counter()
+    fn(0, probe)
+    per_row = (time.perf_counter() - t0) / probe
+    n_steps = args.warmup + args.steps
+    rows = M if per_row * M * n_steps <= args.ref_seconds else \
+        int(min(M, max(threads, args.ref_seconds / (n_steps * per_row))))
+    walls = []
+    for i in range(n_steps):
+        t0 = time.perf_counter()
+        fn(0, rows)
+        dt = time.perf_counter() - t0
         if i >= args.warmup:
-            per.append(cb["value"])
-    val = statistics.mean(per)
-    flops = 2.0 * M * N * K
+            walls.append(dt)
+    ms = statistics.mean(walls) * 1e3
+    flops = 2.0 * rows * N * K
+    val = flops / (ms * 1e-3) / 1e12
+    what = "all of C" if rows == M else f"rows 0..{rows - 1} of C (bounded by --ref-seconds {args.ref_seconds:g})"
+    cb = {"value": val, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+          "sample": f"every step: {what}, {rows}x{N} outputs, full K={K}; fp64 dequantise + naive triple loop, "
+                    f"OpenMP over rows; mean step {ms / 1e3:.2f} s"}
     line = {"impl": "reference", "metric": METRIC, "value": val, "unit": "TFLOP/s", "n_gpus": args.gpus,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": flops / (val * 1e12) * 1e3,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": args.workload, "M": M, "N": N, "K": K, "seed": args.seed},
-            "cpu_baseline": dict(cb, value=val),
+            "rows_per_step": rows, "extrapolated": False,
+            "cpu_baseline": cb,
             "e2e": {"value": val, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_cpu_all(args):
+    """Oracle time on every blockscale and MXFP8 workload (seed 0, all of C, all
+    host cores), plus one core for the smallest blockscale workload and the
+    M = 1024 MXFP8 workloads (a child process with OMP_NUM_THREADS=1)."""
+    import oracle
+    import platform
+    out = {"cpu_all": True, "cores": oracle.max_threads(), "cpu": platform.processor() or platform.machine(),
+           "kind": "oracle", "what": "all of C per workload, seed 0, fp64 dequantise + naive triple loop, "
+                                     "OpenMP over rows", "workloads": {}}
+    for name, w in workloads.WORKLOADS.items():
+        if w["kind"] not in ("bs", "mx"):
+            continue
+        kind, M, N, K = workload_shape(name)
+        x = workloads.make_inputs(kind, M, N, K, 0)
+        fn = _oracle_fn(kind, x)
+        t0 = time.perf_counter()
+        fn(0, M)
+        dt = time.perf_counter() - t0
+        out["workloads"][name] = {"seconds": dt, "tflops": 2.0 * M * N * K / dt / 1e12}
+    single = {}
+    for name in ("bs_tiny_256x512x512", "mx_1024x5120x2048", "mx_1024x8192x1280"):
+        code = (f"import sys, time, json; sys.path.insert(0, {ROOT!r}); import bench, workloads, oracle; "
+                f"k, M, N, K = bench.workload_shape({name!r}); x = workloads.make_inputs(k, M, N, K, 0); "
+                f"fn = bench._oracle_fn(k, x); t0 = time.perf_counter(); fn(0, M); dt = time.perf_counter() - t0; "
+                f"print(json.dumps({{'threads': oracle.max_threads(), 'seconds': dt, "
+                f"'tflops': 2.0 * M * N * K / dt / 1e12}}))")
+        env = dict(os.environ, OMP_NUM_THREADS="1")
+        r = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True, timeout=900)
+        single[name] = json.loads(r.stdout.strip().splitlines()[-1]) if r.returncode == 0 else {"error": r.stderr[-300:]}
+    out["single_core"] = single
+    print(json.dumps(out), flush=True)
     return 0
 
 
@@ -359,6 +445,7 @@ def run_ours(args):
     traffic = profiled_traffic(kname, args.workload)
     roofline = {"bound": "tensor", "achieved": kernel_tflops, "peak": peaks["fp8_tflops"], "unit": "TFLOP/s",
                 "frac": kernel_tflops / peaks["fp8_tflops"], "traffic": traffic,
+                "tensor_active_pct_ncu": profiled_tensor_active(kname, args.workload),
                 "peak_source": f"{peaks['source']}: 2 x MEASURED_PEAKS bf16_tflops (fp8/bf16 nominal ratio 2)"
                 if peaks["source"] == "measured" else "fallback 2 x 1900 TFLOP/s bf16",
                 "algorithmic_bytes": algorithmic_bytes(kind, M, N, K),
@@ -377,6 +464,10 @@ def run_ours(args):
     if not args.no_e2e:
         e2e = measure_e2e(args, torch, f, kind, M, N, K, host, gemm)
 
+    mx_gates = None
+    if kind == "bs" and args.workload == DEFAULT_WORKLOAD and not args.no_mx_gates:
+        mx_gates = {w: measure_mx_gate(args, torch, f, w, flush, stream, peaks) for w in MX_GATES}
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_oracle_sample(kind, x, args.cpu_seconds)
@@ -392,7 +483,7 @@ def run_ours(args):
                        "parallelism": f"{world} independent replicas (weak scaling)",
                        "wall_s_timed_loop": wall, "warmup_steps_run": n_w, "ms_min": min(per_ms),
                        "ms_median": statistics.median(per_ms), "hot_l2_ms_per_step": hot_ms},
-            "roofline": roofline, "ceiling_twin": twin, "e4m3_out": e4m3,
+            "roofline": roofline, "ceiling_twin": twin, "e4m3_out": e4m3, "mxfp8_gates": mx_gates,
             "gpu_launches": args.steps * (f.lib().fp8bs_launches_per_call() if kind == "bs"
                                           else f.lib().fp8mx_launches_per_call()),
             "clocks": clocks, "e2e": e2e, "cpu_baseline": cpu}
@@ -401,6 +492,57 @@ def run_ours(args):
     if pg:
         pg.destroy_process_group()
     return 0
+
+
+MX_GATES = ("mx_16384x5120x2048", "mx_16384x8192x1280")
+
+
+def measure_mx_gate(args, torch, f, workload, flush, stream, peaks):
+    """One of the two gated MXFP8 workloads (M = 16384), timed beside the default
+    blockscale line with the same protocol (L2 flushed before every step, CUDA
+    events on the launching stream, warm-up first): the public call (scale pack
+    + GEMM, what a user of fp8mx_gemm gets) and the GEMM alone on packed scales
+    (the roofline kernel). The configuration that ran is asserted to be the
+    CTA-pair kernel the shape rule picks for M >= 4096."""
+    kind, M, N, K = workload_shape(workload)
+    _, _, d = make_device_inputs(kind, M, N, K, 0, torch)
+    C = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    n = max(5, min(args.steps, 50))
+
+    def timed(fn):
+        for _ in range(3):
+            fn()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+        for a, b in ev:
+            flush.fill_(1)
+            a.record(stream)
+            fn()
+            b.record(stream)
+        torch.cuda.synchronize()
+        assert f.get_status() == 0
+        return statistics.mean(a.elapsed_time(b) for a, b in ev)
+
+    call_ms = timed(lambda: f.gemm_mxfp8(d[0], d[1], d[2], d[3], C=C))
+    cfg_id = f.last_config_id()
+    dec = f.decode_config(cfg_id)
+    assert dec["kind"] == "mxfp8_pair", dec
+    a_sf = f.pack_mx_scales(d[1], K)
+    b_sf = f.pack_mx_scales(d[3], K)
+    gemm_ms = timed(lambda: f.gemm_mxfp8_packed(d[0], a_sf, d[2], b_sf, C=C))
+    assert f.last_config_id() == cfg_id
+    flops = 2.0 * M * N * K
+    kname = kernel_name(dec)
+    tf = flops / (gemm_ms * 1e-3) / 1e12
+    return {"M": M, "N": N, "K": K, "seed": 0, "config_id": cfg_id, "steps": n,
+            "public_call": {"ms": call_ms, "achieved": flops / (call_ms * 1e-3) / 1e12,
+                            "frac": flops / (call_ms * 1e-3) / 1e12 / peaks["fp8_tflops"], "unit": "TFLOP/s",
+                            "launches": f.lib().fp8mx_launches_per_call()},
+            "roofline": {"bound": "tensor", "achieved": tf, "peak": peaks["fp8_tflops"], "unit": "TFLOP/s",
+                         "frac": tf / peaks["fp8_tflops"], "kernel": kname, "kernel_ms": gemm_ms,
+                         "traffic": profiled_traffic(kname, workload),
+                         "tensor_active_pct_ncu": profiled_tensor_active(kname, workload),
+                         "algorithmic_bytes": algorithmic_bytes(kind, M, N, K)},
+            "gate": {"frac_at_least": 0.60, "met": tf / peaks["fp8_tflops"] >= 0.60}}
 
 
 def measure_twin(args, torch, f, d, C, flush, stream, flops, kernel_ms, peaks):
@@ -695,23 +837,45 @@ def run_moe(args):
 
 
 def run_moe_reference(args):
+    """The oracle on the grouped workload: every step computes the same sort
+    blocks (all of them when the run fits --ref-seconds, else the first ones
+    that do); ms_per_step is the measured wall time of one step."""
+    import oracle
     world, rank, _ = dist_setup(args)
     if rank != 0:
         return 0
     w = workloads.WORKLOADS[args.workload]
     x = workloads.make_moe_inputs(w["tokens"], w["top_k"], w["experts"], w["N"], w["K"], seed=args.seed,
                                   skew=w["skew"])
-    per, cb = [], None
-    for i in range(args.warmup + args.steps):
-        cb = moe_cpu_sample(x, args.cpu_seconds / max(1, args.steps + args.warmup))
+
+    def blocks(nb):
+        for b in range(nb):
+            e = int(x.block_expert[b])
+            rows = slice(64 * b, 64 * b + 64)
+            oracle.blockscale(x.A[rows], x.a_scale[rows], x.B[e], x.b_scale[e])
+
+    t0 = time.perf_counter()
+    blocks(1)
+    per_block = time.perf_counter() - t0
+    n_steps = args.warmup + args.steps
+    nb = x.n_blocks if per_block * x.n_blocks * n_steps <= args.ref_seconds else \
+        int(min(x.n_blocks, max(1, args.ref_seconds / (n_steps * per_block))))
+    walls = []
+    for i in range(n_steps):
+        t0 = time.perf_counter()
+        blocks(nb)
         if i >= args.warmup:
-            per.append(cb["value"])
-    val = statistics.mean(per)
-    flops, _ = moe_work(w, x)
+            walls.append(time.perf_counter() - t0)
+    ms = statistics.mean(walls) * 1e3
+    val = 2.0 * 64 * nb * x.N * x.K / (ms * 1e-3) / 1e12
+    cb = {"value": val, "unit": "TFLOP/s", "cores": oracle.max_threads(), "kind": "oracle",
+          "sample": f"every step: {nb} of {x.n_blocks} sort blocks (64 rows each, padded rows included), "
+                    f"fp64 dequantise + naive triple loop; mean step {ms / 1e3:.2f} s"}
     line = {"impl": "reference", "metric": METRIC, "value": val, "unit": "TFLOP/s", "n_gpus": args.gpus,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": flops / (val * 1e12) * 1e3,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": args.workload, "seed": args.seed}, "cpu_baseline": dict(cb, value=val),
+            "config": {"workload": args.workload, "seed": args.seed}, "blocks_per_step": nb, "extrapolated": False,
+            "cpu_baseline": cb,
             "e2e": {"value": val, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
     return 0
@@ -761,6 +925,8 @@ def run_ksweep(args):
 
 def main():
     args = parse()
+    if args.cpu_all:
+        return run_cpu_all(args)
     if args.ksweep:
         return run_ksweep(args)
     moe = workloads.WORKLOADS[args.workload]["kind"] == "moe"

@@ -389,8 +389,8 @@ __global__ void pack_a_scale_kernel(const float *__restrict__ src, float *__rest
 // (cfg.kind 2) or of the tensor-scale twin (cfg.kind 4, no scale atoms, one
 // alpha): a persistent grid of min(tiles, SMs) CTAs, or the stream-K grid.
 int launch_mx(Config &cfg, const void *A, const uint8_t *a_sf, const void *B, const uint8_t *b_sf, void *C, int M,
-              int N, int K, float alpha, int *status_ptr, int num_sms, cudaMemPool_t pool, cudaStream_t s,
-              bool c_e4m3 = false, float c_scale = 1.f)
+              int N, int K, float alpha, int *status_ptr, int num_sms, int mx_pair_clusters, cudaMemPool_t pool,
+              cudaStream_t s, bool c_e4m3 = false, float c_scale = 1.f)
 {
     if (c_e4m3)
         cfg.sched = 1;   // the E4M3-output MXFP8 kernel runs one CTA per tile (cfg reports what ran)
@@ -464,10 +464,9 @@ int launch_mx(Config &cfg, const void *A, const uint8_t *a_sf, const void *B, co
         args.status = status_ptr;
         args.wait_limit_ns = g_wait_limit_ns.load();
         args.teardown_limit_ns = teardown_limit();
-        int dev = 0;
-        cudaGetDevice(&dev);
-        const cudaError_t e =
-            launch_mxfp8_pair<kMxPairStages>(tmA, tmB, tmSFA, tmSFB, tmC, args, g_dev[dev].mx_pair_clusters, s);
+        if (mx_pair_clusters < 1)
+            return FP8BS_ERR_LAUNCH;
+        const cudaError_t e = launch_mxfp8_pair<kMxPairStages>(tmA, tmB, tmSFA, tmSFB, tmC, args, mx_pair_clusters, s);
         return e == cudaSuccess ? FP8BS_OK : FP8BS_ERR_LAUNCH;
     }
     CUtensorMap tmA, tmB, tmC;
@@ -793,8 +792,8 @@ static int mx_gemm_packed_any(const void *A, const uint8_t *a_sf, const void *B,
     Config cfg = choose_config(2, M, N, K, st->num_sms);
     if (!override_config(2, 5, cfg, 6))
         return FP8BS_ERR_SHAPE;
-    if ((rc = launch_mx(cfg, A, a_sf, B, b_sf, C, M, N, K, 1.f, st->status_ptr, st->num_sms, st->pool,
-                        static_cast<cudaStream_t>(stream), c_e4m3, c_scale)))
+    if ((rc = launch_mx(cfg, A, a_sf, B, b_sf, C, M, N, K, 1.f, st->status_ptr, st->num_sms, st->mx_pair_clusters,
+                        st->pool, static_cast<cudaStream_t>(stream), c_e4m3, c_scale)))
         return rc;
     t_last_config = config_id(cfg);
     return FP8BS_OK;
@@ -852,8 +851,8 @@ int fp8bs_gemm_tensorscale(const void *A, const void *B, void *C, int M, int N, 
     Config cfg = choose_config(4, M, N, K, st->num_sms);
     if (!override_config(4, 4, cfg))
         return FP8BS_ERR_SHAPE;
-    if ((rc = launch_mx(cfg, A, nullptr, B, nullptr, C, M, N, K, alpha, st->status_ptr, st->num_sms, st->pool,
-                        static_cast<cudaStream_t>(stream))))
+    if ((rc = launch_mx(cfg, A, nullptr, B, nullptr, C, M, N, K, alpha, st->status_ptr, st->num_sms,
+                        st->mx_pair_clusters, st->pool, static_cast<cudaStream_t>(stream))))
         return rc;
     t_last_config = config_id(cfg);
     return FP8BS_OK;
@@ -1095,6 +1094,7 @@ struct NoAllocDevice {
     int num_sms = 0;
     int *status_ptr = nullptr;
     uint8_t *scratch = nullptr;   // device address of g_noalloc_scratch
+    int mx_pair_clusters = 0;     // co-resident CTA pairs of the MXFP8 pair kernel (M >= 4096 shapes)
 };
 NoAllocDevice g_noalloc_dev[kMaxDevices];
 
@@ -1119,6 +1119,10 @@ int noalloc_setup(int &dev, NoAllocDevice *&nd)
         return nd->status = FP8BS_ERR_CUDA;
     if (cudaGetSymbolAddress(reinterpret_cast<void **>(&nd->scratch), g_noalloc_scratch) != cudaSuccess ||
         !nd->scratch)
+        return nd->status = FP8BS_ERR_CUDA;
+    // The shape rule picks the CTA-pair kernel for M >= 4096; its persistent
+    // grid is the number of co-resident pairs (an occupancy query, no allocation).
+    if (max_mx_pair_clusters<kMxPairStages>(&nd->mx_pair_clusters) != cudaSuccess || nd->mx_pair_clusters < 1)
         return nd->status = FP8BS_ERR_CUDA;
     if (!g_encode) {
         cudaDriverEntryPointQueryResult q;
@@ -1160,7 +1164,7 @@ int fp8mx_gemm_noalloc(const void *A, const uint8_t *a_e8m0, const void *B, cons
     if ((rc = noalloc_setup(dev, nd)))
         return rc;
     Config cfg = choose_config(2, M, N, K, nd->num_sms);
-    if (!override_config(2, 6, cfg))   // the decode kernel needs no workspace either
+    if (!override_config(2, 5, cfg, 6))   // the pair and decode kernels need no workspace either
         return FP8BS_ERR_SHAPE;
     cfg.sched = 1;   // stream-K needs a workspace: one CTA per tile here
     cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -1169,7 +1173,8 @@ int fp8mx_gemm_noalloc(const void *A, const uint8_t *a_e8m0, const void *B, cons
     rc = launch_pack_scales(a_e8m0, a_sf, M, b_e8m0, b_sf, N, K, nd->num_sms, s);
     if (rc)
         return rc;
-    if ((rc = launch_mx(cfg, A, a_sf, B, b_sf, C, M, N, K, 1.f, nd->status_ptr, nd->num_sms, nullptr, s)))
+    if ((rc = launch_mx(cfg, A, a_sf, B, b_sf, C, M, N, K, 1.f, nd->status_ptr, nd->num_sms, nd->mx_pair_clusters,
+                        nullptr, s)))
         return rc;
     t_last_config = config_id(cfg);
     return FP8BS_OK;

@@ -224,15 +224,18 @@ int fp8mx_pack_scales(const uint8_t *e8m0, uint8_t *packed, int rows, int K, voi
  * from a memory pool; this entry point uses a fixed device array of
  * fp8mx_noalloc_scratch_bytes() bytes (8 MiB) built into the library instead,
  * which every GPU that loads the library holds until the process exits. It
- * always runs one CTA per tile (stream-K would need a workspace); the MXFP8
- * decode kernel (config 6128601, by override), which needs none, runs too.
+ * always runs one CTA per tile (stream-K would need a workspace); the CTA-pair
+ * kernel (chosen from M = 4096 as in fp8mx_gemm, or forced) and the MXFP8
+ * decode kernel (config 6128601, by override), which need none, run too.
  *
  * Limit: fp8mx_packed_scale_bytes(M, K) + fp8mx_packed_scale_bytes(N, K) must
  * not exceed that size, else FP8BS_ERR_SCRATCH_TOO_SMALL (checked on the host,
  * before anything runs). All calls share the one array: two calls whose kernels
  * overlap on the GPU (e.g. on different streams without ordering between them)
  * race on it. The first call on a device looks up the array's device address
- * (no allocation); make that first call before any stream capture.
+ * and the CTA-pair kernel's co-resident cluster count (no allocation), with no
+ * other call of this library needed before it; make that first call before any
+ * stream capture.
  * Launches two kernels on `stream` (scale pack, GEMM), like fp8mx_gemm.
  */
 int fp8mx_gemm_noalloc(const void *A, const uint8_t *a_e8m0, const void *B, const uint8_t *b_e8m0, void *C,

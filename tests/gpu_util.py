@@ -62,6 +62,38 @@ def compare(gpu_bits, ref_bits, what=""):
     return m
 
 
+def compare_rows(gpu_bits, ref_bits, what="", rows_per_chunk=512):
+    """compare() over a large output in row chunks (the metrics are accumulated
+    over the whole matrix; nothing of size M x N is held in float64)."""
+    assert gpu_bits.shape == ref_bits.shape
+    M = gpu_bits.shape[0]
+    sq_err = sq_ref = sq_gpu = dot = 0.0
+    maxabs = 0.0
+    n_bad = 0
+    first_bad = []
+    for r0 in range(0, M, rows_per_chunk):
+        g = oracle.bf16_bits_to_float(gpu_bits[r0:r0 + rows_per_chunk]).astype(np.float64)
+        o = oracle.bf16_bits_to_float(ref_bits[r0:r0 + rows_per_chunk]).astype(np.float64)
+        assert np.all(np.isfinite(g)), f"{what}: non-finite GPU output in rows {r0}.."
+        err = np.abs(g - o)
+        bad = err > ATOL + RTOL * np.abs(o)
+        if bad.any():
+            n_bad += int(bad.sum())
+            if len(first_bad) < 5:
+                first_bad += (np.argwhere(bad)[:5] + [r0, 0]).tolist()
+        maxabs = max(maxabs, float(err.max()) if err.size else 0.0)
+        sq_err += float(np.sum(err * err))
+        sq_ref += float(np.sum(o * o))
+        sq_gpu += float(np.sum(g * g))
+        dot += float(np.sum(g * o))
+    rel = (sq_err / sq_ref) ** 0.5 if sq_ref > 0 else sq_err ** 0.5
+    cos = dot / (sq_gpu * sq_ref) ** 0.5 if sq_ref > 0 and sq_gpu > 0 else 1.0
+    m = {"maxabs": maxabs, "rel_l2": rel, "cos": cos, "n_out_of_tol": n_bad, "n": int(gpu_bits.size)}
+    assert n_bad == 0, f"{what}: {m}; first bad {first_bad[:5]}"
+    assert rel <= REL_L2, f"{what}: {m}"
+    return m
+
+
 def _e4m3_table():
     """Values of the 256 E4M3FN codes (NaN for 0x7F/0xFF), from the oracle's decoder."""
     return np.array([oracle.e4m3_decode(c) for c in range(256)], dtype=np.float64)

@@ -9,7 +9,7 @@ import pytest
 
 import oracle
 import workloads
-from gpu_util import compare, compare_e4m3, run_blockscale, run_mxfp8, to_dev
+from gpu_util import compare, compare_e4m3, compare_rows, run_blockscale, run_mxfp8, to_dev
 
 pytestmark = pytest.mark.gpu
 
@@ -280,50 +280,36 @@ def test_m_zero_is_noop():
     assert C.shape == (0, 8)
 
 
-# ------------------------------------------------ full-size workloads (sampled rows)
-
-def _sample_rows(M, rng):
-    """Two rows from every 128-row tile (random offsets) plus the first and last row."""
-    rows = set([0, M - 1])
-    for t in range(0, M, 128):
-        hi = min(128, M - t)
-        rows.update((t + rng.integers(0, hi, size=2)).tolist())
-    return sorted(rows)
-
+# ------------------------------------------------ full-size workloads (whole output)
 
 def _check_full_size(kind, M, N, K, seed):
+    """The workload at its full size in the configuration the library chooses
+    (the one the benchmark times), compared element by element with the oracle
+    over the whole of C."""
     x = workloads.make_inputs(kind, M, N, K, seed)
     if kind == "bs":
         got = run_blockscale(x.A, x.a_scale, x.B, x.b_scale)
+        ref = oracle.blockscale(x.A, x.a_scale, x.B, x.b_scale)
     else:
         got = run_mxfp8(x.A, x.a_e8m0, x.B, x.b_e8m0)
-    rng = np.random.Generator(np.random.PCG64(1000 + seed))
-    rows = _sample_rows(M, rng)
-    # Row m of C depends only on row m of A and its scales: the oracle runs on
-    # the gathered sample rows as one smaller problem.
-    if kind == "bs":
-        ref = oracle.blockscale(x.A[rows], x.a_scale[rows], x.B, x.b_scale)
-    else:
-        ref = oracle.mxfp8(x.A[rows], x.a_e8m0[rows], x.B, x.b_e8m0)
-    return compare(got[rows], ref, f"{kind} {M}x{N}x{K} seed {seed}")
+        ref = oracle.mxfp8(x.A, x.a_e8m0, x.B, x.b_e8m0)
+    return compare_rows(got, ref, f"{kind} {M}x{N}x{K} seed {seed}")
 
 
 @pytest.mark.parametrize("seed", [0, 1, 2, 3])
-def test_full_blockscale_narrowN_4096x2048x7168(seed):
-    _check_full_size("bs", 4096, 2048, 7168, seed)
-
-
-@pytest.mark.parametrize("name", ["bs_narrowN_16384x1536x7168", "bs_Klight_16384x7168x768",
-                                  "bs_wideN_4096x65536x1536"])
-def test_full_blockscale_other_shapes(name):
+@pytest.mark.parametrize("name", ["bs_narrowN_4096x2048x7168", "bs_narrowN_16384x1536x7168",
+                                  "bs_Klight_16384x7168x768", "bs_wideN_4096x65536x1536"])
+def test_full_blockscale(name, seed):
     w = workloads.WORKLOADS[name]
-    _check_full_size("bs", w["M"], w["N"], w["K"], 0)
+    assert seed in w["seeds"]
+    _check_full_size("bs", w["M"], w["N"], w["K"], seed)
 
 
+@pytest.mark.parametrize("seed", [0, 1])
 @pytest.mark.parametrize("M", [1024, 2048, 4096, 16384])
 @pytest.mark.parametrize("N,K", [(5120, 2048), (8192, 1280)])
-def test_full_mxfp8(M, N, K):
-    _check_full_size("mx", M, N, K, 0)
+def test_full_mxfp8(M, N, K, seed):
+    _check_full_size("mx", M, N, K, seed)
 
 
 # ---------------------------------------------------------------- stream-K

@@ -51,7 +51,7 @@ def test_reference_arm_prints_only_on_rank0(capsys, monkeypatch):
     monkeypatch.setenv("RANK", "1")
     monkeypatch.setenv("WORLD_SIZE", "2")
     args = type("A", (), dict(workload="bs_tiny_256x512x512", seed=0, steps=1, warmup=1, gpus=2,
-                              cpu_seconds=1.0))()
+                              cpu_seconds=1.0, ref_seconds=5.0))()
     assert bench.run_reference(args) == 0
     assert capsys.readouterr().out == ""
 
@@ -63,8 +63,10 @@ def test_reference_arm_line_rank0(capsys, monkeypatch):
     monkeypatch.setenv("RANK", "0")
     monkeypatch.setenv("WORLD_SIZE", "1")
     args = type("A", (), dict(workload="bs_tiny_256x512x512", seed=0, steps=2, warmup=1, gpus=1,
-                              cpu_seconds=1.0))()
+                              cpu_seconds=1.0, ref_seconds=5.0))()
     assert bench.run_reference(args) == 0
     line = json.loads(capsys.readouterr().out.strip())
     assert line["impl"] == "reference" and line["unit"] == "TFLOP/s" and line["value"] > 0
+    # nothing extrapolated: the per-step time is the measured one, for the rows the line names
+    assert line["extrapolated"] is False and line["ms_per_step"] > 0 and 1 <= line["rows_per_step"] <= 256
     assert line["cpu_baseline"]["kind"] == "oracle" and line["e2e"]["h2d_bytes_per_step"] == 0
