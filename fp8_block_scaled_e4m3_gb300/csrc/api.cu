@@ -21,11 +21,6 @@ template <int BN, int STAGES>
 cudaError_t launch_blockscale_moe(const CUtensorMap &, const CUtensorMap &, const CUtensorMap &, const CUtensorMap &,
                                   const GemmArgs &, int, cudaStream_t);
 template <int STAGES>
-cudaError_t launch_blockscale_pair(const CUtensorMap &, const CUtensorMap &, const CUtensorMap &, const CUtensorMap &,
-                                   const GemmArgs &, int, cudaStream_t);
-template <int STAGES>
-cudaError_t max_pair_clusters(int *);
-template <int STAGES>
 cudaError_t launch_mxfp8_pair(const CUtensorMap &, const CUtensorMap &, const CUtensorMap &, const CUtensorMap &,
                               const CUtensorMap &, const GemmArgs &, int, cudaStream_t);
 template <int STAGES>
@@ -44,7 +39,6 @@ __device__ int g_status_word;   // per-device status written by the kernels
 
 constexpr int kMaxDevices = 64;
 constexpr unsigned long long kDefaultWaitLimitNs = 2000000000ull;
-constexpr int kPairStages = 8;
 constexpr int kMxPairStages = 6;
 
 struct DeviceState {
@@ -53,7 +47,6 @@ struct DeviceState {
     int num_sms = 0;
     int *status_ptr = nullptr;      // device address of g_status_word
     cudaMemPool_t pool = nullptr;   // stream-ordered pool for fp8mx_gemm's packed scales
-    int pair_clusters = 0;          // co-resident CTA pairs of the pair kernel
     int mx_pair_clusters = 0;       // co-resident CTA pairs of the MXFP8 pair kernel
 };
 
@@ -103,8 +96,6 @@ int ensure_device(int &dev, DeviceState *&st)
     uint64_t keep = UINT64_MAX;   // keep freed workspace in the pool between calls
     if (cudaMemPoolSetAttribute(st->pool, cudaMemPoolAttrReleaseThreshold, &keep) != cudaSuccess)
         return st->status = FP8BS_ERR_CUDA;
-    if (max_pair_clusters<kPairStages>(&st->pair_clusters) != cudaSuccess || st->pair_clusters < 1)
-        return st->status = FP8BS_ERR_CUDA;
     if (max_mx_pair_clusters<kMxPairStages>(&st->mx_pair_clusters) != cudaSuccess || st->mx_pair_clusters < 1)
         return st->status = FP8BS_ERR_CUDA;
     if (!g_encode) {
@@ -148,9 +139,10 @@ int check_shape(int M, int N, int K)
 }
 
 // Kernel configuration. kind 1: one-CTA blockscale kernel, 2: MXFP8 kernel,
-// 3: CTA-pair blockscale kernel (256 x 128 tiles over two SMs), 4: tensor-scale
-// twin (the MXFP8 kernel's pipeline with plain fp8 MMAs), 5: CTA-pair MXFP8
-// kernel (256 x 256 tiles over two SMs).
+// 4: tensor-scale twin (the MXFP8 kernel's pipeline with plain fp8 MMAs), 5:
+// CTA-pair MXFP8 kernel (256 x 256 tiles over two SMs), 6: MXFP8 decode kernel.
+// (Kind 3, a CTA-pair blockscale kernel with 256 x 128 tiles, measured slower
+// than kind 1 on every shape and was removed.)
 // sched 1: one CTA per tile; 2: stream-K (256-wide tile of kinds 1, 2 and 4).
 struct Config {
     int kind, block_n, stages, raster, sched;
@@ -171,14 +163,12 @@ bool decode_config_id(int id, Config &c)
     c.sched = id % 10;
     // stream-K: the 256-wide tile of kinds 1, 2 and 4, and the MXFP8 kernel's 128-wide tile
     if (c.sched < 1 || c.sched > 2 || c.raster > 1 ||
-        (c.sched == 2 && (c.kind == 3 || (c.block_n != 256 && !(c.kind == 2 && c.block_n == 128)))))
+        (c.sched == 2 && c.block_n != 256 && !(c.kind == 2 && c.block_n == 128)))
         return false;
     if (c.kind == 1)
         return (c.block_n == 256 && c.stages == 4) || (c.block_n == 128 && c.stages == 6);
     if (c.kind == 2 || c.kind == 4)
         return (c.block_n == 256 && c.stages == 4) || (c.block_n == 128 && c.stages == 6);
-    if (c.kind == 3)
-        return c.block_n == 128 && c.stages == kPairStages;
     if (c.kind == 5)
         return c.block_n == 256 && c.stages == kMxPairStages && c.sched == 1;
     if (c.kind == 6)
@@ -275,9 +265,7 @@ Config choose_config(int kind, int M, int N, int K, int num_sms)
     c.kind = kind;
     // Blockscale and MXFP8 alike: wide one-CTA tiles (128 x 256), which keep
     // shared-memory operand traffic at 96 B/clk per SM and give each tcgen05.mma
-    // 128 clocks of work (narrower MMAs are issue-bound). The CTA-pair
-    // blockscale kernel (kind 3) measured slower on every shape and is
-    // selectable by override.
+    // 128 clocks of work (narrower MMAs are issue-bound).
     c.block_n = 256;
     c.stages = 4;
     const long long tiles256 = (long long)((M + 127) / 128) * ((N + 255) / 256);
@@ -531,17 +519,13 @@ int blockscale_gemm(const void *A, const float *a_scale, const void *B, const fl
     if ((rc = ensure_device(dev, st)))
         return rc;
     Config cfg = choose_config(1, M, N, K, st->num_sms);
-    if (!override_config(1, 3, cfg))
+    if (!override_config(1, 1, cfg))
         return FP8BS_ERR_SHAPE;
-    const bool pair = cfg.kind == 3;
-    if (pair && c_e4m3)
-        return FP8BS_ERR_SHAPE;   // the CTA-pair kernel stores bf16 only
     const int KB = K / 128;
     const uint64_t ld_sa = static_cast<uint64_t>(fp8bs_a_scale_ld(M));
-    const uint32_t b_box_rows = pair ? cfg.block_n / 2 : cfg.block_n;   // a pair CTA holds half of B
     CUtensorMap tmA, tmB, tmSA, tmC;
     if (!encode_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, A, K, M, K, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !encode_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, B, K, N, K, 128, b_box_rows, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, B, K, N, K, 128, cfg.block_n, CU_TENSOR_MAP_SWIZZLE_128B) ||
         !encode_2d(&tmSA, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, a_scale, ld_sa, KB, ld_sa * 4, 128, 1,
                    CU_TENSOR_MAP_SWIZZLE_NONE) ||
         !(c_e4m3 ? encode_2d(&tmC, CU_TENSOR_MAP_DATA_TYPE_UINT8, C, N, M, static_cast<uint64_t>(N), 64, 32,
@@ -555,8 +539,7 @@ int blockscale_gemm(const void *A, const float *a_scale, const void *B, const fl
     args.K = K;
     args.c_e4m3 = c_e4m3 ? 1 : 0;
     args.c_scale = c_scale;
-    const int tile_m = pair ? 2 * kBlockM : kBlockM;
-    args.raster.m_tiles = (M + tile_m - 1) / tile_m;
+    args.raster.m_tiles = (M + kBlockM - 1) / kBlockM;
     args.raster.n_tiles = (N + cfg.block_n - 1) / cfg.block_n;
     args.raster.raster = cfg.raster;
     args.raster.group = 1;
@@ -569,15 +552,13 @@ int blockscale_gemm(const void *A, const float *a_scale, const void *B, const fl
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     void *ws = nullptr;
     if (cfg.sched == 2) {
-        if (pair || cfg.block_n != 256)
+        if (cfg.block_n != 256)
             return FP8BS_ERR_SHAPE;
         if ((rc = setup_stream_k(tiles, KB, st->num_sms, st->pool, s, args, grid, ws)))
             return rc;
     }
     cudaError_t e;
-    if (pair)
-        e = launch_blockscale_pair<kPairStages>(tmA, tmB, tmSA, tmC, args, st->pair_clusters, s);
-    else if (cfg.block_n == 256)
+    if (cfg.block_n == 256)
         e = launch_blockscale<256, 4>(tmA, tmB, tmSA, tmC, args, grid, s);
     else
         e = launch_blockscale<128, 6>(tmA, tmB, tmSA, tmC, args, grid, s);
@@ -1060,7 +1041,7 @@ int fp8bs_device_info(int *num_sms, int *pair_clusters)
     if (num_sms)
         *num_sms = st->num_sms;
     if (pair_clusters)
-        *pair_clusters = st->pair_clusters;
+        *pair_clusters = st->mx_pair_clusters;
     return FP8BS_OK;
 }
 

@@ -431,28 +431,6 @@ __host__ __device__ constexpr uint32_t idesc_mxf8f6f4_e4m3(int M, int N, int sfa
            (static_cast<uint32_t>(M >> 4) << 24) | (static_cast<uint32_t>(sfa_id & 3) << 29);
 }
 
-// Two fp32 lanes in one 64-bit register: lane 0 = low word.
-__device__ __forceinline__ uint64_t pack_f32x2(uint32_t lo, uint32_t hi)
-{
-    uint64_t d;
-    asm("mov.b64 %0, {%1, %2};" : "=l"(d) : "r"(lo), "r"(hi));
-    return d;
-}
-
-__device__ __forceinline__ void unpack_f32x2(uint64_t v, float &lo, float &hi)
-{
-    uint32_t a, b;
-    asm("mov.b64 {%0, %1}, %2;" : "=r"(a), "=r"(b) : "l"(v));
-    lo = __uint_as_float(a);
-    hi = __uint_as_float(b);
-}
-
-// acc = p * s + acc on two fp32 lanes at once, each lane rounded as fmaf.
-__device__ __forceinline__ void ffma2(uint64_t &acc, uint64_t p, uint64_t s)
-{
-    asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(acc) : "l"(p), "l"(s));
-}
-
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
 {
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);

@@ -86,8 +86,7 @@ int fp8bs_gemm(const void *A, const float *a_scale, const void *B, const float *
  * E4M3, e.g. 16 / rms(C)).
  *   C8  E4M3 [M][N] row-major, written, 16-byte aligned.
  * Other arguments, schedule and errors as fp8bs_gemm; in addition N % 16 == 0
- * (FP8BS_ERR_SHAPE otherwise), and a forced CTA-pair configuration is rejected
- * (FP8BS_ERR_SHAPE: that kernel stores bf16 only).
+ * (FP8BS_ERR_SHAPE otherwise).
  */
 int fp8bs_gemm_e4m3out(const void *A, const float *a_scale, const void *B, const float *b_scale, void *C8,
                        float c_scale, int M, int N, int K, void *stream);
@@ -275,8 +274,7 @@ const char *fp8bs_status_string(int status);
 /* Identifier of the kernel configuration the last successful GEMM call on this
  * host thread launched (0 if none): kind*1000000 + block_n*1000 + stages*100 +
  * raster*10 + schedule; kind 1 = one-CTA blockscale kernel (128 x block_n
- * tiles), 2 = mxfp8 kernel, 3 = CTA-pair blockscale kernel (256 x block_n tiles
- * over two SMs), 4 = tensor-scale twin (fp8bs_gemm_tensorscale), 5 = CTA-pair
+ * tiles), 2 = mxfp8 kernel, 4 = tensor-scale twin (fp8bs_gemm_tensorscale), 5 = CTA-pair
  * mxfp8 kernel (256 x 256 tiles over two SMs), 6 = mxfp8 decode kernel
  * (6128601 only; selectable by fp8bs_set_config_override, never chosen by the
  * shape rule: M <= 128, the K steps of each 128-column tile cut into up to 8
@@ -305,7 +303,7 @@ int fp8mx_select_config(int M, int N, int K, int num_sms);
  * measurements of each kernel variant. */
 int fp8bs_set_config_override(int config_id);
 /* SM count of the current device and the number of two-CTA clusters of the
- * CTA-pair kernel that can be resident at once (its persistent grid size). */
+ * CTA-pair MXFP8 kernel that can be resident at once (its persistent grid size). */
 int fp8bs_device_info(int *num_sms, int *pair_clusters);
 /* Number of kernels one fp8bs_gemm call launches (1). */
 int fp8bs_launches_per_call(void);

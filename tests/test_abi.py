@@ -154,7 +154,7 @@ def test_config_selection(lib):
     assert L.fp8bs_set_config_override(1160511) == -3      # the 160-wide tile was removed
     assert L.fp8bs_set_config_override(2128612) == 0       # the MXFP8 kernel's 128-wide tile has stream-K too
     assert L.fp8bs_set_config_override(4128612) == -3
-    assert L.fp8bs_set_config_override(3128812) == -3      # no stream-K for the CTA pair
+    assert L.fp8bs_set_config_override(3128811) == -3      # kind 3 (a removed kernel) names nothing built
     assert L.fp8bs_set_config_override(1256413) == -3      # no such schedule
     assert L.fp8bs_set_config_override(1128612) == -3      # stream-K runs with the 256-wide tile only
     # the MXFP8 decode kernel (K slices in clusters): selectable, one id only, never chosen by the rule
