@@ -166,7 +166,7 @@ bool decode_config_id(int id, Config &c)
         (c.sched == 2 && c.block_n != 256 && !(c.kind == 2 && c.block_n == 128)))
         return false;
     if (c.kind == 1)
-        return (c.block_n == 256 && c.stages == 4) || (c.block_n == 128 && c.stages == 6);
+        return (c.block_n == 256 && (c.stages == 4 || c.stages == 3)) || (c.block_n == 128 && c.stages == 6);
     if (c.kind == 2 || c.kind == 4)
         return (c.block_n == 256 && c.stages == 4) || (c.block_n == 128 && c.stages == 6);
     if (c.kind == 5)
@@ -255,8 +255,8 @@ int setup_stream_k(int tiles, int KB, int num_sms, cudaMemPool_t pool, cudaStrea
     return FP8BS_OK;
 }
 
-// Shape class -> configuration, from (M, N, K) only.
-Config choose_config(int kind, int M, int N, int K, int num_sms)
+// Shape class -> configuration before the blockscale stage choice below.
+Config choose_config_base(int kind, int M, int N, int K, int num_sms)
 {
     Config c;
     // Stream the larger operand once past a resident set of panels of the smaller one.
@@ -306,6 +306,25 @@ Config choose_config(int kind, int M, int N, int K, int num_sms)
         c.kind = 5;
         c.stages = 6;
     }
+    return c;
+}
+
+// Blockscale GEMM with few K blocks per tile (K <= 1024): the three-stage
+// instance, whose freed shared memory gives the epilogue two 4 KiB buffers per
+// warp, so the C store of a tile overlaps less of the next tile's K loop.
+// Same-session times (us, L2 flushed, tile / stream-K schedule, 4 -> 3 stages):
+// 16384x7168x768 119.2 -> 109.0 / 123.9 -> 114.8; 16384x7168x1024 141.3 ->
+// 133.3; 16384x7168x1536 183.8 -> 180.3; 4096x65536x1536 398.5 -> 405.1;
+// 16384x7168x2048 225.4 -> 229.9; 4096x2048x7168 63.5 -> 71.7 (one producer
+// thread fills the odd-count ring, which deep K loops feel).
+constexpr int kWideCMaxKBlocks = 8;
+
+// Shape class -> configuration, from (M, N, K) only.
+Config choose_config(int kind, int M, int N, int K, int num_sms)
+{
+    Config c = choose_config_base(kind, M, N, K, num_sms);
+    if (kind == 1 && c.block_n == 256 && K / 128 <= kWideCMaxKBlocks)
+        c.stages = 3;
     return c;
 }
 
@@ -523,6 +542,7 @@ int blockscale_gemm(const void *A, const float *a_scale, const void *B, const fl
         return FP8BS_ERR_SHAPE;
     const int KB = K / 128;
     const uint64_t ld_sa = static_cast<uint64_t>(fp8bs_a_scale_ld(M));
+    const bool wide_c = cfg.block_n == 256 && cfg.stages == 3;   // 32 x 64 bf16 C boxes, 128-byte swizzle
     CUtensorMap tmA, tmB, tmSA, tmC;
     if (!encode_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, A, K, M, K, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
         !encode_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, B, K, N, K, 128, cfg.block_n, CU_TENSOR_MAP_SWIZZLE_128B) ||
@@ -531,7 +551,8 @@ int blockscale_gemm(const void *A, const float *a_scale, const void *B, const fl
         !(c_e4m3 ? encode_2d(&tmC, CU_TENSOR_MAP_DATA_TYPE_UINT8, C, N, M, static_cast<uint64_t>(N), 64, 32,
                              CU_TENSOR_MAP_SWIZZLE_64B)
                  : encode_2d(&tmC, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, C, N, M, static_cast<uint64_t>(N) * 2,
-                             kCChunkCols, 32, CU_TENSOR_MAP_SWIZZLE_64B)))
+                             wide_c ? 64 : kCChunkCols, 32,
+                             wide_c ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B)))
         return FP8BS_ERR_LAUNCH;
     GemmArgs args = {};
     args.M = M;
@@ -558,7 +579,9 @@ int blockscale_gemm(const void *A, const float *a_scale, const void *B, const fl
             return rc;
     }
     cudaError_t e;
-    if (cfg.block_n == 256)
+    if (cfg.block_n == 256 && cfg.stages == 3)
+        e = launch_blockscale<256, 3>(tmA, tmB, tmSA, tmC, args, grid, s);
+    else if (cfg.block_n == 256)
         e = launch_blockscale<256, 4>(tmA, tmB, tmSA, tmC, args, grid, s);
     else
         e = launch_blockscale<128, 6>(tmA, tmB, tmSA, tmC, args, grid, s);

@@ -17,7 +17,8 @@
 //
 // Persistent, warp-specialised, one CTA per SM, 12 warps (3 warpgroups):
 //   warps 0, 3  TMA producers, warp 0 for the even K-block steps and warp 3 for
-//               the odd ones: A tile [128 x 128] e4m3 and B tile [BN x 128] e4m3
+//               the odd ones (warp 0 alone with an odd stage count):
+//               A tile [128 x 128] e4m3 and B tile [BN x 128] e4m3
 //               of one K block into stage s of a STAGES-deep shared-memory ring
 //               (full/empty mbarriers, a stage is freed by the MMA commit), and
 //               the a_scale slice [128] fp32 of the K block into a separate
@@ -41,7 +42,9 @@
 //               the MMA's critical path; for BN = 256 the buffer is released
 //               after the last 64-column round.
 //               After the last K block: bf16 convert, 64-byte-swizzled staging
-//               of 32 x 32 chunks, TMA store (tails clipped by the tensor map).
+//               of 32 x 32 chunks, TMA store (tails clipped by the tensor map);
+//               with three stages (shapes with few K blocks per tile) 32 x 64
+//               chunks through two alternating 4 KiB buffers per warp.
 // Registers: the launch gives 168 per thread (3 warps per SM sub-partition);
 // warpgroup 0 drops to 40 and the two promote warpgroups rise to 232, so one
 // sub-partition holds 40 + 232 + 232 = 504 <= 512 registers per lane and the
@@ -60,7 +63,11 @@ constexpr int kSaSlots = 16;   // a_scale ring depth (>= STAGES + NBUF, so it ne
 
 template <int BN, int STAGES>
 struct BsLayout {
-    static_assert(STAGES % 2 == 0, "two producers and two MMA issuers split the steps by parity");
+    // Three stages leave room for wider C staging: two 4 KiB buffers per
+    // epilogue warp (64-column chunks, alternating), for shapes with few K
+    // blocks per tile, where the epilogue is a large part of each tile.
+    static constexpr bool WIDE_C = STAGES == 3;
+    static constexpr int C_BYTES = WIDE_C ? 2 * 4096 : kCStageBytes;   // per epilogue warp
     static constexpr int A_BYTES = kBlockM * kBlockK;
     static constexpr int B_BYTES = BN * kBlockK;
     static constexpr int SA_BYTES = kBlockM * 4;
@@ -68,7 +75,7 @@ struct BsLayout {
     static constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
     static constexpr int OFF_SA = OFF_B + STAGES * B_BYTES;
     static constexpr int OFF_C = (OFF_SA + kSaSlots * SA_BYTES + 1023) / 1024 * 1024;
-    static constexpr int OFF_BAR = OFF_C + kEpiWarps * kCStageBytes;
+    static constexpr int OFF_BAR = OFF_C + kEpiWarps * C_BYTES;
     static constexpr int NBUF = 512 / BN;        // TMEM partial buffers
     // Column parts of a buffer with barriers of their own: the 256-wide tile's
     // MMAs go out as two N = 128 halves, each signalled to (and released by)
@@ -144,12 +151,21 @@ __global__ void __launch_bounds__(kBsThreads, 1)
 
     if (warp < 4) {
     ptx::setmaxnreg_dec<kBsRegsLow<BN>>();
-    if (warp == 0 || warp == 3) {
+    // Parity waits are unambiguous only while a barrier is at most one phase
+    // ahead of its waiter, i.e. when one thread waits on it for every phase
+    // in turn. With an even stage count each stage (like each a_scale slot and
+    // TMEM buffer) belongs to the producer and issuer of one step parity. With
+    // an odd count a stage's uses alternate between parities, so one producer
+    // thread fills every stage, and each issuer waits for its TMEM buffer
+    // before the stage: the buffer is released only after the promote of the
+    // step before, hence after the stage's previous use was consumed.
+    constexpr bool kOneProducer = STAGES % 2 == 1;
+    if (warp == 0 || (warp == 3 && !kOneProducer)) {
         // ----------------------------------------------------------- producers
         // Warp 0 fills the stages of the even steps, warp 3 those of the odd
-        // steps (STAGES and kSaSlots are even, so each stage and a_scale slot
-        // belongs to one of them and is waited on by that thread alone, in
-        // order of its phases).
+        // steps (with an even STAGES each stage and a_scale slot belongs to
+        // one of them and is waited on by that thread alone, in order of its
+        // phases); with an odd STAGES warp 0 fills all of them.
         if (lane == 0) {
             const int par = warp == 3 ? 1 : 0;
             ptx::prefetch_tmap(&tmA);
@@ -164,7 +180,7 @@ __global__ void __launch_bounds__(kBsThreads, 1)
             for (; it < span.total; ++it, span.advance(it, t, kb)) {
                 if (it == 0 || kb == 0 || it == span.dp_steps)   // a new tile (a stream-K range may start mid-tile)
                     geo = tile_geo<MOE>(args, t, BN, n_leaders);
-                if ((it & 1) != par)
+                if (!kOneProducer && (it & 1) != par)
                     continue;
                 const int s = it % STAGES;
                 const uint32_t ph = (it / STAGES) & 1;
@@ -179,19 +195,21 @@ __global__ void __launch_bounds__(kBsThreads, 1)
                 ptx::mbar_arrive_expect_tx(sa_full_bar(a), L::SA_BYTES);
                 ptx::tma_load_2d(sbase + L::OFF_SA + a * L::SA_BYTES, &tmSA, sa_full_bar(a), geo.a_row, kb);
             }
-            // Every load issued must have landed before the CTA exits.
-            for (int s = par; s < STAGES; s += 2) {
+            // Every load issued must have landed before the CTA exits: wait for
+            // the last use of each stage this producer filled (earlier uses
+            // landed before the stage could be refilled).
+            for (int s = kOneProducer ? 0 : par; s < STAGES; s += kOneProducer ? 1 : 2) {
                 const int uses = it > s ? (it - s + STAGES - 1) / STAGES : 0;
                 if (uses > 0)
                     wait_teardown(full_bar(s), (uses - 1) & 1, args);
             }
-            for (int a = par; a < kSaSlots; a += 2) {
+            for (int a = kOneProducer ? 0 : par; a < kSaSlots; a += kOneProducer ? 1 : 2) {
                 const int uses = it > a ? (it - a + kSaSlots - 1) / kSaSlots : 0;
                 if (uses > 0)
                     wait_teardown(sa_full_bar(a), (uses - 1) & 1, args);
             }
         }
-    } else {
+    } else if (warp == 1 || warp == 2) {
         // -------------------------------------------------------- MMA issuers
         // Warp 1 issues the MMAs of the even steps, warp 2 those of the odd
         // steps (NBUF is even, so each TMEM buffer, like each stage, has one
@@ -211,6 +229,10 @@ __global__ void __launch_bounds__(kBsThreads, 1)
                 const uint32_t ph = (it / STAGES) & 1;
                 const int buf = it % L::NBUF;
                 const uint32_t tph = (it / L::NBUF) & 1;
+                // Odd stage count: first the buffer, whose release orders this
+                // wait after the stage's previous use (see kOneProducer).
+                if (kOneProducer && !wait_bounded(tempty_bar(buf, 0), tph ^ 1, abort_flag, args))
+                    break;
                 if (!wait_bounded(full_bar(s), ph, abort_flag, args))
                     break;
                 const uint64_t adesc = ptx::desc_kmajor_sw128(sbase + L::OFF_A + s * L::A_BYTES);
@@ -254,7 +276,8 @@ __global__ void __launch_bounds__(kBsThreads, 1)
         const int q = warp & 3;                      // TMEM lane quadrant this warp may access
         const int row = q * 32 + lane;               // row of the tile
         const int NB = (args.N + 127) / 128;
-        const uint32_t cstage = sbase + L::OFF_C + ew * kCStageBytes;
+        const uint32_t cstage = sbase + L::OFF_C + ew * L::C_BYTES;
+        int cbuf = 0;   // wide staging: which of the warp's two 4 KiB buffers the next chunk uses
         WorkSpan span;
         span.init(args, KB, tiles);
         const int total = span.total;
@@ -429,6 +452,13 @@ __global__ void __launch_bounds__(kBsThreads, 1)
 #pragma unroll
                 for (int c = 0; c < HALF / 64; ++c)
                     store_c8_chunk(&tmC, cstage, lane, acc + c * 64, args.c_scale, x0 + c * 64, y0, args.M, args.N);
+            } else if constexpr (L::WIDE_C) {
+#pragma unroll
+                for (int c = 0; c < HALF / 64; ++c) {
+                    store_c64_chunk(&tmC, cstage + 4096u * (cbuf & 1), lane, acc + c * 64, x0 + c * 64, y0, args.M,
+                                    args.N);
+                    ++cbuf;
+                }
             } else {
 #pragma unroll
                 for (int c = 0; c < HALF / kCChunkCols; ++c)
@@ -483,6 +513,8 @@ cudaError_t launch_blockscale_moe(const CUtensorMap &tmA, const CUtensorMap &tmB
 template cudaError_t launch_blockscale<256, 4>(const CUtensorMap &, const CUtensorMap &, const CUtensorMap &,
                                                const CUtensorMap &, const GemmArgs &, int, cudaStream_t);
 template cudaError_t launch_blockscale<128, 6>(const CUtensorMap &, const CUtensorMap &, const CUtensorMap &,
+                                               const CUtensorMap &, const GemmArgs &, int, cudaStream_t);
+template cudaError_t launch_blockscale<256, 3>(const CUtensorMap &, const CUtensorMap &, const CUtensorMap &,
                                                const CUtensorMap &, const GemmArgs &, int, cudaStream_t);
 template cudaError_t launch_blockscale_moe<256, 4>(const CUtensorMap &, const CUtensorMap &, const CUtensorMap &,
                                                    const CUtensorMap &, const GemmArgs &, int, cudaStream_t);

@@ -133,9 +133,15 @@ def test_config_selection(lib):
     # wide tiles for the large shapes, the narrow tile when a wide grid would starve the SMs
     # blockscale: wide one-CTA tiles for the large shape classes, the narrow tile
     # when a wide grid would starve the SMs
-    for M, N, K in [(4096, 2048, 7168), (16384, 1536, 7168), (16384, 7168, 768), (4096, 65536, 1536)]:
+    for M, N, K in [(4096, 2048, 7168), (16384, 1536, 7168), (4096, 65536, 1536)]:
         c = lib.decode_config(lib.select_config("bs", M, N, K, 152))
         assert c["kind"] == "blockscale" and c["block_n"] == 256 and c["stages"] == 4
+    # few K blocks per tile (K <= 1024): the three-stage instance with the wider C staging
+    for M, N, K in [(16384, 7168, 768), (16384, 7168, 1024), (4096, 4096, 512)]:
+        c = lib.decode_config(lib.select_config("bs", M, N, K, 152))
+        assert c["kind"] == "blockscale" and c["block_n"] == 256 and c["stages"] == 3, (M, N, K, c)
+    assert lib.decode_config(lib.select_config("bs", 16384, 7168, 1152, 152))["stages"] == 4
+    assert lib.decode_config(lib.select_config("mx", 16384, 7168, 768, 152))["stages"] != 3
     assert lib.decode_config(lib.select_config("bs", 256, 512, 512, 152))["block_n"] == 128
     # mxfp8: wide tiles, the narrow tile when the wide grid would starve the SMs
     assert lib.decode_config(lib.select_config("mx", 16384, 5120, 2048, 152))["block_n"] == 256
