@@ -75,6 +75,13 @@ def parse():
                    help="default line: skip timing the two gated MXFP8 workloads (M = 16384) beside it")
     p.add_argument("--ref-seconds", type=float, default=240.0,
                    help="reference arm: CPU time budget of the whole run (warm-up + timed steps)")
+    p.add_argument("--raster", type=int, choices=[0, 1], default=None,
+                   help="force the tile order of the workload's configuration (0: N panels in groups, M inside; "
+                        "1: the converse); default: the shape rule's")
+    p.add_argument("--raster-group", type=int, default=0, help="panels per raster group (0 = default 1)")
+    p.add_argument("--raster-sweep", action="store_true",
+                   help="time the workload's GEMM for both raster directions and several group sizes "
+                        "(skill card 'Mechanism B'); one JSON line")
     p.add_argument("--cpu-all", action="store_true",
                    help="time the oracle on every workload (full C, all host cores) and on one core for the "
                         "smallest blockscale and MXFP8 workloads; one JSON line, no GPU")
@@ -345,6 +352,54 @@ def run_cpu_all(args):
     return 0
 
 
+def apply_raster_knobs(args, f, kind, M, N, K):
+    """--raster / --raster-group: force the tile order of the shape rule's configuration."""
+    f.set_raster_group(args.raster_group)
+    if args.raster is not None:
+        cid = f.select_config(kind, M, N, K, f.device_info()["num_sms"])
+        f.set_config_override(cid - ((cid // 10) % 10) * 10 + 10 * args.raster)
+
+
+def run_raster_sweep(args):
+    """Time the workload's GEMM (its own configuration) under each tile order:
+    raster 0 / 1 and panel groups of 1, 2, 4, 8, 16 (L2 flushed, CUDA events)."""
+    import torch
+    import fp8_block_scaled_e4m3_gb300 as f
+    kind, M, N, K = workload_shape(args.workload)
+    _, _, d = make_device_inputs(kind, M, N, K, args.seed, torch)
+    C = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    gemm = f.gemm_blockscale if kind == "bs" else f.gemm_mxfp8
+    flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.int32, device="cuda")
+    stream = torch.cuda.current_stream()
+    base = f.select_config(kind, M, N, K, f.device_info()["num_sms"])
+    n = max(10, min(args.steps, 50))
+    rows = []
+    try:
+        for raster in (0, 1):
+            for group in (1, 2, 4, 8, 16):
+                f.set_config_override(base - ((base // 10) % 10) * 10 + 10 * raster)
+                f.set_raster_group(group)
+                for _ in range(3):
+                    gemm(d[0], d[1], d[2], d[3], C=C)
+                ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+                for a, b in ev:
+                    flush.fill_(1)
+                    a.record(stream)
+                    gemm(d[0], d[1], d[2], d[3], C=C)
+                    b.record(stream)
+                torch.cuda.synchronize()
+                assert f.get_status() == 0
+                us = statistics.mean(a.elapsed_time(b) for a, b in ev) * 1e3
+                rows.append({"raster": raster, "group": group, "config_id": f.last_config_id(), "us": us,
+                             "tflops": 2.0 * M * N * K / (us * 1e-6) / 1e12})
+    finally:
+        f.set_config_override(0)
+        f.set_raster_group(0)
+    print(json.dumps({"raster_sweep": args.workload, "M": M, "N": N, "K": K, "shape_rule_config": base,
+                      "l2": "flushed", "steps": n, "points": rows}), flush=True)
+    return 0
+
+
 def run_ours(args):
     import torch
     world, rank, local = dist_setup(args)
@@ -368,6 +423,7 @@ def run_ours(args):
     def step():
         gemm(d[0], d[1], d[2], d[3], C=C)
 
+    apply_raster_knobs(args, f, kind, M, N, K)
     # correctness gate and runtime signature before timing
     step()
     assert f.get_status() == 0
@@ -434,6 +490,9 @@ def run_ours(args):
     torch.cuda.synchronize()
     assert f.get_status() == 0
     hot_ms = statistics.mean(a.elapsed_time(b) for a, b in hev)
+    if args.raster is not None or args.raster_group:
+        f.set_config_override(0)   # the twin and the MXFP8 lines below run their own shape rules
+        f.set_raster_group(0)
 
     flops = 2.0 * M * N * K
     value = aggregate_tflops(world, flops, ms)
@@ -927,6 +986,8 @@ def main():
         return run_cpu_all(args)
     if args.ksweep:
         return run_ksweep(args)
+    if args.raster_sweep:
+        return run_raster_sweep(args)
     moe = workloads.WORKLOADS[args.workload]["kind"] == "moe"
     if args.impl == "reference":
         return run_moe_reference(args) if moe else run_reference(args)

@@ -60,6 +60,7 @@ _SIGS = {
     "fp8bs_launches_per_call": (_i, []),
     "fp8bs_set_wait_limit_ns": (None, [ctypes.c_uint64]),
     "fp8bs_set_config_override": (_i, [_i]),
+    "fp8bs_set_raster_group": (_i, [_i]),
     "fp8bs_device_info": (_i, [_p, _p]),
     "fp8bs_version": (ctypes.c_char_p, []),
 }
@@ -337,6 +338,11 @@ def device_info() -> dict:
 def set_config_override(config_id: int) -> None:
     """Force a kernel configuration (0 = choose by shape); see include/fp8bs.h."""
     _check(_lib.fp8bs_set_config_override(int(config_id)), "fp8bs_set_config_override")
+
+
+def set_raster_group(group: int) -> None:
+    """Tile-order group size of later launches (0 = default 1); see include/fp8bs.h."""
+    _check(_lib.fp8bs_set_raster_group(int(group)), "fp8bs_set_raster_group")
 
 
 def set_wait_limit_ns(ns: int) -> None:

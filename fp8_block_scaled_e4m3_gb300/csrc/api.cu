@@ -54,6 +54,7 @@ std::mutex g_mutex;
 DeviceState g_dev[kMaxDevices];
 std::atomic<unsigned long long> g_wait_limit_ns{kDefaultWaitLimitNs};
 std::atomic<int> g_config_override{0};
+std::atomic<int> g_raster_group{1};   // panels per raster group (1 = plain M-inner / N-inner order)
 std::atomic<unsigned long long> g_sk_token{0};   // stream-K hand-off tokens, unique per call
 // Whether clusters of n CTAs (2..8) of the MXFP8 decode kernel fit on a device:
 // 0 not yet asked, 1 yes, -1 no. A property of the device and the kernel, so it
@@ -467,7 +468,7 @@ int launch_mx(Config &cfg, const void *A, const uint8_t *a_sf, const void *B, co
         args.raster.m_tiles = (M + 2 * kBlockM - 1) / (2 * kBlockM);
         args.raster.n_tiles = (N + 255) / 256;
         args.raster.raster = cfg.raster;
-        args.raster.group = 1;
+        args.raster.group = g_raster_group.load();
         args.status = status_ptr;
         args.wait_limit_ns = g_wait_limit_ns.load();
         args.teardown_limit_ns = teardown_limit();
@@ -493,7 +494,7 @@ int launch_mx(Config &cfg, const void *A, const uint8_t *a_sf, const void *B, co
     args.raster.m_tiles = (M + kBlockM - 1) / kBlockM;
     args.raster.n_tiles = (N + cfg.block_n - 1) / cfg.block_n;
     args.raster.raster = cfg.raster;
-    args.raster.group = 1;
+    args.raster.group = g_raster_group.load();
     args.a_sf = a_sf;
     args.b_sf = b_sf;
     args.alpha = alpha;
@@ -563,7 +564,7 @@ int blockscale_gemm(const void *A, const float *a_scale, const void *B, const fl
     args.raster.m_tiles = (M + kBlockM - 1) / kBlockM;
     args.raster.n_tiles = (N + cfg.block_n - 1) / cfg.block_n;
     args.raster.raster = cfg.raster;
-    args.raster.group = 1;
+    args.raster.group = g_raster_group.load();
     args.b_scale = b_scale;
     args.status = st->status_ptr;
     args.wait_limit_ns = g_wait_limit_ns.load();
@@ -731,7 +732,7 @@ int moe_gemm(const void *A, const float *a_scale, const void *B, const float *b_
     args.raster.m_tiles = (M + kBlockM - 1) / kBlockM;
     args.raster.n_tiles = (N + cfg.block_n - 1) / cfg.block_n;
     args.raster.raster = 0;
-    args.raster.group = 1;
+    args.raster.group = 1;   // unused: the grouped mode orders tiles by leader
     args.b_scale = b_scale;
     args.status = st->status_ptr;
     args.wait_limit_ns = g_wait_limit_ns.load();
@@ -1020,6 +1021,14 @@ int fp8mx_select_config(int M, int N, int K, int num_sms)
     if (check_shape(M, N, K) || num_sms <= 0)
         return FP8BS_ERR_SHAPE;
     return config_id(choose_config(2, M, N, K, num_sms));
+}
+
+int fp8bs_set_raster_group(int group)
+{
+    if (group < 0 || group > 4096)
+        return FP8BS_ERR_SHAPE;
+    g_raster_group.store(group ? group : 1);
+    return FP8BS_OK;
 }
 
 int fp8bs_set_config_override(int config_id)

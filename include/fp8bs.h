@@ -302,6 +302,15 @@ int fp8mx_select_config(int M, int N, int K, int num_sms);
  * Returns FP8BS_ERR_SHAPE for an id that names no built kernel. For tests and
  * measurements of each kernel variant. */
 int fp8bs_set_config_override(int config_id);
+/* Tile-order group size of subsequent GEMM launches in this process (1..4096;
+ * 0 restores the default 1). The raster visits tiles in groups of `group`
+ * panels of the smaller operand and walks the larger operand inside a group,
+ * so a group's panels stay resident in L2 while the other operand streams
+ * past (skill card "FlyDSL fp8 blockscale GEMM", section "Mechanism B": tile
+ * order as an L2-locality lever). Any group size gives the same result. For
+ * measurements (the default of 1 is what the configuration ids report).
+ * FP8BS_ERR_SHAPE for a value outside that range. */
+int fp8bs_set_raster_group(int group);
 /* SM count of the current device and the number of two-CTA clusters of the
  * CTA-pair MXFP8 kernel that can be resident at once (its persistent grid size). */
 int fp8bs_device_info(int *num_sms, int *pair_clusters);

@@ -169,6 +169,8 @@ def test_config_selection(lib):
     for bad in (6256601, 6128401, 6128602, 6128611):
         assert L.fp8bs_set_config_override(bad) == -3
     assert L.fp8bs_set_config_override(0) == 0
+    assert L.fp8bs_set_raster_group(-1) == -3 and L.fp8bs_set_raster_group(4097) == -3
+    assert L.fp8bs_set_raster_group(8) == 0 and L.fp8bs_set_raster_group(0) == 0
     for M, N, K in [(1, 5120, 2048), (32, 8192, 1280), (128, 5120, 2048)]:
         assert lib.decode_config(lib.select_config("mx", M, N, K, 152))["kind"] == "mxfp8"
 

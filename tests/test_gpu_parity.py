@@ -312,6 +312,34 @@ def test_full_mxfp8(M, N, K, seed):
     _check_full_size("mx", M, N, K, seed)
 
 
+def test_raster_group_sizes_give_the_same_bits(override):
+    """The tile order (raster direction and group size) changes which CTA computes
+    which tile, never a tile's arithmetic: every order gives the same bits, for
+    both GEMMs and with a group that does not divide the panel count."""
+    import fp8_block_scaled_e4m3_gb300 as f
+    x = workloads.make_blockscale_inputs(600, 1800, 512, seed=91)
+    y = workloads.make_mxfp8_inputs(600, 1800, 512, seed=92)
+    ref_bs = ref_mx = None
+    try:
+        for raster in (0, 1):
+            override(1256401 + 10 * raster)
+            for group in (1, 2, 3, 8):
+                f.set_raster_group(group)
+                got = run_blockscale(x.A, x.a_scale, x.B, x.b_scale)
+                ref_bs = got if ref_bs is None else ref_bs
+                assert np.array_equal(got, ref_bs), (raster, group)
+        override(0)
+        for group in (1, 4, 7):
+            f.set_raster_group(group)
+            got = run_mxfp8(y.A, y.a_e8m0, y.B, y.b_e8m0)
+            ref_mx = got if ref_mx is None else ref_mx
+            assert np.array_equal(got, ref_mx), group
+    finally:
+        f.set_raster_group(0)
+    compare(ref_bs, oracle.blockscale(x.A, x.a_scale, x.B, x.b_scale), "raster groups, blockscale")
+    compare(ref_mx, oracle.mxfp8(y.A, y.a_e8m0, y.B, y.b_e8m0), "raster groups, mxfp8")
+
+
 # ---------------------------------------------------------------- stream-K
 @pytest.mark.parametrize("cfg", [1256402, 1256302])
 def test_stream_k_repeated_calls_same_bits(override, cfg):
