@@ -77,13 +77,9 @@ struct BsLayout {
     static constexpr int OFF_C = (OFF_SA + kSaSlots * SA_BYTES + 1023) / 1024 * 1024;
     static constexpr int OFF_BAR = OFF_C + kEpiWarps * C_BYTES;
     static constexpr int NBUF = 512 / BN;        // TMEM partial buffers
-    // Column parts of a buffer with barriers of their own: the 256-wide tile's
-    // MMAs go out as two N = 128 halves, each signalled to (and released by)
-    // the promote warpgroup that owns those columns.
-    static constexpr int NSUB = BN == 256 ? 2 : 1;
     static_assert(NBUF % 2 == 0, "two MMA issuers split the buffers by parity");
     // full[S], empty[S], tfull[NBUF], tempty[NBUF], mma_done, sa_full[kSaSlots], sa_empty[kSaSlots]
-    static constexpr int NBAR = 2 * STAGES + 2 * NBUF * NSUB + 1 + 2 * kSaSlots;
+    static constexpr int NBAR = 2 * STAGES + 2 * NBUF + 1 + 2 * kSaSlots;
     static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
     static constexpr int BYTES = OFF_MISC + 16;
     static constexpr int DYN_SMEM = BYTES + 1024;   // slack to align the base to 1024
@@ -113,9 +109,9 @@ __global__ void __launch_bounds__(kBsThreads, 1)
 
     auto full_bar = [&](int s) { return sbase + L::OFF_BAR + 8u * s; };
     auto empty_bar = [&](int s) { return sbase + L::OFF_BAR + 8u * (STAGES + s); };
-    constexpr int NT = L::NBUF * L::NSUB;   // TMEM (buffer, column part) barriers
-    auto tfull_bar = [&](int b, int h) { return sbase + L::OFF_BAR + 8u * (2 * STAGES + b * L::NSUB + h); };
-    auto tempty_bar = [&](int b, int h) { return sbase + L::OFF_BAR + 8u * (2 * STAGES + NT + b * L::NSUB + h); };
+    constexpr int NT = L::NBUF;   // TMEM buffer barriers
+    auto tfull_bar = [&](int b) { return sbase + L::OFF_BAR + 8u * (2 * STAGES + b); };
+    auto tempty_bar = [&](int b) { return sbase + L::OFF_BAR + 8u * (2 * STAGES + NT + b); };
     const uint32_t mma_done_bar = sbase + L::OFF_BAR + 8u * (2 * STAGES + 2 * NT);
     auto sa_full_bar = [&](int a) { return sbase + L::OFF_BAR + 8u * (2 * STAGES + 2 * NT + 1 + a); };
     auto sa_empty_bar = [&](int a) { return sbase + L::OFF_BAR + 8u * (2 * STAGES + 2 * NT + 1 + kSaSlots + a); };
@@ -131,11 +127,10 @@ __global__ void __launch_bounds__(kBsThreads, 1)
             ptx::mbar_init(sa_full_bar(a), 1);
             ptx::mbar_init(sa_empty_bar(a), kEpiWarps);   // every promote warp has read the slice
         }
-        for (int b = 0; b < L::NBUF; ++b)
-            for (int h = 0; h < L::NSUB; ++h) {
-                ptx::mbar_init(tfull_bar(b, h), 1);
-                ptx::mbar_init(tempty_bar(b, h), kEpiWarps / L::NSUB);   // the warps owning those columns
-            }
+        for (int b = 0; b < L::NBUF; ++b) {
+            ptx::mbar_init(tfull_bar(b), 1);
+            ptx::mbar_init(tempty_bar(b), kEpiWarps);     // every promote warp has loaded its slice
+        }
         ptx::mbar_init(mma_done_bar, 2);                  // both MMA issuers
         *abort_flag = 0;
         ptx::fence_mbar_init();
@@ -220,8 +215,7 @@ __global__ void __launch_bounds__(kBsThreads, 1)
         // different phases, which a parity wait cannot tell apart.)
         if (lane == 0) {
             const int par = warp - 1;
-            constexpr int SUBN = BN / L::NSUB;
-            constexpr uint32_t idesc = ptx::idesc_f8f6f4_e4m3(kBlockM, SUBN);
+            constexpr uint32_t idesc = ptx::idesc_f8f6f4_e4m3(kBlockM, BN);
             WorkSpan span;
             span.init(args, KB, tiles);
             for (int it = par; it < span.total; it += 2) {
@@ -229,32 +223,29 @@ __global__ void __launch_bounds__(kBsThreads, 1)
                 const uint32_t ph = (it / STAGES) & 1;
                 const int buf = it % L::NBUF;
                 const uint32_t tph = (it / L::NBUF) & 1;
-                // Odd stage count: first the buffer, whose release orders this
-                // wait after the stage's previous use (see kOneProducer).
-                if (kOneProducer && !wait_bounded(tempty_bar(buf, 0), tph ^ 1, abort_flag, args))
+                // The stage and the TMEM buffer; with an odd stage count the
+                // buffer first, whose release orders the stage wait after the
+                // stage's previous use (see kOneProducer).
+                if (kOneProducer && !wait_bounded(tempty_bar(buf), tph ^ 1, abort_flag, args))
                     break;
                 if (!wait_bounded(full_bar(s), ph, abort_flag, args))
                     break;
-                const uint64_t adesc = ptx::desc_kmajor_sw128(sbase + L::OFF_A + s * L::A_BYTES);
-                bool ok = true;
-#pragma unroll
-                for (int h = 0; h < L::NSUB; ++h) {
-                    // columns [h * SUBN, (h+1) * SUBN) of the buffer: B rows of that part
-                    if (!wait_bounded(tempty_bar(buf, h), tph ^ 1, abort_flag, args)) {
-                        ok = false;
-                        break;
-                    }
-                    ptx::tc_fence_after();
-                    const uint64_t bdesc =
-                        ptx::desc_kmajor_sw128(sbase + L::OFF_B + s * L::B_BYTES + h * SUBN * kBlockK);
-                    const uint32_t d = tmem_base + static_cast<uint32_t>(buf * BN + h * SUBN);
-#pragma unroll
-                    for (int kk = 0; kk < kBlockK / kMmaK; ++kk)
-                        ptx::mma_f8f6f4(d, adesc + 2 * kk, bdesc + 2 * kk, idesc, kk > 0 ? 1u : 0u);
-                    ptx::tc_commit(tfull_bar(buf, h));
-                }
-                if (!ok)
+                if (!kOneProducer && !wait_bounded(tempty_bar(buf), tph ^ 1, abort_flag, args))
                     break;
+                ptx::tc_fence_after();
+                // One N = BN MMA per 32-wide K slice: on the 256-wide tile, two
+                // N = 128 halves with barriers of their own measured slower
+                // (4096x2048x7168 64.1 -> 61.7 us, 16384x1536x7168 153.0 ->
+                // 149.1 us without the split): twice the MMA instructions, and
+                // issuing them holds up the promote warps of the issuer's SM
+                // sub-partition.
+                const uint64_t adesc = ptx::desc_kmajor_sw128(sbase + L::OFF_A + s * L::A_BYTES);
+                const uint64_t bdesc = ptx::desc_kmajor_sw128(sbase + L::OFF_B + s * L::B_BYTES);
+                const uint32_t d = tmem_base + static_cast<uint32_t>(buf * BN);
+#pragma unroll
+                for (int kk = 0; kk < kBlockK / kMmaK; ++kk)
+                    ptx::mma_f8f6f4(d, adesc + 2 * kk, bdesc + 2 * kk, idesc, kk > 0 ? 1u : 0u);
+                ptx::tc_commit(tfull_bar(buf));
                 ptx::tc_commit(empty_bar(s));
             }
             // No MMA may still be running when the tensor memory is freed.
@@ -328,7 +319,7 @@ __global__ void __launch_bounds__(kBsThreads, 1)
                 const uint32_t aph = (it / kSaSlots) & 1;
                 const int buf = it % L::NBUF;
                 const uint32_t tph = (it / L::NBUF) & 1;
-                if (!wait_bounded_warp(tfull_bar(buf, L::NSUB == 2 ? wg : 0), tph, abort_flag, args) ||
+                if (!wait_bounded_warp(tfull_bar(buf), tph, abort_flag, args) ||
                     !wait_bounded_warp(sa_full_bar(a), aph, abort_flag, args)) {
                     ok = false;
                     break;
@@ -347,7 +338,7 @@ __global__ void __launch_bounds__(kBsThreads, 1)
                     ptx::tc_fence_before();
                     __syncwarp();
                     if (lane == 0) {
-                        ptx::mbar_arrive(tempty_bar(buf, L::NSUB == 2 ? wg : 0));
+                        ptx::mbar_arrive(tempty_bar(buf));
                         ptx::mbar_arrive(sa_empty_bar(a));
                     }
 #pragma unroll
@@ -367,7 +358,7 @@ __global__ void __launch_bounds__(kBsThreads, 1)
                             ptx::tc_fence_before();
                             __syncwarp();
                             if (lane == 0) {
-                                ptx::mbar_arrive(tempty_bar(buf, L::NSUB == 2 ? wg : 0));
+                                ptx::mbar_arrive(tempty_bar(buf));
                                 ptx::mbar_arrive(sa_empty_bar(a));
                             }
                         }
