@@ -56,6 +56,8 @@ def kernel_name(decoded):
         return "fp8bs_mxfp8_pair_kernel"
     if kind == "mxfp8":
         return "fp8bs_mxfp8_sk_kernel" if sched == "stream_k" else "fp8bs_mxfp8_kernel"
+    if kind == "blockscale_pair":
+        return "fp8bs_blockscale_pair_kernel"
     return "fp8bs_blockscale_kernel"
 
 

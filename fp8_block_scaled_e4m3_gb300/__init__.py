@@ -321,7 +321,7 @@ def select_config(kind: str, M: int, N: int, K: int, num_sms: int) -> int:
 
 
 def decode_config(cid: int) -> dict:
-    return {"kind": {1: "blockscale", 2: "mxfp8", 4: "tensorscale", 5: "mxfp8_pair",
+    return {"kind": {1: "blockscale", 2: "mxfp8", 3: "blockscale_pair", 4: "tensorscale", 5: "mxfp8_pair",
                       6: "mxfp8_decode"}.get(cid // 1000000, "?"),
             "block_n": (cid // 1000) % 1000,
             "stages": (cid // 100) % 10, "raster": (cid // 10) % 10,

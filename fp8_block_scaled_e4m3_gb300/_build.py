@@ -11,7 +11,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libfp8bs.so")
-SOURCES = ["api.cu", "bs_kernel.cu", "mx_kernel.cu", "mx2_kernel.cu", "mxd_kernel.cu"]
+SOURCES = ["api.cu", "bs_kernel.cu", "bs2_kernel.cu", "mx_kernel.cu", "mx2_kernel.cu", "mxd_kernel.cu"]
 HEADERS = ["ptx.cuh", "common.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

@@ -21,6 +21,11 @@ template <int BN, int STAGES>
 cudaError_t launch_blockscale_moe(const CUtensorMap &, const CUtensorMap &, const CUtensorMap &, const CUtensorMap &,
                                   const GemmArgs &, int, cudaStream_t);
 template <int STAGES>
+cudaError_t launch_blockscale_pair(const CUtensorMap &, const CUtensorMap &, const CUtensorMap &, const CUtensorMap &,
+                                   const GemmArgs &, int, cudaStream_t);
+template <int STAGES>
+cudaError_t max_bs_pair_clusters(int *);
+template <int STAGES>
 cudaError_t launch_mxfp8_pair(const CUtensorMap &, const CUtensorMap &, const CUtensorMap &, const CUtensorMap &,
                               const CUtensorMap &, const GemmArgs &, int, cudaStream_t);
 template <int STAGES>
@@ -40,6 +45,8 @@ __device__ int g_status_word;   // per-device status written by the kernels
 constexpr int kMaxDevices = 64;
 constexpr unsigned long long kDefaultWaitLimitNs = 2000000000ull;
 constexpr int kMxPairStages = 6;
+constexpr int kBsPairStages = 6;
+constexpr int kPairMinKBlocks = 12;   // K blocks per tile from which the blockscale pair kernel may be chosen
 
 struct DeviceState {
     bool ready = false;
@@ -48,6 +55,7 @@ struct DeviceState {
     int *status_ptr = nullptr;      // device address of g_status_word
     cudaMemPool_t pool = nullptr;   // stream-ordered pool for fp8mx_gemm's packed scales
     int mx_pair_clusters = 0;       // co-resident CTA pairs of the MXFP8 pair kernel
+    int bs_pair_clusters = 0;       // co-resident CTA pairs of the blockscale pair kernel
 };
 
 std::mutex g_mutex;
@@ -98,6 +106,8 @@ int ensure_device(int &dev, DeviceState *&st)
     if (cudaMemPoolSetAttribute(st->pool, cudaMemPoolAttrReleaseThreshold, &keep) != cudaSuccess)
         return st->status = FP8BS_ERR_CUDA;
     if (max_mx_pair_clusters<kMxPairStages>(&st->mx_pair_clusters) != cudaSuccess || st->mx_pair_clusters < 1)
+        return st->status = FP8BS_ERR_CUDA;
+    if (max_bs_pair_clusters<kBsPairStages>(&st->bs_pair_clusters) != cudaSuccess || st->bs_pair_clusters < 1)
         return st->status = FP8BS_ERR_CUDA;
     if (!g_encode) {
         cudaDriverEntryPointQueryResult q;
@@ -170,6 +180,8 @@ bool decode_config_id(int id, Config &c)
         return (c.block_n == 256 && (c.stages == 4 || c.stages == 3)) || (c.block_n == 128 && c.stages == 6);
     if (c.kind == 2 || c.kind == 4)
         return (c.block_n == 256 && c.stages == 4) || (c.block_n == 128 && c.stages == 6);
+    if (c.kind == 3)
+        return c.block_n == 256 && c.stages == kBsPairStages && c.sched == 1;
     if (c.kind == 5)
         return c.block_n == 256 && c.stages == kMxPairStages && c.sched == 1;
     if (c.kind == 6)
@@ -324,8 +336,24 @@ constexpr int kWideCMaxKBlocks = 8;
 Config choose_config(int kind, int M, int N, int K, int num_sms)
 {
     Config c = choose_config_base(kind, M, N, K, num_sms);
-    if (kind == 1 && c.block_n == 256 && K / 128 <= kWideCMaxKBlocks)
+    if (kind == 1 && c.block_n == 256 && K / 128 <= kWideCMaxKBlocks) {
         c.stages = 3;
+    } else if (kind == 1 && c.block_n == 256 && c.sched == 1 && K / 128 >= kPairMinKBlocks) {
+        // One CTA per tile, at least four waves of 256 x 256 tiles over the CTA
+        // pairs and at least 12 K blocks per tile: the pair kernel (half of B
+        // per CTA, six stages, half the MMA instructions per SM). Same-session
+        // times (us, L2 flushed, one-CTA -> pair): 8192x8192x3072 184.7 ->
+        // 181.3, 16384x7168x2048 224.1 -> 221.7, 4096x65536x1536 397.0 ->
+        // 393.5; at fewer waves it gains nothing (4096x2048x7168 62.2 -> 61.6,
+        // 2048x2048x7168 34.8 -> 34.9), and with few K blocks its narrow C
+        // staging loses (16384x7168x768 112.9 with the three-stage instance,
+        // ~120 with four stages, 122.7 with the pair).
+        const long long pair_tiles = static_cast<long long>((M + 255) / 256) * ((N + 255) / 256);
+        if (num_sms >= 2 && pair_tiles >= 4ll * (num_sms / 2)) {
+            c.kind = 3;
+            c.stages = kBsPairStages;
+        }
+    }
     return c;
 }
 
@@ -539,14 +567,20 @@ int blockscale_gemm(const void *A, const float *a_scale, const void *B, const fl
     if ((rc = ensure_device(dev, st)))
         return rc;
     Config cfg = choose_config(1, M, N, K, st->num_sms);
-    if (!override_config(1, 1, cfg))
+    if (c_e4m3 && cfg.kind == 3)
+        cfg = choose_config_base(1, M, N, K, st->num_sms);   // the E4M3 store is the one-CTA kernel's
+    if (!override_config(1, 3, cfg))
         return FP8BS_ERR_SHAPE;
+    const bool pair = cfg.kind == 3;   // CTA-pair kernel: 256 x 256 tiles, half of the B tile per CTA
+    if (pair && c_e4m3)
+        return FP8BS_ERR_SHAPE;         // forced by the override
     const int KB = K / 128;
     const uint64_t ld_sa = static_cast<uint64_t>(fp8bs_a_scale_ld(M));
     const bool wide_c = cfg.block_n == 256 && cfg.stages == 3;   // 32 x 64 bf16 C boxes, 128-byte swizzle
     CUtensorMap tmA, tmB, tmSA, tmC;
     if (!encode_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, A, K, M, K, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !encode_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, B, K, N, K, 128, cfg.block_n, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, B, K, N, K, 128, pair ? cfg.block_n / 2 : cfg.block_n,
+                   CU_TENSOR_MAP_SWIZZLE_128B) ||
         !encode_2d(&tmSA, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, a_scale, ld_sa, KB, ld_sa * 4, 128, 1,
                    CU_TENSOR_MAP_SWIZZLE_NONE) ||
         !(c_e4m3 ? encode_2d(&tmC, CU_TENSOR_MAP_DATA_TYPE_UINT8, C, N, M, static_cast<uint64_t>(N), 64, 32,
@@ -561,7 +595,7 @@ int blockscale_gemm(const void *A, const float *a_scale, const void *B, const fl
     args.K = K;
     args.c_e4m3 = c_e4m3 ? 1 : 0;
     args.c_scale = c_scale;
-    args.raster.m_tiles = (M + kBlockM - 1) / kBlockM;
+    args.raster.m_tiles = (M + (pair ? 2 * kBlockM : kBlockM) - 1) / (pair ? 2 * kBlockM : kBlockM);
     args.raster.n_tiles = (N + cfg.block_n - 1) / cfg.block_n;
     args.raster.raster = cfg.raster;
     args.raster.group = g_raster_group.load();
@@ -572,6 +606,12 @@ int blockscale_gemm(const void *A, const float *a_scale, const void *B, const fl
     const int tiles = args.raster.num_tiles();
     int grid = tiles < st->num_sms ? tiles : st->num_sms;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (pair) {
+        if (launch_blockscale_pair<kBsPairStages>(tmA, tmB, tmSA, tmC, args, st->bs_pair_clusters, s) != cudaSuccess)
+            return FP8BS_ERR_LAUNCH;
+        t_last_config = config_id(cfg);
+        return FP8BS_OK;
+    }
     void *ws = nullptr;
     if (cfg.sched == 2) {
         if (cfg.block_n != 256)

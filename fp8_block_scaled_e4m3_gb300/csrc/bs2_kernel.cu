@@ -1,0 +1,374 @@
+// FP8 block-scaled GEMM kernel for sm_103a, CTA-pair version.
+//
+// Same result as fp8bs_blockscale_kernel (bs_kernel.cu):
+//   C[m,n] = bf16( sum_kb P_kb[m,n] * a_scale[m,kb] * b_scale[n/128,kb] ),
+// P_kb the unscaled fp8 product of 128-wide K block kb, promoted in fp32 after
+// the matrix unit (skill card "FlyDSL fp8 blockscale GEMM", "Mechanism A").
+//
+// Two CTAs of a cluster (two SMs) share one 256 x 256 tile. Each CTA owns 128
+// rows of A and C and holds 128 of the 256 B rows; the even CTA issues
+// tcgen05.mma.cta_group::2 (M256 x N256 x K32), which reads A from each CTA's
+// own shared memory, exchanges the B halves and writes each CTA's 128 x 256
+// partial P_kb into that CTA's tensor memory (two 256-column buffers per CTA,
+// as in the one-CTA kernel). Against the one-CTA kernel on 128 x 256 tiles:
+//   - a CTA's stage is A 16 KiB + half of B 16 KiB, so six stages fit where
+//     the one-CTA kernel has four, and the shared-memory fill per K block
+//     (the L2 -> SM stream) drops from 48 to 32 KiB per SM;
+//   - one MMA instruction does two SMs' work, so each SM issues half as many
+//     (issuing holds up the promote warps of the issuer's sub-partition).
+// The promote (fp32 FMAs on TMEM loads) and the epilogue are the one-CTA
+// kernel's, per CTA.
+//
+// Per CTA, 12 warps (3 warpgroups):
+//   warps 0, 3  TMA producers for the even and the odd K-block steps: own A
+//               rows and own B half into stage s; both CTAs' bytes complete on
+//               the even CTA's full[s], which the even CTA's producer arms with
+//               the pair's total (an odd-CTA copy may land first: the phase
+//               cannot complete before that arrive). The a_scale slice [128] of
+//               the CTA's own rows goes to a local ring.
+//   warps 1, 2  pair TMEM allocation (warp 1) and, in the even CTA only, the MMA
+//               issuers of the even and the odd steps (one thread each; each
+//               owns one TMEM buffer and every other stage); tcgen05.commit
+//               multicasts "partial ready" and the stage release to both CTAs.
+//   warps 4..11 promote + epilogue for this CTA's 128 rows: thread = one row,
+//               128 columns of one 128-column N block (one b_scale value);
+//               a buffer is released on the even CTA's tempty barrier (16
+//               arrivals, 8 warps of each CTA; the odd CTA's are relaxed remote
+//               arrives).
+// One CTA pair per tile (no stream-K); E4M3 C runs on the one-CTA kernel.
+#include "common.cuh"
+
+namespace fp8bs {
+
+constexpr int kBs2Threads = (4 + kEpiWarps) * 32;
+constexpr int kBs2BN = 256;             // N of the pair tile and of each CTA's partial
+constexpr int kBs2NBuf = 2;             // TMEM partial buffers per CTA (2 x 256 columns)
+constexpr int kBs2SaSlots = 16;
+// Register split as in the one-CTA kernel's 256-wide tile: 168 per thread at
+// launch; warpgroup 0 drops to 40 and the promote warpgroups rise to 232.
+constexpr int kBs2RegsLow = 40;
+constexpr int kBs2RegsHigh = 232;
+static_assert(128 * kBs2RegsLow + 256 * kBs2RegsHigh <= kBs2Threads * 168, "register split");
+
+template <int STAGES>
+struct Bs2Layout {
+    static constexpr int A_BYTES = kBlockM * kBlockK;             // own 128 rows
+    static constexpr int B_BYTES = (kBs2BN / 2) * kBlockK;        // own 128 of the tile's 256 B rows
+    static constexpr int SA_BYTES = kBlockM * 4;
+    static constexpr int OFF_A = 0;
+    static constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
+    static constexpr int OFF_SA = OFF_B + STAGES * B_BYTES;
+    static constexpr int OFF_C = (OFF_SA + kBs2SaSlots * SA_BYTES + 1023) / 1024 * 1024;
+    static constexpr int OFF_BAR = OFF_C + kEpiWarps * kCStageBytes;
+    // full[S], empty[S], tfull[NBUF], tempty[NBUF], mma_done, sa_full[SA], sa_empty[SA]
+    static constexpr int NBAR = 2 * STAGES + 2 * kBs2NBuf + 1 + 2 * kBs2SaSlots;
+    static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
+    static constexpr int BYTES = OFF_MISC + 16;
+    static constexpr int DYN_SMEM = BYTES + 1024;
+    static constexpr int TMEM_COLS = kBs2NBuf * kBs2BN;
+    static_assert(TMEM_COLS == 512, "tensor memory");
+    static_assert(STAGES % 2 == 0 && kBs2SaSlots % 2 == 0 && kBs2NBuf == 2,
+                  "producers and issuers split the stages, slots and buffers by step parity");
+    static_assert(DYN_SMEM <= 232448, "shared memory budget");
+};
+
+template <int STAGES>
+__global__ void __launch_bounds__(kBs2Threads, 1)
+    fp8bs_blockscale_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                                 const __grid_constant__ CUtensorMap tmSA, const __grid_constant__ CUtensorMap tmC,
+                                 const GemmArgs args)
+{
+    using L = Bs2Layout<STAGES>;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_s = ptx::smem_u32(smem_raw);
+    const uint32_t sbase = (raw_s + 1023u) & ~1023u;
+    uint8_t *smem = smem_raw + (sbase - raw_s);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const uint32_t rank = ptx::cluster_ctarank();   // 0 = even CTA (issues the MMAs)
+    const int cluster = static_cast<int>(blockIdx.x) >> 1;
+    const int num_clusters = static_cast<int>(gridDim.x) >> 1;
+    const int KB = args.K / kBlockK;
+    const int num_tiles = args.raster.num_tiles();   // pair tiles (256 x 256)
+    const int my_tiles = cluster < num_tiles ? (num_tiles - cluster + num_clusters - 1) / num_clusters : 0;
+    const int total = my_tiles * KB;                 // K-block steps of this pair
+
+    auto full_bar = [&](int s) { return sbase + L::OFF_BAR + 8u * s; };
+    auto empty_bar = [&](int s) { return sbase + L::OFF_BAR + 8u * (STAGES + s); };
+    auto tfull_bar = [&](int b) { return sbase + L::OFF_BAR + 8u * (2 * STAGES + b); };
+    auto tempty_bar = [&](int b) { return sbase + L::OFF_BAR + 8u * (2 * STAGES + kBs2NBuf + b); };
+    const uint32_t mma_done_bar = sbase + L::OFF_BAR + 8u * (2 * STAGES + 2 * kBs2NBuf);
+    auto sa_full_bar = [&](int a) { return sbase + L::OFF_BAR + 8u * (2 * STAGES + 2 * kBs2NBuf + 1 + a); };
+    auto sa_empty_bar = [&](int a) {
+        return sbase + L::OFF_BAR + 8u * (2 * STAGES + 2 * kBs2NBuf + 1 + kBs2SaSlots + a);
+    };
+    uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + L::OFF_MISC);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::OFF_MISC + 4);
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            ptx::mbar_init(full_bar(s), 1);                 // even CTA's producer (expect_tx of both CTAs' bytes)
+            ptx::mbar_init(empty_bar(s), 1);                // multicast MMA commit
+        }
+        for (int b = 0; b < kBs2NBuf; ++b) {
+            ptx::mbar_init(tfull_bar(b), 1);                // multicast MMA commit
+            ptx::mbar_init(tempty_bar(b), 2 * kEpiWarps);   // promote warps of both CTAs (even CTA's copy)
+        }
+        ptx::mbar_init(mma_done_bar, 2);                    // both issuers' multicast commits
+        for (int a = 0; a < kBs2SaSlots; ++a) {
+            ptx::mbar_init(sa_full_bar(a), 1);
+            ptx::mbar_init(sa_empty_bar(a), kEpiWarps);     // this CTA's promote warps
+        }
+        *abort_flag = 0;
+        ptx::fence_mbar_init();
+    }
+    if (warp == 1) {
+        ptx::tmem_alloc_pair(ptx::smem_u32(tmem_holder), L::TMEM_COLS);
+        ptx::tmem_relinquish_pair();
+    }
+    ptx::tc_fence_before();
+    ptx::cluster_sync();   // barriers of both CTAs initialised before any remote arrive
+    ptx::tc_fence_after();
+    const uint32_t tmem_base = *tmem_holder;
+
+    if (warp < 4) {
+        ptx::setmaxnreg_dec<kBs2RegsLow>();
+        if (warp == 0 || warp == 3) {
+            // ----------------------------------------------------------- producers
+            // Warp 0 fills the stages and a_scale slots of the even steps, warp 3
+            // those of the odd steps: with even STAGES and slot counts each stage
+            // and slot has one producer thread, which waits on it phase by phase.
+            if (lane == 0) {
+                const int par = warp == 3 ? 1 : 0;
+                ptx::prefetch_tmap(&tmA);
+                ptx::prefetch_tmap(&tmB);
+                ptx::prefetch_tmap(&tmSA);
+                int it = 0;
+                bool ok = true;
+                for (int t = cluster; t < num_tiles && ok; t += num_clusters) {
+                    int mb, nb;
+                    args.raster.coords(t, mb, nb);
+                    const int row0 = mb * 2 * kBlockM + static_cast<int>(rank) * kBlockM;
+                    const int brow0 = nb * kBs2BN + static_cast<int>(rank) * (kBs2BN / 2);
+                    for (int kb = 0; kb < KB; ++kb, ++it) {
+                        if ((it & 1) != par)
+                            continue;
+                        const int s = it % STAGES;
+                        const uint32_t ph = (it / STAGES) & 1;
+                        const int a = it % kBs2SaSlots;
+                        const uint32_t aph = (it / kBs2SaSlots) & 1;
+                        if (!wait_bounded(empty_bar(s), ph ^ 1, abort_flag, args) ||
+                            !wait_bounded(sa_empty_bar(a), aph ^ 1, abort_flag, args)) {
+                            ok = false;
+                            break;
+                        }
+                        const uint32_t leader_full = ptx::mapa_shared(full_bar(s), 0);
+                        if (rank == 0)
+                            ptx::mbar_arrive_expect_tx(full_bar(s), 2 * (L::A_BYTES + L::B_BYTES));
+                        ptx::tma_load_2d_pair(sbase + L::OFF_A + s * L::A_BYTES, &tmA, leader_full, kb * kBlockK,
+                                              row0);
+                        ptx::tma_load_2d_pair(sbase + L::OFF_B + s * L::B_BYTES, &tmB, leader_full, kb * kBlockK,
+                                              brow0);
+                        ptx::mbar_arrive_expect_tx(sa_full_bar(a), L::SA_BYTES);
+                        ptx::tma_load_2d(sbase + L::OFF_SA + a * L::SA_BYTES, &tmSA, sa_full_bar(a), row0, kb);
+                    }
+                }
+                // Every load this thread issued must have landed before the CTA
+                // exits: the last use of each of its stages and slots (earlier
+                // uses landed before they could be refilled). The odd CTA learns
+                // it from the even CTA's multicast stage release.
+                for (int s = par; s < STAGES; s += 2) {
+                    const int uses = it > s ? (it - s + STAGES - 1) / STAGES : 0;
+                    if (uses > 0)
+                        wait_teardown(rank == 0 ? full_bar(s) : empty_bar(s), (uses - 1) & 1, args);
+                }
+                for (int a = par; a < kBs2SaSlots; a += 2) {
+                    const int uses = it > a ? (it - a + kBs2SaSlots - 1) / kBs2SaSlots : 0;
+                    if (uses > 0)
+                        wait_teardown(sa_full_bar(a), (uses - 1) & 1, args);
+                }
+            }
+        } else if (lane == 0 && rank == 0) {
+            // ------------------------------------------------ MMA issuers (even CTA)
+            // Warp 1 issues the even steps (TMEM buffer 0, even stages), warp 2
+            // the odd steps (buffer 1, odd stages).
+            const int par = warp - 1;
+            constexpr uint32_t idesc = ptx::idesc_f8f6f4_e4m3(2 * kBlockM, kBs2BN);
+            for (int it = par; it < total; it += 2) {
+                const int s = it % STAGES;
+                const uint32_t ph = (it / STAGES) & 1;
+                const int buf = it % kBs2NBuf;
+                const uint32_t tph = (it / kBs2NBuf) & 1;
+                if (!wait_bounded(full_bar(s), ph, abort_flag, args) ||
+                    !wait_bounded(tempty_bar(buf), tph ^ 1, abort_flag, args))
+                    break;
+                ptx::tc_fence_after();
+                const uint64_t adesc = ptx::desc_kmajor_sw128(sbase + L::OFF_A + s * L::A_BYTES);
+                const uint64_t bdesc = ptx::desc_kmajor_sw128(sbase + L::OFF_B + s * L::B_BYTES);
+                const uint32_t d = tmem_base + static_cast<uint32_t>(buf * kBs2BN);
+#pragma unroll
+                for (int kk = 0; kk < kBlockK / kMmaK; ++kk)
+                    ptx::mma_f8f6f4_pair(d, adesc + 2 * kk, bdesc + 2 * kk, idesc, kk > 0 ? 1u : 0u);
+                ptx::tc_commit_pair_mc(tfull_bar(buf), 0x3);
+                ptx::tc_commit_pair_mc(empty_bar(s), 0x3);
+            }
+            ptx::tc_commit_pair_mc(mma_done_bar, 0x3);
+        }
+        // No pair MMA may still write this CTA's tensor memory when it is freed.
+        if (warp == 1 && lane == 0)
+            wait_teardown(mma_done_bar, 0, args);
+    } else {
+        ptx::setmaxnreg_inc<kBs2RegsHigh>();
+        // ------------------------------------------------- promote + epilogue
+        constexpr int HALF = kBs2BN / 2;             // columns per thread
+        const int ew = warp - 4;                     // 0..7
+        const int wg = ew >> 2;                      // column half
+        const int q = warp & 3;                      // TMEM lane quadrant this warp may access
+        const int row = q * 32 + lane;               // row of this CTA's 128
+        const int NB = (args.N + 127) / 128;
+        const uint32_t cstage = sbase + L::OFF_C + ew * kCStageBytes;
+
+        float acc[HALF];
+        int it = 0;
+        bool ok = true;
+        for (int t = cluster; t < num_tiles && ok; t += num_clusters) {
+            // b_scale of this thread's 128-column N block for the tile's K
+            // blocks, 32 ahead: lane l holds K block 32*c + l of batch c (taken
+            // with a shuffle); batch c+1 is requested when batch c starts.
+            const float *sbrow;
+            {
+                int mb, nb;
+                args.raster.coords(t, mb, nb);
+                const int nblk = (nb * kBs2BN + wg * HALF) >> 7;
+                sbrow = nblk < NB ? args.b_scale + static_cast<size_t>(nblk) * KB : nullptr;
+            }
+            float sb_cur = sbrow && lane < KB ? ptx::ldg_nc_f32(sbrow + lane) : 0.f;
+            float sb_next = sbrow && 32 + lane < KB ? ptx::ldg_nc_f32(sbrow + 32 + lane) : 0.f;
+#pragma unroll
+            for (int j = 0; j < HALF; ++j)
+                acc[j] = 0.f;
+            for (int kb = 0; kb < KB; ++kb, ++it) {
+                const float sb = __shfl_sync(0xffffffffu, sb_cur, kb & 31);
+                if ((kb & 31) == 31) {
+                    sb_cur = sb_next;
+                    sb_next = sbrow && kb + 33 + lane < KB ? ptx::ldg_nc_f32(sbrow + kb + 33 + lane) : 0.f;
+                }
+                const int a = it % kBs2SaSlots;
+                const uint32_t aph = (it / kBs2SaSlots) & 1;
+                const int buf = it % kBs2NBuf;
+                const uint32_t tph = (it / kBs2NBuf) & 1;
+                if (!wait_bounded_warp(tfull_bar(buf), tph, abort_flag, args) ||
+                    !wait_bounded_warp(sa_full_bar(a), aph, abort_flag, args)) {
+                    ok = false;
+                    break;
+                }
+                ptx::tc_fence_after();
+                const float sa = reinterpret_cast<const float *>(smem + L::OFF_SA + a * L::SA_BYTES)[row];
+                const float scale = sa * sb;
+                const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
+                                       static_cast<uint32_t>(buf * kBs2BN + wg * HALF);
+                // Two 64-column rounds; the buffer is released once the second
+                // round is loaded.
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    uint32_t r0[32], r1[32];
+                    ptx::tmem_ld_32x32b_x32(taddr + h * 64, r0);
+                    ptx::tmem_ld_32x32b_x32(taddr + h * 64 + 32, r1);
+                    ptx::tmem_wait_ld();
+                    if (h == 1) {
+                        ptx::tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) {
+                            // the even CTA's barrier, by its cluster address from
+                            // either CTA (the loads above have completed)
+                            ptx::mbar_arrive_cluster_relaxed(ptx::mapa_shared(tempty_bar(buf), 0));
+                            ptx::mbar_arrive(sa_empty_bar(a));
+                        }
+                    }
+#pragma unroll
+                    for (int j = 0; j < 32; ++j)
+                        acc[h * 64 + j] = fmaf(__uint_as_float(r0[j]), scale, acc[h * 64 + j]);
+#pragma unroll
+                    for (int j = 0; j < 32; ++j)
+                        acc[h * 64 + 32 + j] = fmaf(__uint_as_float(r1[j]), scale, acc[h * 64 + 32 + j]);
+                }
+            }
+            if (!ok)
+                break;
+            int mb, nb;
+            args.raster.coords(t, mb, nb);
+            const int x0 = nb * kBs2BN + wg * HALF;
+            const int y0 = mb * 2 * kBlockM + static_cast<int>(rank) * kBlockM + q * 32;
+#pragma unroll
+            for (int c = 0; c < HALF / kCChunkCols; ++c)
+                store_c_chunk(&tmC, cstage, lane, acc + c * kCChunkCols, x0 + c * kCChunkCols, y0, args.M, args.N);
+        }
+        if (lane == 0)
+            ptx::bulk_wait_all();
+    }
+
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::cluster_sync();   // no remote arrive or multicast commit may target an exited CTA
+    if (warp == 1) {
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc_pair(tmem_base, L::TMEM_COLS);
+    }
+}
+
+template <int STAGES>
+cudaError_t launch_blockscale_pair(const CUtensorMap &tmA, const CUtensorMap &tmB, const CUtensorMap &tmSA,
+                                   const CUtensorMap &tmC, const GemmArgs &args, int max_clusters, cudaStream_t stream)
+{
+    using L = Bs2Layout<STAGES>;
+    auto kern = fp8bs_blockscale_pair_kernel<STAGES>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::DYN_SMEM);
+    if (e != cudaSuccess)
+        return e;
+    const int tiles = args.raster.num_tiles();
+    const int clusters = tiles < max_clusters ? tiles : max_clusters;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * clusters);
+    cfg.blockDim = dim3(kBs2Threads);
+    cfg.dynamicSmemBytes = L::DYN_SMEM;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, tmA, tmB, tmSA, tmC, args);
+}
+
+// Co-resident clusters of two CTAs for this kernel on the current device.
+template <int STAGES>
+cudaError_t max_bs_pair_clusters(int *out)
+{
+    using L = Bs2Layout<STAGES>;
+    auto kern = fp8bs_blockscale_pair_kernel<STAGES>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::DYN_SMEM);
+    if (e != cudaSuccess)
+        return e;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2);
+    cfg.blockDim = dim3(kBs2Threads);
+    cfg.dynamicSmemBytes = L::DYN_SMEM;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaOccupancyMaxActiveClusters(out, kern, &cfg);
+}
+
+template cudaError_t launch_blockscale_pair<6>(const CUtensorMap &, const CUtensorMap &,
+                                                           const CUtensorMap &, const CUtensorMap &, const GemmArgs &,
+                                                           int, cudaStream_t);
+template cudaError_t max_bs_pair_clusters<6>(int *);
+
+} // namespace fp8bs

@@ -78,6 +78,7 @@ struct BsLayout {
     static constexpr int OFF_BAR = OFF_C + kEpiWarps * C_BYTES;
     static constexpr int NBUF = 512 / BN;        // TMEM partial buffers
     static_assert(NBUF % 2 == 0, "two MMA issuers split the buffers by parity");
+    static_assert(STAGES % 2 == 1 || kSaSlots % 2 == 0, "two producers split the a_scale slots by parity");
     // full[S], empty[S], tfull[NBUF], tempty[NBUF], mma_done, sa_full[kSaSlots], sa_empty[kSaSlots]
     static constexpr int NBAR = 2 * STAGES + 2 * NBUF + 1 + 2 * kSaSlots;
     static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;

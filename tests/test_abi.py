@@ -133,9 +133,14 @@ def test_config_selection(lib):
     # wide tiles for the large shapes, the narrow tile when a wide grid would starve the SMs
     # blockscale: wide one-CTA tiles for the large shape classes, the narrow tile
     # when a wide grid would starve the SMs
-    for M, N, K in [(4096, 2048, 7168), (16384, 1536, 7168), (4096, 65536, 1536)]:
+    for M, N, K in [(4096, 2048, 7168), (16384, 1536, 7168), (2048, 2048, 7168)]:
         c = lib.decode_config(lib.select_config("bs", M, N, K, 152))
         assert c["kind"] == "blockscale" and c["block_n"] == 256 and c["stages"] == 4
+    # one CTA per tile and at least four waves of 256 x 256 tiles: the CTA-pair kernel
+    # (and at least 12 K blocks per tile)
+    for M, N, K in [(4096, 65536, 1536), (8192, 8192, 3072), (16384, 7168, 2048)]:
+        c = lib.decode_config(lib.select_config("bs", M, N, K, 152))
+        assert c["kind"] == "blockscale_pair" and c["block_n"] == 256 and c["stages"] == 6, (M, N, K, c)
     # few K blocks per tile (K <= 1024): the three-stage instance with the wider C staging
     for M, N, K in [(16384, 7168, 768), (16384, 7168, 1024), (4096, 4096, 512)]:
         c = lib.decode_config(lib.select_config("bs", M, N, K, 152))
@@ -160,7 +165,10 @@ def test_config_selection(lib):
     assert L.fp8bs_set_config_override(1160511) == -3      # the 160-wide tile was removed
     assert L.fp8bs_set_config_override(2128612) == 0       # the MXFP8 kernel's 128-wide tile has stream-K too
     assert L.fp8bs_set_config_override(4128612) == -3
-    assert L.fp8bs_set_config_override(3128811) == -3      # kind 3 (a removed kernel) names nothing built
+    assert L.fp8bs_set_config_override(3256611) == 0       # the blockscale CTA-pair kernel: 256 x 256, six stages
+    assert lib.decode_config(3256611)["kind"] == "blockscale_pair"
+    for bad in (3128811, 3256411, 3256612):                # no other tile, stage count or schedule
+        assert L.fp8bs_set_config_override(bad) == -3
     assert L.fp8bs_set_config_override(1256413) == -3      # no such schedule
     assert L.fp8bs_set_config_override(1128612) == -3      # stream-K runs with the 256-wide tile only
     # the MXFP8 decode kernel (K slices in clusters): selectable, one id only, never chosen by the rule

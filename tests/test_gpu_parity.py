@@ -178,8 +178,9 @@ def test_pack_a_scale_bit_exact():
 
 
 # every built kernel configuration, forced through the override
-# one-CTA 128x256, 128x128 (one CTA per tile), 128x256 stream-K
-BS_CONFIGS = [1256411, 1128611, 1256412, 1256311, 1256312]
+# one-CTA 128x256, 128x128 (one CTA per tile), 128x256 stream-K, three-stage
+# 128x256 (both schedules), CTA-pair 256x256
+BS_CONFIGS = [1256411, 1128611, 1256412, 1256311, 1256312, 3256611]
 MX_CONFIGS = [2256411, 2128611, 2256412, 2128612, 5256611]
 
 
@@ -310,6 +311,19 @@ def test_full_blockscale(name, seed):
 @pytest.mark.parametrize("N,K", [(5120, 2048), (8192, 1280)])
 def test_full_mxfp8(M, N, K, seed):
     _check_full_size("mx", M, N, K, seed)
+
+
+@pytest.mark.parametrize("M,N,K", [(4096, 2048, 7168), (1000, 2824, 1408), (384, 256, 128)])
+def test_blockscale_pair_kernel_full_output(override, M, N, K):
+    """The CTA-pair kernel (256 x 256 tiles) on the whole of C: the full-size
+    narrow-N workload, and ragged shapes whose last pair tile is cut in M (the
+    odd CTA's rows past M) and in N (a 128-column half past N)."""
+    import fp8_block_scaled_e4m3_gb300 as f
+    override(3256601 + 10 * (1 if M >= N else 0))
+    x = workloads.make_blockscale_inputs(M, N, K, seed=M + N)
+    got = run_blockscale(x.A, x.a_scale, x.B, x.b_scale)
+    assert f.last_config_id() == 3256601 + 10 * (1 if M >= N else 0)
+    compare_rows(got, oracle.blockscale(x.A, x.a_scale, x.B, x.b_scale), f"bs pair {M}x{N}x{K}")
 
 
 def test_raster_group_sizes_give_the_same_bits(override):
