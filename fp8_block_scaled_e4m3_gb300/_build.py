@@ -58,14 +58,15 @@ def parse_ptxas(log_path: str) -> dict:
 
 
 def check_resources(log_path: str) -> None:
-    """The blockscale kernel and the stream-K MXFP8 and tensor-scale kernels
-    re-split their registers with setmaxnreg (4 warps low, 8 high) out of a
-    launch allotment of 384 threads x 168; that split is only valid when the
-    kernel is compiled to exactly 168 registers. No kernel may spill or keep
-    an array in local memory (a stack frame)."""
+    """The blockscale kernels (one CTA and CTA pair) and the stream-K MXFP8 and
+    tensor-scale kernels re-split their registers with setmaxnreg (4 warps
+    low, 8 high) out of a launch allotment of 384 threads x 168; that split is
+    only valid when the kernel is compiled to exactly 168 registers. No kernel
+    may spill or keep an array in local memory (a stack frame)."""
     info = parse_ptxas(log_path)
     for sym, r in info.items():
-        split = any(k in sym for k in ("fp8bs_blockscale_kernel", "fp8bs_mxfp8_sk_kernel", "fp8bs_tensorscale_sk_kernel"))
+        split = any(k in sym for k in ("fp8bs_blockscale_kernel", "fp8bs_blockscale_pair_kernel",
+                                       "fp8bs_mxfp8_sk_kernel", "fp8bs_tensorscale_sk_kernel"))
         if split and r.get("registers") != 168:
             raise RuntimeError(f"{sym}: {r.get('registers')} registers, the setmaxnreg split needs 168")
         if r.get("spill_stores", 0) or r.get("spill_loads", 0) or r.get("stack", 0):
@@ -113,5 +114,28 @@ def build(force: bool = False, verbose: bool = False) -> str:
     return LIB
 
 
+def resources_table(log_path: str) -> str:
+    """One line per kernel instance from a ptxas -v log: registers, stack, spills, static shared memory."""
+    import re
+    smem, cur = {}, None
+    with open(log_path) as f:
+        for line in f:
+            m = re.search(r"Compiling entry function '(\S+)'", line)
+            if m:
+                cur = m.group(1)
+            m = re.search(r"Used \d+ registers.*?(\d+) bytes smem", line)
+            if m and cur:
+                smem[cur] = int(m.group(1))
+    rows = ["registers  stack  spill_st  spill_ld  static_smem  kernel (mangled symbol)"]
+    for sym, r in sorted(parse_ptxas(log_path).items()):
+        rows.append(f"{r.get('registers', 0):9d}  {r.get('stack', 0):5d}  {r.get('spill_stores', 0):8d}  "
+                    f"{r.get('spill_loads', 0):8d}  {smem.get(sym, 0):11d}  {sym}")
+    return "\n".join(rows)
+
+
 if __name__ == "__main__":
-    print(build(force="--force" in sys.argv, verbose=True))
+    lib = build(force="--force" in sys.argv, verbose="--resources" not in sys.argv)
+    if "--resources" in sys.argv:
+        print(resources_table(os.path.join(BUILD, "ptxas.log")))
+    else:
+        print(lib)
