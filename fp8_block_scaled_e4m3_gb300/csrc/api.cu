@@ -45,8 +45,8 @@ __device__ int g_status_word;   // per-device status written by the kernels
 constexpr int kMaxDevices = 64;
 constexpr unsigned long long kDefaultWaitLimitNs = 2000000000ull;
 constexpr int kMxPairStages = 6;
-constexpr int kBsPairStages = 6;
-constexpr int kPairMinKBlocks = 12;   // K blocks per tile from which the blockscale pair kernel may be chosen
+constexpr int kBsPairStages = 4;
+constexpr int kPairMinM = 2048;       // rows from which the blockscale pair kernel is chosen
 
 struct DeviceState {
     bool ready = false;
@@ -322,37 +322,43 @@ Config choose_config_base(int kind, int M, int N, int K, int num_sms)
     return c;
 }
 
-// Blockscale GEMM with few K blocks per tile (K <= 1024): the three-stage
-// instance, whose freed shared memory gives the epilogue two 4 KiB buffers per
-// warp, so the C store of a tile overlaps less of the next tile's K loop.
-// Same-session times (us, L2 flushed, tile / stream-K schedule, 4 -> 3 stages):
-// 16384x7168x768 119.2 -> 109.0 / 123.9 -> 114.8; 16384x7168x1024 141.3 ->
-// 133.3; 16384x7168x1536 183.8 -> 180.3; 4096x65536x1536 398.5 -> 405.1;
-// 16384x7168x2048 225.4 -> 229.9; 4096x2048x7168 63.5 -> 71.7 (one producer
-// thread fills the odd-count ring, which deep K loops feel).
+// Blockscale GEMM with few K blocks per tile (K <= 1024), one-CTA kernel: the
+// three-stage instance, whose freed shared memory holds a whole C tile that a
+// warp of its own stores, so the C store of a tile overlaps the next tile's K
+// loop. Same-session times (us, L2 flushed, tile / stream-K schedule, 4 -> 3
+// stages, with two alternating 4 KiB C buffers per warp, which the tile buffer
+// matches within 0.5%): 16384x7168x768 119.2 -> 109.0 / 123.9 -> 114.8;
+// 16384x7168x1024 141.3 -> 133.3; 16384x7168x1536 183.8 -> 180.3;
+// 4096x65536x1536 398.5 -> 405.1; 16384x7168x2048 225.4 -> 229.9;
+// 4096x2048x7168 63.5 -> 71.7 (one producer thread fills the odd-count ring,
+// which deep K loops feel).
 constexpr int kWideCMaxKBlocks = 8;
+
+// The one-CTA kernels' rule: shape class -> configuration.
+Config choose_config_one_cta(int kind, int M, int N, int K, int num_sms)
+{
+    Config c = choose_config_base(kind, M, N, K, num_sms);
+    if (kind == 1 && c.block_n == 256 && K / 128 <= kWideCMaxKBlocks)
+        c.stages = 3;
+    return c;
+}
 
 // Shape class -> configuration, from (M, N, K) only.
 Config choose_config(int kind, int M, int N, int K, int num_sms)
 {
-    Config c = choose_config_base(kind, M, N, K, num_sms);
-    if (kind == 1 && c.block_n == 256 && K / 128 <= kWideCMaxKBlocks) {
-        c.stages = 3;
-    } else if (kind == 1 && c.block_n == 256 && c.sched == 1 && K / 128 >= kPairMinKBlocks) {
-        // One CTA per tile, at least four waves of 256 x 256 tiles over the CTA
-        // pairs and at least 12 K blocks per tile: the pair kernel (half of B
-        // per CTA, six stages, half the MMA instructions per SM). Same-session
-        // times (us, L2 flushed, one-CTA -> pair): 8192x8192x3072 184.7 ->
-        // 181.3, 16384x7168x2048 224.1 -> 221.7, 4096x65536x1536 397.0 ->
-        // 393.5; at fewer waves it gains nothing (4096x2048x7168 62.2 -> 61.6,
-        // 2048x2048x7168 34.8 -> 34.9), and with few K blocks its narrow C
-        // staging loses (16384x7168x768 112.9 with the three-stage instance,
-        // ~120 with four stages, 122.7 with the pair).
-        const long long pair_tiles = static_cast<long long>((M + 255) / 256) * ((N + 255) / 256);
-        if (num_sms >= 2 && pair_tiles >= 4ll * (num_sms / 2)) {
-            c.kind = 3;
-            c.stages = kBsPairStages;
-        }
+    Config c = choose_config_one_cta(kind, M, N, K, num_sms);
+    // Blockscale, one CTA per tile, M >= 2048: the CTA-pair kernel (256 x 256
+    // tiles, half of B per CTA, four stages and a whole-tile C buffer).
+    // Same-session times (us, L2 flushed; one-CTA kernel (three / four stages)
+    // -> pair): 16384x7168x768 107.8 / 121.4 -> 105.5; 16384x7168x1024 131.2 /
+    // 142.8 -> 125.7; 16384x7168x1536 176.8 / 185.4 -> 166.6; 16384x7168x2048
+    // 225.1 / 229.5 -> 206.5; 16384x7168x3072 318.3 / 316.0 -> 288.5;
+    // 8192x8192x3072 191.3 / 188.5 -> 173.9; 4096x65536x1536 396.0 / 405.3 ->
+    // 362.1; 4096x2048x7168 71.8 / 63.6 -> 61.8. Stream-K shapes keep the
+    // one-CTA kernel (16384x1536x7168: 149 with stream-K, 162.1 with the pair).
+    if (kind == 1 && c.block_n == 256 && c.sched == 1 && M >= kPairMinM) {
+        c.kind = 3;
+        c.stages = kBsPairStages;
     }
     return c;
 }
@@ -567,8 +573,12 @@ int blockscale_gemm(const void *A, const float *a_scale, const void *B, const fl
     if ((rc = ensure_device(dev, st)))
         return rc;
     Config cfg = choose_config(1, M, N, K, st->num_sms);
-    if (c_e4m3 && cfg.kind == 3)
-        cfg = choose_config_base(1, M, N, K, st->num_sms);   // the E4M3 store is the one-CTA kernel's
+    // The E4M3 store is the one-CTA kernel's four-stage instance (stages 2 KiB
+    // E4M3 chunks per warp; the whole-tile bf16 buffer of the three-stage
+    // instance does not apply): 16384x7168x768 103.4 us there, 116.8 with
+    // three stages.
+    if (c_e4m3)
+        cfg = choose_config_base(1, M, N, K, st->num_sms);
     if (!override_config(1, 3, cfg))
         return FP8BS_ERR_SHAPE;
     const bool pair = cfg.kind == 3;   // CTA-pair kernel: 256 x 256 tiles, half of the B tile per CTA
@@ -576,7 +586,8 @@ int blockscale_gemm(const void *A, const float *a_scale, const void *B, const fl
         return FP8BS_ERR_SHAPE;         // forced by the override
     const int KB = K / 128;
     const uint64_t ld_sa = static_cast<uint64_t>(fp8bs_a_scale_ld(M));
-    const bool wide_c = cfg.block_n == 256 && cfg.stages == 3;   // 32 x 64 bf16 C boxes, 128-byte swizzle
+    // whole-tile C buffer (one-CTA three stages, and the pair kernel): 128 x 64 bf16 C boxes, 128-byte swizzle
+    const bool tile_c = cfg.block_n == 256 && (pair || cfg.stages == 3);
     CUtensorMap tmA, tmB, tmSA, tmC;
     if (!encode_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, A, K, M, K, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
         !encode_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, B, K, N, K, 128, pair ? cfg.block_n / 2 : cfg.block_n,
@@ -586,8 +597,8 @@ int blockscale_gemm(const void *A, const float *a_scale, const void *B, const fl
         !(c_e4m3 ? encode_2d(&tmC, CU_TENSOR_MAP_DATA_TYPE_UINT8, C, N, M, static_cast<uint64_t>(N), 64, 32,
                              CU_TENSOR_MAP_SWIZZLE_64B)
                  : encode_2d(&tmC, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, C, N, M, static_cast<uint64_t>(N) * 2,
-                             wide_c ? 64 : kCChunkCols, 32,
-                             wide_c ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B)))
+                             tile_c ? 64 : kCChunkCols, tile_c ? 128 : 32,
+                             tile_c ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B)))
         return FP8BS_ERR_LAUNCH;
     GemmArgs args = {};
     args.M = M;

@@ -11,9 +11,9 @@
 // own shared memory, exchanges the B halves and writes each CTA's 128 x 256
 // partial P_kb into that CTA's tensor memory (two 256-column buffers per CTA,
 // as in the one-CTA kernel). Against the one-CTA kernel on 128 x 256 tiles:
-//   - a CTA's stage is A 16 KiB + half of B 16 KiB, so six stages fit where
-//     the one-CTA kernel has four, and the shared-memory fill per K block
-//     (the L2 -> SM stream) drops from 48 to 32 KiB per SM;
+//   - a CTA's stage is A 16 KiB + half of B 16 KiB, so four stages take 128
+//     KiB where the one-CTA kernel's take 192, and the shared-memory fill per
+//     K block (the L2 -> SM stream) drops from 48 to 32 KiB per SM;
 //   - one MMA instruction does two SMs' work, so each SM issues half as many
 //     (issuing holds up the promote warps of the issuer's sub-partition).
 // The promote (fp32 FMAs on TMEM loads) and the epilogue are the one-CTA
@@ -35,6 +35,14 @@
 //               a buffer is released on the even CTA's tempty barrier (16
 //               arrivals, 8 warps of each CTA; the odd CTA's are relaxed remote
 //               arrives).
+//   - the shared memory left over holds this CTA's whole 128 x 256 bf16 C
+//     tile (64 KiB): every promote warp converts its rows into it and goes on
+//     to the next tile, and warps 4..7 each store one 64-column x 128-row chunk
+//     by TMA once all eight have written (c_full), releasing the buffer
+//     (c_empty) when their store has read it, at the next tile's epilogue. The
+//     C store of a tile thus overlaps the next tile's K loop instead of
+//     holding the MMAs at the tile boundary (the one-CTA four-stage kernel
+//     stages C in 2 KiB chunks per warp and has no room for this).
 // One CTA pair per tile (no stream-K); E4M3 C runs on the one-CTA kernel.
 #include "common.cuh"
 
@@ -59,9 +67,10 @@ struct Bs2Layout {
     static constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
     static constexpr int OFF_SA = OFF_B + STAGES * B_BYTES;
     static constexpr int OFF_C = (OFF_SA + kBs2SaSlots * SA_BYTES + 1023) / 1024 * 1024;
-    static constexpr int OFF_BAR = OFF_C + kEpiWarps * kCStageBytes;
+    static constexpr int C_AREA = kBlockM * kBs2BN * 2;   // the whole-tile C buffer (bf16)
+    static constexpr int OFF_BAR = OFF_C + C_AREA;
     // full[S], empty[S], tfull[NBUF], tempty[NBUF], mma_done, sa_full[SA], sa_empty[SA]
-    static constexpr int NBAR = 2 * STAGES + 2 * kBs2NBuf + 1 + 2 * kBs2SaSlots;
+    static constexpr int NBAR = 2 * STAGES + 2 * kBs2NBuf + 1 + 2 * kBs2SaSlots + 2;   // + c_full, c_empty
     static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
     static constexpr int BYTES = OFF_MISC + 16;
     static constexpr int DYN_SMEM = BYTES + 1024;
@@ -103,6 +112,8 @@ __global__ void __launch_bounds__(kBs2Threads, 1)
     auto sa_empty_bar = [&](int a) {
         return sbase + L::OFF_BAR + 8u * (2 * STAGES + 2 * kBs2NBuf + 1 + kBs2SaSlots + a);
     };
+    const uint32_t c_full_bar = sbase + L::OFF_BAR + 8u * (2 * STAGES + 2 * kBs2NBuf + 1 + 2 * kBs2SaSlots);
+    const uint32_t c_empty_bar = c_full_bar + 8u;
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + L::OFF_MISC);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::OFF_MISC + 4);
 
@@ -116,6 +127,8 @@ __global__ void __launch_bounds__(kBs2Threads, 1)
             ptx::mbar_init(tempty_bar(b), 2 * kEpiWarps);   // promote warps of both CTAs (even CTA's copy)
         }
         ptx::mbar_init(mma_done_bar, 2);                    // both issuers' multicast commits
+        ptx::mbar_init(c_full_bar, kEpiWarps);              // tile C buffer written
+        ptx::mbar_init(c_empty_bar, kBlockM * kBs2BN * 2 / (kBlockM * 128));   // its chunk stores have read it
         for (int a = 0; a < kBs2SaSlots; ++a) {
             ptx::mbar_init(sa_full_bar(a), 1);
             ptx::mbar_init(sa_empty_bar(a), kEpiWarps);     // this CTA's promote warps
@@ -227,7 +240,7 @@ __global__ void __launch_bounds__(kBs2Threads, 1)
         const int q = warp & 3;                      // TMEM lane quadrant this warp may access
         const int row = q * 32 + lane;               // row of this CTA's 128
         const int NB = (args.N + 127) / 128;
-        const uint32_t cstage = sbase + L::OFF_C + ew * kCStageBytes;
+        int n_stored = 0;   // tiles written to the tile C buffer
 
         float acc[HALF];
         int it = 0;
@@ -298,11 +311,39 @@ __global__ void __launch_bounds__(kBs2Threads, 1)
                 break;
             int mb, nb;
             args.raster.coords(t, mb, nb);
-            const int x0 = nb * kBs2BN + wg * HALF;
-            const int y0 = mb * 2 * kBlockM + static_cast<int>(rank) * kBlockM + q * 32;
+            constexpr int NCHUNK = kBs2BN / 64;      // 64-column chunks of the tile, one per storing warp
+            // The previous tile's chunk stores must have read the buffer.
+            if (n_stored > 0) {
+                if (ew < NCHUNK && lane == 0) {
+                    ptx::bulk_wait_read_all();
+                    ptx::mbar_arrive(c_empty_bar);
+                }
+                if (!wait_bounded_warp(c_empty_bar, (n_stored - 1) & 1, abort_flag, args)) {
+                    ok = false;
+                    break;
+                }
+            }
 #pragma unroll
-            for (int c = 0; c < HALF / kCChunkCols; ++c)
-                store_c_chunk(&tmC, cstage, lane, acc + c * kCChunkCols, x0 + c * kCChunkCols, y0, args.M, args.N);
+            for (int c = 0; c < HALF / 64; ++c)
+                stage_c64_row(sbase + L::OFF_C + (wg * (HALF / 64) + c) * (kBlockM * 128), row, acc + c * 64);
+            ptx::fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0)
+                ptx::mbar_arrive(c_full_bar);
+            if (ew < NCHUNK) {
+                if (!wait_bounded_warp(c_full_bar, n_stored & 1, abort_flag, args)) {
+                    ok = false;
+                    break;
+                }
+                const int x = nb * kBs2BN + ew * 64;
+                const int y = mb * 2 * kBlockM + static_cast<int>(rank) * kBlockM;
+                if (lane == 0) {
+                    if (x < args.N && y < args.M)
+                        ptx::tma_store_2d(&tmC, sbase + L::OFF_C + ew * (kBlockM * 128), x, y);
+                    ptx::bulk_commit();
+                }
+            }
+            ++n_stored;
         }
         if (lane == 0)
             ptx::bulk_wait_all();
@@ -366,9 +407,9 @@ cudaError_t max_bs_pair_clusters(int *out)
     return cudaOccupancyMaxActiveClusters(out, kern, &cfg);
 }
 
-template cudaError_t launch_blockscale_pair<6>(const CUtensorMap &, const CUtensorMap &,
+template cudaError_t launch_blockscale_pair<4>(const CUtensorMap &, const CUtensorMap &,
                                                            const CUtensorMap &, const CUtensorMap &, const GemmArgs &,
                                                            int, cudaStream_t);
-template cudaError_t max_bs_pair_clusters<6>(int *);
+template cudaError_t max_bs_pair_clusters<4>(int *);
 
 } // namespace fp8bs

@@ -42,9 +42,14 @@
 //               the MMA's critical path; for BN = 256 the buffer is released
 //               after the last 64-column round.
 //               After the last K block: bf16 convert, 64-byte-swizzled staging
-//               of 32 x 32 chunks, TMA store (tails clipped by the tensor map);
-//               with three stages (shapes with few K blocks per tile) 32 x 64
-//               chunks through two alternating 4 KiB buffers per warp.
+//               of 32 x 32 chunks, TMA store (tails clipped by the tensor map).
+//               With three stages (shapes with few K blocks per tile) the freed
+//               shared memory holds a whole 128 x 256 bf16 C tile: the promote
+//               warps convert their rows into it and go straight on to the next
+//               tile, and warp 3 (idle with one producer) stores it by TMA.
+//   warp 3 (three stages) C store: waits for the eight promote warps to fill
+//               the tile buffer, issues four 64-column x 128-row TMA stores,
+//               waits for them to read the buffer, releases it.
 // Registers: the launch gives 168 per thread (3 warps per SM sub-partition);
 // warpgroup 0 drops to 40 and the two promote warpgroups rise to 232, so one
 // sub-partition holds 40 + 232 + 232 = 504 <= 512 registers per lane and the
@@ -63,11 +68,13 @@ constexpr int kSaSlots = 16;   // a_scale ring depth (>= STAGES + NBUF, so it ne
 
 template <int BN, int STAGES>
 struct BsLayout {
-    // Three stages leave room for wider C staging: two 4 KiB buffers per
-    // epilogue warp (64-column chunks, alternating), for shapes with few K
-    // blocks per tile, where the epilogue is a large part of each tile.
-    static constexpr bool WIDE_C = STAGES == 3;
-    static constexpr int C_BYTES = WIDE_C ? 2 * 4096 : kCStageBytes;   // per epilogue warp
+    // Three stages leave room for a whole C tile (128 x 256 bf16, 64 KiB, four
+    // 128-byte-swizzled 64-column chunks), stored by a warp of its own, for
+    // shapes with few K blocks per tile, where the epilogue is a large part
+    // of each tile. (An E4M3 C keeps the per-warp 2 KiB staging, inside it.)
+    static constexpr bool TILE_C = STAGES == 3;
+    static constexpr int C_BYTES = kCStageBytes;    // per epilogue warp (per-warp staging)
+    static constexpr int C_AREA = TILE_C ? kBlockM * BN * 2 : kEpiWarps * C_BYTES;
     static constexpr int A_BYTES = kBlockM * kBlockK;
     static constexpr int B_BYTES = BN * kBlockK;
     static constexpr int SA_BYTES = kBlockM * 4;
@@ -75,12 +82,14 @@ struct BsLayout {
     static constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
     static constexpr int OFF_SA = OFF_B + STAGES * B_BYTES;
     static constexpr int OFF_C = (OFF_SA + kSaSlots * SA_BYTES + 1023) / 1024 * 1024;
-    static constexpr int OFF_BAR = OFF_C + kEpiWarps * C_BYTES;
+    static constexpr int OFF_BAR = OFF_C + C_AREA;
     static constexpr int NBUF = 512 / BN;        // TMEM partial buffers
     static_assert(NBUF % 2 == 0, "two MMA issuers split the buffers by parity");
     static_assert(STAGES % 2 == 1 || kSaSlots % 2 == 0, "two producers split the a_scale slots by parity");
-    // full[S], empty[S], tfull[NBUF], tempty[NBUF], mma_done, sa_full[kSaSlots], sa_empty[kSaSlots]
-    static constexpr int NBAR = 2 * STAGES + 2 * NBUF + 1 + 2 * kSaSlots;
+    // full[S], empty[S], tfull[NBUF], tempty[NBUF], mma_done, sa_full[kSaSlots], sa_empty[kSaSlots],
+    // c_full, c_empty
+    static constexpr int NBAR = 2 * STAGES + 2 * NBUF + 1 + 2 * kSaSlots + 2;
+    static_assert(!TILE_C || (BN == 256 && C_AREA >= kEpiWarps * C_BYTES), "tile C buffer");
     static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
     static constexpr int BYTES = OFF_MISC + 16;
     static constexpr int DYN_SMEM = BYTES + 1024;   // slack to align the base to 1024
@@ -116,6 +125,8 @@ __global__ void __launch_bounds__(kBsThreads, 1)
     const uint32_t mma_done_bar = sbase + L::OFF_BAR + 8u * (2 * STAGES + 2 * NT);
     auto sa_full_bar = [&](int a) { return sbase + L::OFF_BAR + 8u * (2 * STAGES + 2 * NT + 1 + a); };
     auto sa_empty_bar = [&](int a) { return sbase + L::OFF_BAR + 8u * (2 * STAGES + 2 * NT + 1 + kSaSlots + a); };
+    const uint32_t c_full_bar = sbase + L::OFF_BAR + 8u * (2 * STAGES + 2 * NT + 1 + 2 * kSaSlots);
+    const uint32_t c_empty_bar = c_full_bar + 8u;
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + L::OFF_MISC);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::OFF_MISC + 4);
 
@@ -133,6 +144,8 @@ __global__ void __launch_bounds__(kBsThreads, 1)
             ptx::mbar_init(tempty_bar(b), kEpiWarps);     // every promote warp has loaded its slice
         }
         ptx::mbar_init(mma_done_bar, 2);                  // both MMA issuers
+        ptx::mbar_init(c_full_bar, kEpiWarps);            // tile C buffer filled (three stages)
+        ptx::mbar_init(c_empty_bar, 1);                   // tile C buffer read by its TMA stores
         *abort_flag = 0;
         ptx::fence_mbar_init();
     }
@@ -253,6 +266,37 @@ __global__ void __launch_bounds__(kBsThreads, 1)
             ptx::tc_commit(mma_done_bar);
             wait_teardown(mma_done_bar, 0, args);
         }
+    } else if (L::TILE_C && warp == 3 && !args.c_e4m3) {
+        // ---------------------------------------------- C store (three stages)
+        // The tiles this CTA stores are its segments that start at K block 0
+        // (whole tiles, and under stream-K the tiles it finishes), in the
+        // promote warps' order.
+        if (lane == 0) {
+            WorkSpan span;
+            span.init(args, KB, tiles);
+            int n_stored = 0;
+            for (int it = 0; it < span.total;) {
+                int t, kb0;
+                span.step(it, t, kb0);
+                it += (KB - kb0) < (span.total - it) ? (KB - kb0) : (span.total - it);
+                if (kb0 != 0)
+                    continue;
+                if (!wait_bounded(c_full_bar, n_stored & 1, abort_flag, args))
+                    break;
+                const TileGeo geo = tile_geo<MOE>(args, t, BN, n_leaders);
+#pragma unroll
+                for (int c = 0; c < BN / 64; ++c) {
+                    const int x = geo.nb * BN + c * 64;
+                    if (x < args.N && geo.a_row < args.M)
+                        ptx::tma_store_2d(&tmC, sbase + L::OFF_C + c * (kBlockM * 128), x, geo.a_row);
+                }
+                ptx::bulk_commit();
+                ptx::bulk_wait_read_all();
+                ptx::mbar_arrive(c_empty_bar);
+                ++n_stored;
+            }
+            ptx::bulk_wait_all();
+        }
     }
     } else {
         ptx::setmaxnreg_inc<kBsRegsHigh<BN>>();
@@ -269,7 +313,7 @@ __global__ void __launch_bounds__(kBsThreads, 1)
         const int row = q * 32 + lane;               // row of the tile
         const int NB = (args.N + 127) / 128;
         const uint32_t cstage = sbase + L::OFF_C + ew * L::C_BYTES;
-        int cbuf = 0;   // wide staging: which of the warp's two 4 KiB buffers the next chunk uses
+        int n_stored = 0;   // tiles handed to the C store warp (three stages)
         WorkSpan span;
         span.init(args, KB, tiles);
         const int total = span.total;
@@ -444,13 +488,21 @@ __global__ void __launch_bounds__(kBsThreads, 1)
 #pragma unroll
                 for (int c = 0; c < HALF / 64; ++c)
                     store_c8_chunk(&tmC, cstage, lane, acc + c * 64, args.c_scale, x0 + c * 64, y0, args.M, args.N);
-            } else if constexpr (L::WIDE_C) {
-#pragma unroll
-                for (int c = 0; c < HALF / 64; ++c) {
-                    store_c64_chunk(&tmC, cstage + 4096u * (cbuf & 1), lane, acc + c * 64, x0 + c * 64, y0, args.M,
-                                    args.N);
-                    ++cbuf;
+            } else if constexpr (L::TILE_C) {
+                // Into the tile buffer once its previous tile has been read out,
+                // then on to the next tile; the store warp writes C.
+                if (!wait_bounded_warp(c_empty_bar, (n_stored & 1) ^ 1, abort_flag, args)) {
+                    ok = false;
+                    break;
                 }
+#pragma unroll
+                for (int c = 0; c < HALF / 64; ++c)
+                    stage_c64_row(sbase + L::OFF_C + (wg * (HALF / 64) + c) * (kBlockM * 128), row, acc + c * 64);
+                ptx::fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0)
+                    ptx::mbar_arrive(c_full_bar);
+                ++n_stored;
             } else {
 #pragma unroll
                 for (int c = 0; c < HALF / kCChunkCols; ++c)

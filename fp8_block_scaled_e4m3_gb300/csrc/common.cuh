@@ -313,33 +313,21 @@ __device__ __forceinline__ void store_c_chunk(const CUtensorMap *tmC, uint32_t s
     }
 }
 
-// Store one epilogue warp's 32 rows x 64 columns of C (row = lane) with one TMA
-// store of a 4 KiB box, from one of the warp's two staging buffers (`buf`, a
-// 1024-byte aligned shared address; consecutive chunks alternate buffers). The
-// rows are 128 bytes with the 128-byte swizzle: 16-byte unit j of row r sits at
-// unit j ^ (r & 7). A chunk waits only for the store issued two chunks before
-// (the previous use of its buffer) to have read it, so the conversion and
-// staging of one chunk overlap the store of the previous one.
-__device__ __forceinline__ void store_c64_chunk(const CUtensorMap *tmC, uint32_t buf, int lane, const float *v, int x,
-                                                int y, int M, int N)
+// Write one thread's 64 consecutive C columns (bf16) of tile row `row` (0..127)
+// into a 128-row x 64-column chunk of a C tile in shared memory (`chunk`,
+// 1024-byte aligned). Rows are 128 bytes with the 128-byte swizzle (16-byte
+// unit j of row r at unit j ^ (r & 7)): the image one TMA store of a 64 x 128
+// box reads. A warp's 32 rows write 8 distinct units per row group of 8, so
+// each store instruction takes the minimum four shared-memory wavefronts.
+__device__ __forceinline__ void stage_c64_row(uint32_t chunk, int row, const float *v)
 {
-    if (lane == 0)
-        ptx::bulk_wait_read_le1();
-    __syncwarp();
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
         const uint32_t w0 = ptx::pack_bf16x2(v[j * 8 + 0], v[j * 8 + 1]);
         const uint32_t w1 = ptx::pack_bf16x2(v[j * 8 + 2], v[j * 8 + 3]);
         const uint32_t w2 = ptx::pack_bf16x2(v[j * 8 + 4], v[j * 8 + 5]);
         const uint32_t w3 = ptx::pack_bf16x2(v[j * 8 + 6], v[j * 8 + 7]);
-        ptx::st_shared_v4(buf + lane * 128 + ((j ^ (lane & 7)) * 16), w0, w1, w2, w3);
-    }
-    ptx::fence_proxy_async_smem();
-    __syncwarp();
-    if (lane == 0) {
-        if (x < N && y < M)
-            ptx::tma_store_2d(tmC, buf, x, y);
-        ptx::bulk_commit();
+        ptx::st_shared_v4(chunk + row * 128 + ((j ^ (row & 7)) * 16), w0, w1, w2, w3);
     }
 }
 

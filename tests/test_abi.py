@@ -133,19 +133,20 @@ def test_config_selection(lib):
     # wide tiles for the large shapes, the narrow tile when a wide grid would starve the SMs
     # blockscale: wide one-CTA tiles for the large shape classes, the narrow tile
     # when a wide grid would starve the SMs
-    for M, N, K in [(4096, 2048, 7168), (16384, 1536, 7168), (2048, 2048, 7168)]:
+    # one CTA per tile from M = 2048: the CTA-pair kernel (256 x 256 tiles, four
+    # stages, whole-tile C buffer), K-light shapes included
+    for M, N, K in [(4096, 2048, 7168), (2048, 2048, 7168), (4096, 65536, 1536), (8192, 8192, 3072),
+                    (16384, 7168, 2048), (16384, 7168, 768), (16384, 7168, 1152), (4096, 4096, 512)]:
         c = lib.decode_config(lib.select_config("bs", M, N, K, 152))
-        assert c["kind"] == "blockscale" and c["block_n"] == 256 and c["stages"] == 4
-    # one CTA per tile and at least four waves of 256 x 256 tiles: the CTA-pair kernel
-    # (and at least 12 K blocks per tile)
-    for M, N, K in [(4096, 65536, 1536), (8192, 8192, 3072), (16384, 7168, 2048)]:
+        assert c["kind"] == "blockscale_pair" and c["block_n"] == 256 and c["stages"] == 4, (M, N, K, c)
+    # stream-K shapes keep the one-CTA kernel
+    for M, N, K in [(16384, 1536, 7168), (1024, 2048, 7168)]:
         c = lib.decode_config(lib.select_config("bs", M, N, K, 152))
-        assert c["kind"] == "blockscale_pair" and c["block_n"] == 256 and c["stages"] == 6, (M, N, K, c)
-    # few K blocks per tile (K <= 1024): the three-stage instance with the wider C staging
-    for M, N, K in [(16384, 7168, 768), (16384, 7168, 1024), (4096, 4096, 512)]:
+        assert c["kind"] == "blockscale" and c["stages"] == 4 and c["schedule"] == "stream_k", (M, N, K, c)
+    # below M = 2048 with few K blocks per tile (K <= 1024): the one-CTA three-stage instance
+    for M, N, K in [(1024, 7168, 768), (1024, 4096, 512)]:
         c = lib.decode_config(lib.select_config("bs", M, N, K, 152))
         assert c["kind"] == "blockscale" and c["block_n"] == 256 and c["stages"] == 3, (M, N, K, c)
-    assert lib.decode_config(lib.select_config("bs", 16384, 7168, 1152, 152))["stages"] == 4
     assert lib.decode_config(lib.select_config("mx", 16384, 7168, 768, 152))["stages"] != 3
     assert lib.decode_config(lib.select_config("bs", 256, 512, 512, 152))["block_n"] == 128
     # mxfp8: wide tiles, the narrow tile when the wide grid would starve the SMs
@@ -165,9 +166,9 @@ def test_config_selection(lib):
     assert L.fp8bs_set_config_override(1160511) == -3      # the 160-wide tile was removed
     assert L.fp8bs_set_config_override(2128612) == 0       # the MXFP8 kernel's 128-wide tile has stream-K too
     assert L.fp8bs_set_config_override(4128612) == -3
-    assert L.fp8bs_set_config_override(3256611) == 0       # the blockscale CTA-pair kernel: 256 x 256, six stages
-    assert lib.decode_config(3256611)["kind"] == "blockscale_pair"
-    for bad in (3128811, 3256411, 3256612):                # no other tile, stage count or schedule
+    assert L.fp8bs_set_config_override(3256411) == 0       # the blockscale CTA-pair kernel: 256 x 256, four stages
+    assert lib.decode_config(3256411)["kind"] == "blockscale_pair"
+    for bad in (3128811, 3256611, 3256311, 3256412):       # no other tile, stage count or schedule
         assert L.fp8bs_set_config_override(bad) == -3
     assert L.fp8bs_set_config_override(1256413) == -3      # no such schedule
     assert L.fp8bs_set_config_override(1128612) == -3      # stream-K runs with the 256-wide tile only
