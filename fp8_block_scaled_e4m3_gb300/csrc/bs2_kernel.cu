@@ -20,12 +20,12 @@
 // kernel's, per CTA.
 //
 // Per CTA, 12 warps (3 warpgroups):
-//   warps 0, 3  TMA producers for the even and the odd K-block steps: own A
-//               rows and own B half into stage s; both CTAs' bytes complete on
-//               the even CTA's full[s], which the even CTA's producer arms with
-//               the pair's total (an odd-CTA copy may land first: the phase
-//               cannot complete before that arrive). The a_scale slice [128] of
-//               the CTA's own rows goes to a local ring.
+//   warp 0      TMA producer: own A rows and own B half into stage s; both
+//               CTAs' bytes complete on the even CTA's full[s], which the even
+//               CTA's producer arms with the pair's total (an odd-CTA copy may
+//               land first: the phase cannot complete before that arrive). The
+//               a_scale slice [128] of the CTA's own rows goes to a local ring.
+//   warp 3      C store: four TMA stores per tile from the whole-tile buffer.
 //   warps 1, 2  pair TMEM allocation (warp 1) and, in the even CTA only, the MMA
 //               issuers of the even and the odd steps (one thread each; each
 //               owns one TMEM buffer and every other stage); tcgen05.commit
@@ -36,12 +36,12 @@
 //               arrivals, 8 warps of each CTA; the odd CTA's are relaxed remote
 //               arrives).
 //   - the shared memory left over holds this CTA's whole 128 x 256 bf16 C
-//     tile (64 KiB): every promote warp converts its rows into it and goes on
-//     to the next tile, and warps 4..7 each store one 64-column x 128-row chunk
-//     by TMA once all eight have written (c_full), releasing the buffer
-//     (c_empty) when their store has read it, at the next tile's epilogue. The
-//     C store of a tile thus overlaps the next tile's K loop instead of
-//     holding the MMAs at the tile boundary (the one-CTA four-stage kernel
+//     tile (64 KiB): every promote warp converts its rows into it, arrives
+//     (c_full) and goes on to the next tile; warp 3 stores the tile by four TMA
+//     stores of 64 columns x 128 rows and releases the buffer (c_empty) as
+//     soon as they have read it. The C store of a tile thus overlaps the next
+//     tile's K loop, and the promote warps wait on nothing at a tile boundary
+//     but a buffer that was freed long before (the one-CTA four-stage kernel
 //     stages C in 2 KiB chunks per warp and has no room for this).
 // One CTA pair per tile (no stream-K); E4M3 C runs on the one-CTA kernel.
 #include "common.cuh"
@@ -128,7 +128,7 @@ __global__ void __launch_bounds__(kBs2Threads, 1)
         }
         ptx::mbar_init(mma_done_bar, 2);                    // both issuers' multicast commits
         ptx::mbar_init(c_full_bar, kEpiWarps);              // tile C buffer written
-        ptx::mbar_init(c_empty_bar, kBlockM * kBs2BN * 2 / (kBlockM * 128));   // its chunk stores have read it
+        ptx::mbar_init(c_empty_bar, 1);                     // the store warp's TMA stores have read it
         for (int a = 0; a < kBs2SaSlots; ++a) {
             ptx::mbar_init(sa_full_bar(a), 1);
             ptx::mbar_init(sa_empty_bar(a), kEpiWarps);     // this CTA's promote warps
@@ -147,13 +147,11 @@ __global__ void __launch_bounds__(kBs2Threads, 1)
 
     if (warp < 4) {
         ptx::setmaxnreg_dec<kBs2RegsLow>();
-        if (warp == 0 || warp == 3) {
-            // ----------------------------------------------------------- producers
-            // Warp 0 fills the stages and a_scale slots of the even steps, warp 3
-            // those of the odd steps: with even STAGES and slot counts each stage
-            // and slot has one producer thread, which waits on it phase by phase.
+        if (warp == 0) {
+            // ------------------------------------------------------------ producer
+            // One thread fills every stage and a_scale slot, waiting on each
+            // phase by phase (three copies per K block of 32 KiB).
             if (lane == 0) {
-                const int par = warp == 3 ? 1 : 0;
                 ptx::prefetch_tmap(&tmA);
                 ptx::prefetch_tmap(&tmB);
                 ptx::prefetch_tmap(&tmSA);
@@ -165,8 +163,6 @@ __global__ void __launch_bounds__(kBs2Threads, 1)
                     const int row0 = mb * 2 * kBlockM + static_cast<int>(rank) * kBlockM;
                     const int brow0 = nb * kBs2BN + static_cast<int>(rank) * (kBs2BN / 2);
                     for (int kb = 0; kb < KB; ++kb, ++it) {
-                        if ((it & 1) != par)
-                            continue;
                         const int s = it % STAGES;
                         const uint32_t ph = (it / STAGES) & 1;
                         const int a = it % kBs2SaSlots;
@@ -191,18 +187,18 @@ __global__ void __launch_bounds__(kBs2Threads, 1)
                 // exits: the last use of each of its stages and slots (earlier
                 // uses landed before they could be refilled). The odd CTA learns
                 // it from the even CTA's multicast stage release.
-                for (int s = par; s < STAGES; s += 2) {
+                for (int s = 0; s < STAGES; ++s) {
                     const int uses = it > s ? (it - s + STAGES - 1) / STAGES : 0;
                     if (uses > 0)
                         wait_teardown(rank == 0 ? full_bar(s) : empty_bar(s), (uses - 1) & 1, args);
                 }
-                for (int a = par; a < kBs2SaSlots; a += 2) {
+                for (int a = 0; a < kBs2SaSlots; ++a) {
                     const int uses = it > a ? (it - a + kBs2SaSlots - 1) / kBs2SaSlots : 0;
                     if (uses > 0)
                         wait_teardown(sa_full_bar(a), (uses - 1) & 1, args);
                 }
             }
-        } else if (lane == 0 && rank == 0) {
+        } else if ((warp == 1 || warp == 2) && lane == 0 && rank == 0) {
             // ------------------------------------------------ MMA issuers (even CTA)
             // Warp 1 issues the even steps (TMEM buffer 0, even stages), warp 2
             // the odd steps (buffer 1, odd stages).
@@ -227,6 +223,29 @@ __global__ void __launch_bounds__(kBs2Threads, 1)
                 ptx::tc_commit_pair_mc(empty_bar(s), 0x3);
             }
             ptx::tc_commit_pair_mc(mma_done_bar, 0x3);
+        }
+        if (warp == 3 && lane == 0) {
+            // -------------------------------------------------------- C store
+            // Once the eight promote warps have written a tile into the buffer
+            // (c_full), four TMA stores of 64 columns x 128 rows; the buffer is
+            // released (c_empty) as soon as they have read it.
+            for (int t = cluster, n = 0; t < num_tiles; t += num_clusters, ++n) {
+                if (!wait_bounded(c_full_bar, n & 1, abort_flag, args))
+                    break;
+                int mb, nb;
+                args.raster.coords(t, mb, nb);
+                const int y = mb * 2 * kBlockM + static_cast<int>(rank) * kBlockM;
+#pragma unroll
+                for (int c = 0; c < kBs2BN / 64; ++c) {
+                    const int x = nb * kBs2BN + c * 64;
+                    if (x < args.N && y < args.M)
+                        ptx::tma_store_2d(&tmC, sbase + L::OFF_C + c * (kBlockM * 128), x, y);
+                }
+                ptx::bulk_commit();
+                ptx::bulk_wait_read_all();
+                ptx::mbar_arrive(c_empty_bar);
+            }
+            ptx::bulk_wait_all();
         }
         // No pair MMA may still write this CTA's tensor memory when it is freed.
         if (warp == 1 && lane == 0)
@@ -258,9 +277,6 @@ __global__ void __launch_bounds__(kBs2Threads, 1)
             }
             float sb_cur = sbrow && lane < KB ? ptx::ldg_nc_f32(sbrow + lane) : 0.f;
             float sb_next = sbrow && 32 + lane < KB ? ptx::ldg_nc_f32(sbrow + 32 + lane) : 0.f;
-#pragma unroll
-            for (int j = 0; j < HALF; ++j)
-                acc[j] = 0.f;
             for (int kb = 0; kb < KB; ++kb, ++it) {
                 const float sb = __shfl_sync(0xffffffffu, sb_cur, kb & 31);
                 if ((kb & 31) == 31) {
@@ -282,7 +298,8 @@ __global__ void __launch_bounds__(kBs2Threads, 1)
                 const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                                        static_cast<uint32_t>(buf * kBs2BN + wg * HALF);
                 // Two 64-column rounds; the buffer is released once the second
-                // round is loaded.
+                // round is loaded. The tile's first K block sets the
+                // accumulators (an FMA onto zero, no separate reset).
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
                     uint32_t r0[32], r1[32];
@@ -299,29 +316,30 @@ __global__ void __launch_bounds__(kBs2Threads, 1)
                             ptx::mbar_arrive(sa_empty_bar(a));
                         }
                     }
+                    if (kb == 0) {
 #pragma unroll
-                    for (int j = 0; j < 32; ++j)
-                        acc[h * 64 + j] = fmaf(__uint_as_float(r0[j]), scale, acc[h * 64 + j]);
+                        for (int j = 0; j < 32; ++j)
+                            acc[h * 64 + j] = fmaf(__uint_as_float(r0[j]), scale, 0.f);
 #pragma unroll
-                    for (int j = 0; j < 32; ++j)
-                        acc[h * 64 + 32 + j] = fmaf(__uint_as_float(r1[j]), scale, acc[h * 64 + 32 + j]);
+                        for (int j = 0; j < 32; ++j)
+                            acc[h * 64 + 32 + j] = fmaf(__uint_as_float(r1[j]), scale, 0.f);
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j)
+                            acc[h * 64 + j] = fmaf(__uint_as_float(r0[j]), scale, acc[h * 64 + j]);
+#pragma unroll
+                        for (int j = 0; j < 32; ++j)
+                            acc[h * 64 + 32 + j] = fmaf(__uint_as_float(r1[j]), scale, acc[h * 64 + 32 + j]);
+                    }
                 }
             }
             if (!ok)
                 break;
-            int mb, nb;
-            args.raster.coords(t, mb, nb);
-            constexpr int NCHUNK = kBs2BN / 64;      // 64-column chunks of the tile, one per storing warp
-            // The previous tile's chunk stores must have read the buffer.
-            if (n_stored > 0) {
-                if (ew < NCHUNK && lane == 0) {
-                    ptx::bulk_wait_read_all();
-                    ptx::mbar_arrive(c_empty_bar);
-                }
-                if (!wait_bounded_warp(c_empty_bar, (n_stored - 1) & 1, abort_flag, args)) {
-                    ok = false;
-                    break;
-                }
+            // Into the tile buffer once the store warp has read out the previous
+            // tile, then on to the next tile.
+            if (!wait_bounded_warp(c_empty_bar, (n_stored & 1) ^ 1, abort_flag, args)) {
+                ok = false;
+                break;
             }
 #pragma unroll
             for (int c = 0; c < HALF / 64; ++c)
@@ -330,23 +348,8 @@ __global__ void __launch_bounds__(kBs2Threads, 1)
             __syncwarp();
             if (lane == 0)
                 ptx::mbar_arrive(c_full_bar);
-            if (ew < NCHUNK) {
-                if (!wait_bounded_warp(c_full_bar, n_stored & 1, abort_flag, args)) {
-                    ok = false;
-                    break;
-                }
-                const int x = nb * kBs2BN + ew * 64;
-                const int y = mb * 2 * kBlockM + static_cast<int>(rank) * kBlockM;
-                if (lane == 0) {
-                    if (x < args.N && y < args.M)
-                        ptx::tma_store_2d(&tmC, sbase + L::OFF_C + ew * (kBlockM * 128), x, y);
-                    ptx::bulk_commit();
-                }
-            }
             ++n_stored;
         }
-        if (lane == 0)
-            ptx::bulk_wait_all();
     }
 
     ptx::tc_fence_before();
