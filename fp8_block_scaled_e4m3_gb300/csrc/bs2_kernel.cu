@@ -46,6 +46,8 @@
 // One CTA pair per tile (no stream-K); E4M3 C runs on the one-CTA kernel.
 #include "common.cuh"
 
+#include <type_traits>
+
 namespace fp8bs {
 
 constexpr int kBs2Threads = (4 + kEpiWarps) * 32;
@@ -277,7 +279,10 @@ __global__ void __launch_bounds__(kBs2Threads, 1)
             }
             float sb_cur = sbrow && lane < KB ? ptx::ldg_nc_f32(sbrow + lane) : 0.f;
             float sb_next = sbrow && 32 + lane < KB ? ptx::ldg_nc_f32(sbrow + 32 + lane) : 0.f;
-            for (int kb = 0; kb < KB; ++kb, ++it) {
+            // One K block: acc (+)= P_kb * (sa * sb). The tile's first K block is
+            // peeled off the loop and sets the accumulators (an FMA onto zero, no
+            // separate reset), so the loop body stays branch-free.
+            auto kstep = [&](int kb, auto first) -> bool {
                 const float sb = __shfl_sync(0xffffffffu, sb_cur, kb & 31);
                 if ((kb & 31) == 31) {
                     sb_cur = sb_next;
@@ -288,18 +293,15 @@ __global__ void __launch_bounds__(kBs2Threads, 1)
                 const int buf = it % kBs2NBuf;
                 const uint32_t tph = (it / kBs2NBuf) & 1;
                 if (!wait_bounded_warp(tfull_bar(buf), tph, abort_flag, args) ||
-                    !wait_bounded_warp(sa_full_bar(a), aph, abort_flag, args)) {
-                    ok = false;
-                    break;
-                }
+                    !wait_bounded_warp(sa_full_bar(a), aph, abort_flag, args))
+                    return false;
                 ptx::tc_fence_after();
                 const float sa = reinterpret_cast<const float *>(smem + L::OFF_SA + a * L::SA_BYTES)[row];
                 const float scale = sa * sb;
                 const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                                        static_cast<uint32_t>(buf * kBs2BN + wg * HALF);
                 // Two 64-column rounds; the buffer is released once the second
-                // round is loaded. The tile's first K block sets the
-                // accumulators (an FMA onto zero, no separate reset).
+                // round is loaded.
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
                     uint32_t r0[32], r1[32];
@@ -316,23 +318,20 @@ __global__ void __launch_bounds__(kBs2Threads, 1)
                             ptx::mbar_arrive(sa_empty_bar(a));
                         }
                     }
-                    if (kb == 0) {
 #pragma unroll
-                        for (int j = 0; j < 32; ++j)
-                            acc[h * 64 + j] = fmaf(__uint_as_float(r0[j]), scale, 0.f);
+                    for (int j = 0; j < 32; ++j)
+                        acc[h * 64 + j] = fmaf(__uint_as_float(r0[j]), scale, decltype(first)::value ? 0.f : acc[h * 64 + j]);
 #pragma unroll
-                        for (int j = 0; j < 32; ++j)
-                            acc[h * 64 + 32 + j] = fmaf(__uint_as_float(r1[j]), scale, 0.f);
-                    } else {
-#pragma unroll
-                        for (int j = 0; j < 32; ++j)
-                            acc[h * 64 + j] = fmaf(__uint_as_float(r0[j]), scale, acc[h * 64 + j]);
-#pragma unroll
-                        for (int j = 0; j < 32; ++j)
-                            acc[h * 64 + 32 + j] = fmaf(__uint_as_float(r1[j]), scale, acc[h * 64 + 32 + j]);
-                    }
+                    for (int j = 0; j < 32; ++j)
+                        acc[h * 64 + 32 + j] =
+                            fmaf(__uint_as_float(r1[j]), scale, decltype(first)::value ? 0.f : acc[h * 64 + 32 + j]);
                 }
-            }
+                ++it;
+                return true;
+            };
+            ok = kstep(0, std::true_type{});
+            for (int kb = 1; kb < KB && ok; ++kb)
+                ok = kstep(kb, std::false_type{});
             if (!ok)
                 break;
             // Into the tile buffer once the store warp has read out the previous
