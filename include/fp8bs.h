@@ -275,8 +275,8 @@ const char *fp8bs_status_string(int status);
  * host thread launched (0 if none): kind*1000000 + block_n*1000 + stages*100 +
  * raster*10 + schedule; kind 1 = one-CTA blockscale kernel (128 x block_n
  * tiles), 2 = mxfp8 kernel, 3 = CTA-pair blockscale kernel (256 x 256 tiles
- * over two SMs, six stages, one CTA pair per tile: 3256601 / 3256611; chosen
- * for bf16 C when one CTA per tile gives at least four waves of pair tiles),
+ * over two SMs, four stages and a whole-tile C buffer, one CTA pair per tile:
+ * 3256401 / 3256411; chosen for bf16 C with one CTA per tile from M = 2048),
  * 4 = tensor-scale twin (fp8bs_gemm_tensorscale), 5 = CTA-pair
  * mxfp8 kernel (256 x 256 tiles over two SMs), 6 = mxfp8 decode kernel
  * (6128601 only; selectable by fp8bs_set_config_override, never chosen by the
