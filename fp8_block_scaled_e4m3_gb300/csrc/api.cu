@@ -150,11 +150,11 @@ int check_shape(int M, int N, int K)
 }
 
 // Kernel configuration. kind 1: one-CTA blockscale kernel, 2: MXFP8 kernel,
-// 4: tensor-scale twin (the MXFP8 kernel's pipeline with plain fp8 MMAs), 5:
-// CTA-pair MXFP8 kernel (256 x 256 tiles over two SMs), 6: MXFP8 decode kernel.
-// (Kind 3, a CTA-pair blockscale kernel with 256 x 128 tiles, measured slower
-// than kind 1 on every shape and was removed.)
-// sched 1: one CTA per tile; 2: stream-K (256-wide tile of kinds 1, 2 and 4).
+// 3: CTA-pair blockscale kernel (256 x 256 tiles over two SMs), 4: tensor-scale
+// twin (the MXFP8 kernel's pipeline with plain fp8 MMAs), 5: CTA-pair MXFP8
+// kernel (256 x 256 tiles over two SMs), 6: MXFP8 decode kernel.
+// sched 1: one CTA (pair) per tile; 2: stream-K (256-wide tile of kinds 1, 2,
+// 3 and 4).
 struct Config {
     int kind, block_n, stages, raster, sched;
 };
@@ -181,7 +181,7 @@ bool decode_config_id(int id, Config &c)
     if (c.kind == 2 || c.kind == 4)
         return (c.block_n == 256 && c.stages == 4) || (c.block_n == 128 && c.stages == 6);
     if (c.kind == 3)
-        return c.block_n == 256 && c.stages == kBsPairStages && c.sched == 1;
+        return c.block_n == 256 && c.stages == kBsPairStages;
     if (c.kind == 5)
         return c.block_n == 256 && c.stages == kMxPairStages && c.sched == 1;
     if (c.kind == 6)
@@ -236,19 +236,20 @@ long long sk_grid(long long units, long long KB, int num_sms, bool one_row = fal
 constexpr long long kSkMinGainBs = 20;
 constexpr long long kSkMinGainMx = 13;
 
-// Stream-K set-up shared by the one-CTA kernels with a 256-wide tile: the grid,
-// the whole waves run one CTA per tile before the stream-K range (the CTAs of a
-// wave share A and B panels in L2), and the workspace from the stream-ordered
-// pool: one fp32 partial tile and kEpiWarps flags per CTA. Fresh or reused
-// memory never holds this call's token, and finishers reset the flags they
-// consume. The caller frees `ws` on the stream after the launch.
-int setup_stream_k(int tiles, int KB, int num_sms, cudaMemPool_t pool, cudaStream_t s, GemmArgs &args, int &grid,
-                   void *&ws)
+// Stream-K set-up shared by the kernels with a 256-wide tile: the number of
+// workers (`grid`: CTAs, or CTA pairs for the pair kernel, at most `workers`),
+// the whole waves run one worker per tile before the stream-K range (a wave's
+// workers share A and B panels in L2), and the workspace from the stream-ordered
+// pool: one fp32 partial of 128 x 256 and kEpiWarps flags per CTA. Fresh or
+// reused memory never holds this call's token, and finishers reset the flags
+// they consume. The caller frees `ws` on the stream after the launch.
+int setup_stream_k(int tiles, int KB, int workers, cudaMemPool_t pool, cudaStream_t s, GemmArgs &args, int &grid,
+                   void *&ws, int ctas_per_worker = 1)
 {
     const long long units = static_cast<long long>(tiles) * KB;
     if (units >= (1ll << 31) || !pool)
         return FP8BS_ERR_SHAPE;
-    grid = static_cast<int>(sk_grid(units, KB, num_sms, args.M <= 128));
+    grid = static_cast<int>(sk_grid(units, KB, workers, args.M <= 128));
     const int full_waves = tiles / grid;
     args.sk_dp = full_waves >= 2 ? full_waves - 1 : 0;
     // Every CTA must hold at least one unit of the stream-K range: a finisher
@@ -257,13 +258,14 @@ int setup_stream_k(int tiles, int KB, int num_sms, cudaMemPool_t pool, cudaStrea
     // units / 4.)
     if (static_cast<long long>(tiles - args.sk_dp * grid) * KB < grid)
         return FP8BS_ERR_SHAPE;
+    const size_t ctas = static_cast<size_t>(grid) * ctas_per_worker;
     const size_t slot = static_cast<size_t>(kBlockM) * 256 * sizeof(float);
-    const size_t bytes = static_cast<size_t>(grid) * (slot + kEpiWarps * sizeof(unsigned long long));
+    const size_t bytes = ctas * (slot + kEpiWarps * sizeof(unsigned long long));
     if (cudaMallocFromPoolAsync(&ws, bytes, pool, s) != cudaSuccess)
         return FP8BS_ERR_CUDA;
     args.sk = 1;
     args.sk_partial = static_cast<float *>(ws);
-    args.sk_flags = reinterpret_cast<unsigned long long *>(static_cast<char *>(ws) + grid * slot);
+    args.sk_flags = reinterpret_cast<unsigned long long *>(static_cast<char *>(ws) + ctas * slot);
     args.sk_token = g_sk_token.fetch_add(1) + 1;
     return FP8BS_OK;
 }
@@ -355,7 +357,9 @@ Config choose_config(int kind, int M, int N, int K, int num_sms)
     // 225.1 / 229.5 -> 206.5; 16384x7168x3072 318.3 / 316.0 -> 288.5;
     // 8192x8192x3072 191.3 / 188.5 -> 173.9; 4096x65536x1536 396.0 / 405.3 ->
     // 362.1; 4096x2048x7168 71.8 / 63.6 -> 61.8. Stream-K shapes keep the
-    // one-CTA kernel (16384x1536x7168: 149 with stream-K, 162.1 with the pair).
+    // one-CTA kernel; the pair's own stream-K instance (config 3256402/12) is no
+    // faster (us, one session: 16384x1536x7168 153.1 one-CTA stream-K, 152.9
+    // pair stream-K; 4096x2048x7168 pair one per tile 60.4, pair stream-K 67.2).
     if (kind == 1 && c.block_n == 256 && c.sched == 1 && M >= kPairMinM) {
         c.kind = 3;
         c.stages = kBsPairStages;
@@ -615,23 +619,21 @@ int blockscale_gemm(const void *A, const float *a_scale, const void *B, const fl
     args.wait_limit_ns = g_wait_limit_ns.load();
     args.teardown_limit_ns = teardown_limit();
     const int tiles = args.raster.num_tiles();
-    int grid = tiles < st->num_sms ? tiles : st->num_sms;
+    // workers: CTAs, or CTA pairs for the pair kernel
+    const int max_workers = pair ? st->bs_pair_clusters : st->num_sms;
+    int grid = tiles < max_workers ? tiles : max_workers;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (pair) {
-        if (launch_blockscale_pair<kBsPairStages>(tmA, tmB, tmSA, tmC, args, st->bs_pair_clusters, s) != cudaSuccess)
-            return FP8BS_ERR_LAUNCH;
-        t_last_config = config_id(cfg);
-        return FP8BS_OK;
-    }
     void *ws = nullptr;
     if (cfg.sched == 2) {
         if (cfg.block_n != 256)
             return FP8BS_ERR_SHAPE;
-        if ((rc = setup_stream_k(tiles, KB, st->num_sms, st->pool, s, args, grid, ws)))
+        if ((rc = setup_stream_k(tiles, KB, max_workers, st->pool, s, args, grid, ws, pair ? 2 : 1)))
             return rc;
     }
     cudaError_t e;
-    if (cfg.block_n == 256 && cfg.stages == 3)
+    if (pair)
+        e = launch_blockscale_pair<kBsPairStages>(tmA, tmB, tmSA, tmC, args, grid, s);
+    else if (cfg.block_n == 256 && cfg.stages == 3)
         e = launch_blockscale<256, 3>(tmA, tmB, tmSA, tmC, args, grid, s);
     else if (cfg.block_n == 256)
         e = launch_blockscale<256, 4>(tmA, tmB, tmSA, tmC, args, grid, s);

@@ -132,23 +132,29 @@ __device__ __forceinline__ int launch_tiles(const GemmArgs &a)
         return a.raster.num_tiles();
 }
 
-// The work of one CTA as flattened steps g = 0 .. total-1, step g being K block
-// kb of tile t (tile order of TileRaster).
-//   sk == 0: one CTA per tile, tiles blockIdx.x, blockIdx.x + gridDim.x, ...
-//   sk != 0: stream-K after sk_dp whole waves done one CTA per tile (so that a
-//            wave's CTAs share operand panels in L2). The units u = t' * KB + kb
-//            of the remaining tiles t' are cut into gridDim.x contiguous ranges
-//            equal to one unit; CTA c takes [u_c, u_c+1), u_c = floor(c * U /
-//            gridDim.x). A tile cut between CTAs is finished (scaled partials
-//            added, C stored) by the CTA that holds its K block 0, which is that
-//            CTA's last segment; the CTAs after it write their partials at the
-//            start of their range, so the finisher never waits in practice.
-struct WorkSpan {
+// The work of one worker (a CTA, or a cluster of CTAS consecutive CTAs that
+// share each tile) as flattened steps g = 0 .. total-1, step g being K block kb
+// of tile t (tile order of TileRaster). c = blockIdx.x / CTAS is the worker and
+// G = gridDim.x / CTAS the number of workers.
+//   sk == 0: one worker per tile, tiles c, c + G, ...
+//   sk != 0: stream-K after sk_dp whole waves done one worker per tile (so that
+//            a wave's workers share operand panels in L2). The units u = t' * KB
+//            + kb of the remaining tiles t' are cut into G contiguous ranges
+//            equal to one unit; worker c takes [u_c, u_c+1), u_c = floor(c * U /
+//            G). A tile cut between workers is finished (scaled partials added,
+//            C stored) by the worker that holds its K block 0, which is that
+//            worker's last segment; the workers after it write their partials at
+//            the start of their range, so the finisher never waits in practice.
+template <int CTAS>
+struct WorkSpanT {
     int u0;         // first stream-K unit (tiles * KB < 2^31 is checked by the host)
-    int total;      // steps of this CTA
-    int dp_steps;   // steps done one CTA per tile, before the stream-K range (all of them without stream-K)
+    int total;      // steps of this worker
+    int dp_steps;   // steps done one worker per tile, before the stream-K range (all of them without stream-K)
     int tile0;      // first tile of the stream-K range
     int KB;
+
+    __device__ __forceinline__ static int worker() { return static_cast<int>(blockIdx.x) / CTAS; }
+    __device__ __forceinline__ static int workers() { return static_cast<int>(gridDim.x) / CTAS; }
 
     __device__ __forceinline__ static int unit_begin(int U, int c, int G)
     {
@@ -160,8 +166,8 @@ struct WorkSpan {
     __device__ __forceinline__ void init(const GemmArgs &a, int KB_, int tiles)
     {
         KB = KB_;
-        const int c = static_cast<int>(blockIdx.x);
-        const int G = static_cast<int>(gridDim.x);
+        const int c = worker();
+        const int G = workers();
         if (a.sk) {
             dp_steps = a.sk_dp * KB;
             tile0 = a.sk_dp * G;
@@ -185,7 +191,7 @@ struct WorkSpan {
             t += tile0;
         } else {
             const int i = g / KB;
-            t = static_cast<int>(blockIdx.x) + i * static_cast<int>(gridDim.x);
+            t = worker() + i * workers();
             kb = g - i * KB;
         }
     }
@@ -198,10 +204,22 @@ struct WorkSpan {
             if (g >= dp_steps)
                 step(g, t, kb);   // into or inside the stream-K range
             else
-                t += static_cast<int>(gridDim.x);
+                t += workers();
         }
     }
+
+    // The last worker holding a unit of stream-K tile t: the largest c with
+    // floor(c * U / G) <= the tile's last unit.
+    __device__ __forceinline__ int last_worker(int tiles, int t) const
+    {
+        const long long G = workers();
+        const long long U = static_cast<long long>(tiles - tile0) * KB;
+        const long long tile_end = static_cast<long long>(t + 1 - tile0) * KB;
+        return static_cast<int>((tile_end * G - 1) / U);
+    }
 };
+
+using WorkSpan = WorkSpanT<1>;
 
 // Byte offset of (row r in 0..127, group j in 0..3) in a 512-byte scale-factor
 // atom: 32 rows of 16 bytes, row (r % 32) holds rows r%32, r%32+32, r%32+64,
@@ -279,6 +297,25 @@ __device__ __forceinline__ bool sk_wait_flag(const unsigned long long *flag, uns
         }
     }
     return __all_sync(0xffffffffu, got);
+}
+
+// The same wait for one thread (no warp vote).
+__device__ __forceinline__ bool sk_wait_flag_thread(const unsigned long long *flag, unsigned long long token,
+                                                    volatile int *abort_flag, const GemmArgs &a)
+{
+    if (ptx::ld_acquire_gpu_u64(flag) == token)
+        return true;
+    const uint64_t t0 = ptx::globaltimer();
+    while (ptx::ld_acquire_gpu_u64(flag) != token) {
+        if (*abort_flag)
+            return false;
+        if (ptx::globaltimer() - t0 > a.wait_limit_ns) {
+            *abort_flag = 1;
+            atomicExch(a.status, kStatusTimeout);
+            return false;
+        }
+    }
+    return true;
 }
 
 // Store one epilogue warp's 32 rows x 32 columns of C (row = lane) with one

@@ -275,8 +275,10 @@ const char *fp8bs_status_string(int status);
  * host thread launched (0 if none): kind*1000000 + block_n*1000 + stages*100 +
  * raster*10 + schedule; kind 1 = one-CTA blockscale kernel (128 x block_n
  * tiles), 2 = mxfp8 kernel, 3 = CTA-pair blockscale kernel (256 x 256 tiles
- * over two SMs, four stages and a whole-tile C buffer, one CTA pair per tile:
- * 3256401 / 3256411; chosen for bf16 C with one CTA per tile from M = 2048),
+ * over two SMs, four stages and a whole-tile C buffer: 3256401 / 3256411 one
+ * CTA pair per tile, chosen for bf16 C with one CTA per tile from M = 2048;
+ * 3256402 / 3256412 stream-K with the pair as the worker, bf16 C only,
+ * selectable by fp8bs_set_config_override, never chosen by the shape rule),
  * 4 = tensor-scale twin (fp8bs_gemm_tensorscale), 5 = CTA-pair
  * mxfp8 kernel (256 x 256 tiles over two SMs), 6 = mxfp8 decode kernel
  * (6128601 only; selectable by fp8bs_set_config_override, never chosen by the
@@ -285,7 +287,7 @@ const char *fp8bs_status_string(int status);
  * distributed shared memory, in slice order, so the result is the same on
  * every call; a shape it does not take (M > 128, K > 6144, an E4M3 C) runs the
  * one-CTA 128-wide kernel and reports 2128601); schedule 1 = one CTA per tile,
- * 2 = stream-K (kinds 1, 2 and 4 with block_n 256, and kind 2 with block_n 128). */
+ * 2 = stream-K (kinds 1, 2, 3 and 4 with block_n 256, and kind 2 with block_n 128). */
 int fp8bs_last_config_id(void);
 /* Release what the library holds per device: waits for each device it set
  * up (cudaDeviceSynchronize), destroys its stream-ordered workspace pool and

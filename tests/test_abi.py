@@ -168,7 +168,9 @@ def test_config_selection(lib):
     assert L.fp8bs_set_config_override(4128612) == -3
     assert L.fp8bs_set_config_override(3256411) == 0       # the blockscale CTA-pair kernel: 256 x 256, four stages
     assert lib.decode_config(3256411)["kind"] == "blockscale_pair"
-    for bad in (3128811, 3256611, 3256311, 3256412):       # no other tile, stage count or schedule
+    assert L.fp8bs_set_config_override(3256412) == 0       # ... with the stream-K schedule
+    assert lib.decode_config(3256412)["schedule"] == "stream_k"
+    for bad in (3128811, 3256611, 3256311, 3256413):       # no other tile, stage count or schedule
         assert L.fp8bs_set_config_override(bad) == -3
     assert L.fp8bs_set_config_override(1256413) == -3      # no such schedule
     assert L.fp8bs_set_config_override(1128612) == -3      # stream-K runs with the 256-wide tile only

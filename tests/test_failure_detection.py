@@ -30,7 +30,7 @@ def _call(kind, x):
     returns its output tensor."""
     import torch
     import fp8_block_scaled_e4m3_gb300 as f
-    if kind in ("bs", "bs_sk", "bs_pair", "e4m3"):
+    if kind in ("bs", "bs_sk", "bs_pair", "bs_pair_sk", "e4m3"):
         d = (to_dev(x.A), to_dev(workloads.a_scale_to_kmajor(x.a_scale)), to_dev(x.B), to_dev(x.b_scale))
         if kind == "e4m3":
             return lambda: f.gemm_blockscale_e4m3out(*d, 8.0)
@@ -48,10 +48,10 @@ def _call(kind, x):
     return moe
 
 
-OVERRIDE = {"bs_sk": 1256402, "bs_pair": 3256401, "mx_sk": 2256402, "mx_pair": 5256601, "mx_decode": 6128601}
+OVERRIDE = {"bs_sk": 1256402, "bs_pair": 3256401, "bs_pair_sk": 3256402, "mx_sk": 2256402, "mx_pair": 5256601, "mx_decode": 6128601}
 
 
-@pytest.mark.parametrize("kind", ["bs", "bs_sk", "bs_pair", "e4m3", "mx", "mx_sk", "mx_pair", "mx_decode", "twin", "moe"])
+@pytest.mark.parametrize("kind", ["bs", "bs_sk", "bs_pair", "bs_pair_sk", "e4m3", "mx", "mx_sk", "mx_pair", "mx_decode", "twin", "moe"])
 def test_every_path_reports_a_timeout_and_recovers(kind):
     """Stream-K included: a CTA that gives up never publishes its partial, and
     the finishers waiting for it run out of time as well instead of hanging.

@@ -179,8 +179,8 @@ def test_pack_a_scale_bit_exact():
 
 # every built kernel configuration, forced through the override
 # one-CTA 128x256, 128x128 (one CTA per tile), 128x256 stream-K, three-stage
-# 128x256 (both schedules), CTA-pair 256x256
-BS_CONFIGS = [1256411, 1128611, 1256412, 1256311, 1256312, 3256411]
+# 128x256 (both schedules), CTA-pair 256x256 (both schedules)
+BS_CONFIGS = [1256411, 1128611, 1256412, 1256311, 1256312, 3256411, 3256412]
 MX_CONFIGS = [2256411, 2128611, 2256412, 2128612, 5256611]
 
 
@@ -313,15 +313,21 @@ def test_full_mxfp8(M, N, K, seed):
     _check_full_size("mx", M, N, K, seed)
 
 
-@pytest.mark.parametrize("M,N,K", [(4096, 2048, 7168), (1000, 2824, 1408), (384, 256, 128), (4096, 5120, 384)])
-def test_blockscale_pair_kernel_full_output(override, M, N, K):
+@pytest.mark.parametrize("sched", [1, 2])
+@pytest.mark.parametrize("M,N,K", [(4096, 2048, 7168), (1000, 2824, 1408), (384, 256, 128), (4096, 5120, 384),
+                                   (512, 512, 8192), (600, 520, 4096)])
+def test_blockscale_pair_kernel_full_output(override, M, N, K, sched):
     """The CTA-pair kernel (256 x 256 tiles, whole-tile C buffer) on the whole
-    of C: the full-size narrow-N workload; ragged shapes whose last pair tile
-    is cut in M (the odd CTA's rows past M) and in N (a 128-column half past
-    N); and a shape with several tiles per CTA pair and few K blocks (the tile
-    buffer's reuse across tiles)."""
+    of C, one pair per tile and stream-K: the full-size narrow-N workload;
+    ragged shapes whose last pair tile is cut in M (the odd CTA's rows past M)
+    and in N (a 128-column half past N); a shape with several tiles per CTA
+    pair and few K blocks (the tile buffer's reuse across tiles; under
+    stream-K, whole waves first and then tiles of three K blocks cut between
+    pairs); and, under stream-K, tiles whose K blocks are cut between four
+    pairs, so that a finisher adds three partials, with every row of the odd
+    CTA of the last M tile past M (no hand-off for those warps)."""
     import fp8_block_scaled_e4m3_gb300 as f
-    cid = 3256401 + 10 * (1 if M >= N else 0)
+    cid = 3256400 + 10 * (1 if M >= N else 0) + sched
     override(cid)
     x = workloads.make_blockscale_inputs(M, N, K, seed=M + N)
     got = run_blockscale(x.A, x.a_scale, x.B, x.b_scale)
