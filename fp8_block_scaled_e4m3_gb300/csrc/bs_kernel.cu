@@ -98,13 +98,19 @@ struct BsLayout {
     static_assert(BN == 128 || BN == 256, "tile width");
 };
 
-template <int BN, int STAGES, bool MOE>
+// SK: the stream-K instance (256-wide dense tile only). The hand-off lives in
+// its own instance: compiled into the one-CTA-per-tile instance, where it never
+// runs, it made that instance 2-7% slower (4096x2048x7168 63.3 -> 59.1 us
+// without it, 4096x65536x1536 406 -> 387 us, 16384x7168x768 at three stages
+// 106.3 -> 102.6 us; same bits).
+template <int BN, int STAGES, bool MOE, bool SK>
 __global__ void __launch_bounds__(kBsThreads, 1)
     fp8bs_blockscale_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                             const __grid_constant__ CUtensorMap tmSA, const __grid_constant__ CUtensorMap tmC,
                             const GemmArgs args)
 {
     using L = BsLayout<BN, STAGES>;
+    static_assert(!SK || (BN == 256 && !MOE), "stream-K runs with the dense 256-wide tile");
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_s = ptx::smem_u32(smem_raw);
     const uint32_t sbase = (raw_s + 1023u) & ~1023u;
@@ -305,7 +311,7 @@ __global__ void __launch_bounds__(kBsThreads, 1)
         constexpr int kChunk = 16;                   // columns per TMEM load (narrow tile)
         constexpr int NCH = HALF / kChunk;
         constexpr bool kEarlyRelease = HALF <= 64;   // the slice fits next to the accumulator
-        constexpr bool kSk = BN == 256;              // tile width with the stream-K hand-off
+        constexpr bool kSk = SK;                     // the instance with the stream-K hand-off
         static_assert(HALF % kCChunkCols == 0, "epilogue chunking");
         const int ew = warp - 4;                     // 0..7
         const int wg = ew >> 2;                      // column half
@@ -528,7 +534,9 @@ cudaError_t launch_blockscale_any(const CUtensorMap &tmA, const CUtensorMap &tmB
                                   const CUtensorMap &tmC, const GemmArgs &args, int grid, cudaStream_t stream)
 {
     using L = BsLayout<BN, STAGES>;
-    auto kern = fp8bs_blockscale_kernel<BN, STAGES, MOE>;
+    constexpr bool kCanSk = BN == 256 && !MOE;
+    auto kern = kCanSk && args.sk ? fp8bs_blockscale_kernel<BN, STAGES, MOE, kCanSk>
+                                  : fp8bs_blockscale_kernel<BN, STAGES, MOE, false>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::DYN_SMEM);
     if (e != cudaSuccess)
         return e;
