@@ -806,7 +806,7 @@ def test_random_shapes_every_entry_point(override, M, N, K):
     raster = 1 if M >= N else 0
     x = workloads.make_blockscale_inputs(M, N, K, seed=M * 31 + N * 7 + K)
     want = oracle.blockscale(x.A, x.a_scale, x.B, x.b_scale)
-    for cfg in (0, 1256401, 1128601, 1256402):
+    for cfg in (0, 1256401, 1128601, 1256402, 3256401, 3256402):
         if cfg:
             override(cfg + raster * 10)
         compare(run_blockscale(x.A, x.a_scale, x.B, x.b_scale), want, f"bs cfg {cfg} {M}x{N}x{K}")
@@ -831,6 +831,42 @@ def test_random_shapes_every_entry_point(override, M, N, K):
         s = _c_scale(x)
         codes, yv = oracle.blockscale_e4m3out(x.A, x.a_scale, x.B, x.b_scale, s)
         compare_e4m3(_run_e4m3out(x, s), codes, yv, s, f"bs e4m3 {M}x{N}x{K}")
+
+
+def _finite_codes(rng, shape):
+    """Uniformly random E4M3 codes over all 254 finite encodings: both zeros,
+    every subnormal, every normal up to +-448 (0x7F and 0xFF, the NaNs, skipped)."""
+    r = rng.integers(0, 254, size=shape)
+    return (r + (r >= 0x7F)).astype(np.uint8)
+
+
+@pytest.mark.parametrize("M,N,K", [(200, 136, 384), (300, 520, 1280)])
+def test_uniform_random_codes_every_entry_point(override, M, N, K):
+    """The whole E4M3 code range on the GPU: uniformly random finite codes on
+    both operands (subnormals and +-448 included), with scales near 2^-9 per
+    side so that C is O(1) and the absolute term of the tolerance matters;
+    tail shapes, through every blockscale and MXFP8 kernel."""
+    rng = np.random.Generator(np.random.PCG64(M * 7 + N + K))
+    A = _finite_codes(rng, (M, K))
+    B = _finite_codes(rng, (N, K))
+    sa = (rng.uniform(0.5, 1.0, size=(M, K // 128)) * 2.0 ** -9).astype(np.float32)
+    sb = (rng.uniform(0.5, 1.0, size=((N + 127) // 128, K // 128)) * 2.0 ** -9).astype(np.float32)
+    want = oracle.blockscale(A, sa, B, sb)
+    assert np.abs(oracle.bf16_bits_to_float(want)).max() > 1.0   # O(1) outputs, not all below the tolerance
+    raster = 1 if M >= N else 0
+    for cfg in (0, 1256401, 1128601, 1256402, 1256301, 3256401, 3256402):
+        if cfg:
+            override(cfg + raster * 10)
+        compare(run_blockscale(A, sa, B, sb), want, f"bs codes cfg {cfg} {M}x{N}x{K}")
+    override(0)
+    ea = rng.integers(117, 120, size=(M, K // 32)).astype(np.uint8)   # 2^-10 .. 2^-8
+    eb = rng.integers(117, 120, size=(N, K // 32)).astype(np.uint8)
+    want_mx = oracle.mxfp8(A, ea, B, eb)
+    for cfg in (0, 2256401, 2128601, 2256402, 5256601):
+        if cfg:
+            override(cfg + raster * 10)
+        compare(run_mxfp8(A, ea, B, eb), want_mx, f"mx codes cfg {cfg} {M}x{N}x{K}")
+    override(0)
 
 
 # ------------------------------------------------ size limits
